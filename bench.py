@@ -1,0 +1,436 @@
+#!/usr/bin/env python3
+"""Benchmark of one routed MoE layer (route -> bucket -> MXFP4 SwiGLU expert FFN
+-> combine) on GB300, through the k3moe C ABI.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode] [--impl k3moe|reference]
+
+A step is one whole MoE layer over one batch of synthetic input (the default
+workload: 1 token, H=7168, I=2048, 896 experts, top-16, all 21 GB of MXFP4
+weights resident in HBM).  Steps rotate over --sets input sets (different
+tokens, so different experts) and a 256 MiB buffer is written between timed
+steps to flush L2.  Prints one JSON line (rank 0).  With N>1 (torchrun) each
+rank runs an independent replica on its own GPU (no collectives on the data
+path); value = tokens of all ranks / the slowest rank's time.
+
+--impl reference times the float64 C oracle on the host's cores instead."""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import gen  # noqa: E402
+
+METRIC = "MoE-layer tokens/s + achieved HBM GB/s (decode), FP4 TFLOPS (prefill)"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--config", default="decode", choices=sorted(gen.CONFIGS))
+    p.add_argument("--impl", default="k3moe", choices=["k3moe", "reference"])
+    p.add_argument("--mode", type=int, default=0, help="expert FFN mode (0 auto, 1 gemv)")
+    p.add_argument("--sets", type=int, default=64, help="rotating input sets")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle sample budget")
+    return p.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def expert_bytes(s) -> int:
+    """Packed MXFP4 bytes of one expert: 3 matrices x H*I x (1/2 code + 1/32 scale)."""
+    return 3 * s.H * s.I * 17 // 32
+
+
+def input_set(name, s, i):
+    seed = gen.INPUT_SEED + 1000 * i
+    return gen.make_logits(name, s, seed=seed), gen.make_x(s, seed=seed)
+
+
+def routed_experts(s, logits):
+    """Expert ids each token picks (top-k by logit, ties to the lower index).
+    Used only to size the reported byte counts."""
+    order = np.lexsort((np.broadcast_to(np.arange(s.E), logits.shape), -logits.astype(np.float64)), axis=1)
+    return order[:, : s.k]
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.path = os.path.join(ROOT, "gpurun_out", f".clocks_{os.getpid()}.csv")
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        self.gpu = gpu_index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[5:]))
+            except Exception:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        lo, hi = (self.t0 or 0) - 1.0, (self.t1 or 1e18) + 1.0
+        sel = [r for r in rows if lo <= r[0] <= hi] or rows
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in sel:
+            for n, v in zip(names[1:], r[3][1:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median([r[1] for r in sel])), "sm_max_mhz": max(r[2] for r in sel),
+                "reasons": sorted(reasons), "samples": len(sel)}
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        return None
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "mxfp4_expert_ffn_router_gb300", "csrc", "*"))):
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(config: str):
+    """DRAM bytes per launch of the expert FFN from the committed ncu summary, or
+    None when the kernels changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        d = json.load(open(path))
+    except Exception:
+        return None
+    ent = d.get(config)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_call")
+
+
+# ----------------------------------------------------------------------------- oracle
+def oracle_sample(name, s, sets, budget_s):
+    """Time the float64 oracle on whole layers of the first input sets (decode-
+    sized workloads) or on a token sample (prefill), within ~budget_s seconds."""
+    import oracle
+    t_tokens, t_sec, n = 0, 0.0, 0
+    if s.T <= 8:
+        for logits, xbits in sets:
+            ids = np.unique(routed_experts(s, logits))
+            W = oracle.Weights(s.E, {int(e): tuple(z[0] for z in gen.expert_arrays(s.H, s.I, int(e), int(e) + 1))
+                                     for e in ids})
+            t = time.perf_counter()
+            oracle.moe_layer(s, logits, xbits, W)
+            t_sec += time.perf_counter() - t
+            t_tokens += s.T
+            n += 1
+            if t_sec >= budget_s:
+                break
+        return t_tokens / t_sec, f"{n} whole layers of {s.T} token(s) ({name}), 1 thread"
+    logits, xbits = sets[0]
+    t = time.perf_counter()
+    idx, w, _ = oracle.route(s, logits)
+    oracle.bucket(s, idx)
+    t_rb = time.perf_counter() - t
+    cache = {}
+    for tok in range(s.T):
+        for e in idx[tok]:
+            if int(e) not in cache:
+                cache[int(e)] = tuple(z[0] for z in gen.expert_arrays(s.H, s.I, int(e), int(e) + 1))
+        W = oracle.Weights(s.E, {int(e): cache[int(e)] for e in idx[tok]})
+        t = time.perf_counter()
+        oracle.moe_token(s, xbits[tok], idx[tok], w[tok], W)
+        t_sec += time.perf_counter() - t
+        n += 1
+        if t_sec >= budget_s:
+            break
+    per_tok = t_sec / n + t_rb / s.T
+    return 1.0 / per_tok, (f"route+bucket of all {s.T} tokens plus the FFN+combine of {n} tokens "
+                           f"({name}), 1 thread")
+
+
+def run_reference(a):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    s = gen.CONFIGS[a.config]
+    nsets = max(1, min(a.sets, a.steps + a.warmup)) if s.T <= 8 else 1
+    sets = [input_set(a.config, s, i) for i in range(nsets)]
+    import oracle
+    cache = {}
+
+    def weights_for(logits):
+        ids = [int(e) for e in np.unique(routed_experts(s, logits))]
+        for e in ids:
+            if e not in cache:
+                cache[e] = tuple(z[0] for z in gen.expert_arrays(s.H, s.I, e, e + 1))
+        return oracle.Weights(s.E, {e: cache[e] for e in ids})
+
+    def one_step(i):
+        logits, xbits = sets[i % len(sets)]
+        if s.T <= 8:
+            W = weights_for(logits)
+            t = time.perf_counter()
+            oracle.moe_layer(s, logits, xbits, W)
+            return time.perf_counter() - t, s.T
+        # prefill-sized: one step = route+bucket of all tokens + FFN of 2 tokens (bounded sample)
+        t = time.perf_counter()
+        idx, w, _ = oracle.route(s, logits)
+        oracle.bucket(s, idx)
+        rb = time.perf_counter() - t
+        tok = i % s.T
+        W = weights_for(logits[tok:tok + 1])
+        t = time.perf_counter()
+        oracle.moe_token(s, xbits[tok], idx[tok], w[tok], W)
+        ffn = time.perf_counter() - t
+        return rb / s.T + ffn, 1
+
+    for i in range(a.warmup):
+        one_step(i)
+    tot, toks = 0.0, 0
+    for i in range(a.steps):
+        dt, nt = one_step(a.warmup + i)
+        tot += dt
+        toks += nt
+    value = toks / tot
+    sample = (f"{a.steps} whole layers of {s.T} token(s)" if s.T <= 8 else
+              f"{a.steps} steps of route+bucket (amortised per token) plus one token's FFN+combine")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": 1e3 * tot / a.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(a, s),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(a, s):
+    return {"workload": f"{a.config}: T={s.T} tokens, H={s.H}, I={s.I}, E={s.E}, top-{s.k}, "
+                        f"MXFP4 experts resident",
+            "tokens": s.T, "hidden": s.H, "intermediate": s.I, "experts": s.E, "top_k": s.k,
+            "l2": f"{L2_FLUSH_BYTES >> 20} MiB buffer written between timed steps; inputs rotate over "
+                  f"{a.sets} sets", "parallelism": f"replicas x{a.gpus}"}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_gpu(a):
+    import torch
+
+    import mxfp4_expert_ffn_router_gb300 as k3
+    from gen.device import DeviceExperts
+    from mxfp4_expert_ffn_router_gb300 import build as k3build
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if rank == 0:
+        k3build.build()
+    if ws > 1:
+        dist.barrier()
+    s = gen.CONFIGS[a.config]
+    A = s.T * s.k
+    nsets = max(1, a.sets)
+    sets = [input_set(a.config, s, i) for i in range(nsets)]
+    experts = DeviceExperts(s.H, s.I, s.E, device=dev)
+    W = k3.Weights.from_stacked(*experts.tensors)
+    logits_d = [torch.from_numpy(l).to(dev) for l, _ in sets]
+    x_d = [torch.from_numpy(x.view(np.int16)).to(dev) for _, x in sets]
+    uniq = [len(np.unique(routed_experts(s, l))) for l, _ in sets]
+    i32, f32 = torch.int32, torch.float32
+    st = torch.zeros(1, dtype=i32, device=dev)
+    idx = torch.empty((s.T, s.k), dtype=i32, device=dev)
+    w = torch.empty((s.T, s.k), dtype=f32, device=dev)
+    counts = torch.empty(s.E, dtype=i32, device=dev)
+    offsets = torch.empty(s.E + 1, dtype=i32, device=dev)
+    perm = torch.empty(A, dtype=i32, device=dev)
+    inv = torch.empty(A, dtype=i32, device=dev)
+    wsb = torch.empty(max(1, k3.k3moe_workspace_bytes(s, k3.K3MOE_OP_BUCKET)), dtype=torch.uint8, device=dev)
+    wsf = torch.empty(max(1, k3.k3moe_workspace_bytes(s, k3.K3MOE_OP_EXPERT_FFN, a.mode)), dtype=torch.uint8,
+                      device=dev)
+    Y = torch.empty((A, s.H), dtype=f32, device=dev)
+    out = torch.empty((s.T, s.H), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    launches_per_step = 1 + (1 if A <= 4096 else 3) + 3 + 1
+
+    def layer(i, ev=None):
+        j = i % nsets
+        if ev is not None:
+            ev[0].record(stream)
+        k3.k3moe_route(s, logits_d[j], idx, w, st, stream=stream)
+        k3.k3moe_bucket(s, idx, counts, offsets, perm, inv, wsb, st, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        k3.k3moe_expert_ffn(s, x_d[j], W, offsets, perm, Y, a.mode, wsf, st, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        k3.k3moe_combine(s, Y, w, inv, out, None, stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for i in range(a.warmup):
+        flush.fill_(i & 0xFF)
+        layer(i)
+    torch.cuda.synchronize()
+    if int(st.item()) != 0:
+        raise RuntimeError(f"device status {int(st.item())} during warm-up")
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(a.steps)]
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    time.sleep(0.3)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.mark("t0")
+    t_wall = time.perf_counter()
+    for i in range(a.steps):
+        flush.fill_((i + 1) & 0xFF)
+        layer(a.warmup + i, evs[i])
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    clocks.mark("t1")
+    if ws > 1:
+        dist.barrier()
+    time.sleep(0.2)
+    clk = clocks.stop()
+    step_ms = np.array([e[0].elapsed_time(e[3]) for e in evs])
+    ffn_ms = np.array([e[1].elapsed_time(e[2]) for e in evs])
+    tot_ms = float(step_ms.sum())
+    if ws > 1:
+        t = torch.tensor([tot_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot_ms = float(t.item())
+    value = ws * s.T * a.steps / (tot_ms / 1e3)
+    # algorithmic bytes of the expert FFN per call: touched experts' codes+scales,
+    # x read, h written and read (bf16), Y written (fp32)
+    be = expert_bytes(s)
+    ffn_bytes = np.array([uniq[(a.warmup + i) % nsets] * be for i in range(a.steps)], dtype=np.float64)
+    ffn_bytes += s.T * s.H * 2 + A * s.I * 4 + A * s.H * 4
+    achieved = float(ffn_bytes.sum() / (ffn_ms.sum() / 1e3) / 1e9)
+    peaks = measured_peaks()
+    if peaks and "hbm_gbs" in peaks:
+        peak, peak_src = float(peaks["hbm_gbs"]), "measured"
+    else:
+        peak, peak_src = 6800.0, "fallback"
+    roof = {"bound": "hbm", "kernel": "k3moe_expert_ffn (ffn_prep + ffn_gateup + ffn_down)",
+            "achieved": achieved, "peak": peak, "peak_source": peak_src, "unit": "GB/s",
+            "frac": achieved / peak, "traffic": recorded_traffic(a.config),
+            "bytes_per_call": float(ffn_bytes.mean()), "ffn_us_median": float(np.median(ffn_ms) * 1e3)}
+
+    # ------------------------------------------------------------- end to end (host buffers)
+    e2e = None
+    if not a.no_e2e:
+        lg_h = [torch.from_numpy(l).pin_memory() for l, _ in sets]
+        x_h = [torch.from_numpy(x.view(np.int16)).pin_memory() for _, x in sets]
+        out_h = torch.empty((s.T, s.H), dtype=torch.bfloat16).pin_memory()
+        lg_dev = torch.empty_like(logits_d[0])
+        x_dev = torch.empty_like(x_d[0])
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_e2e = max(1, min(a.steps, 500))
+        tot = 0.0
+        for i in range(n_e2e + 3):
+            j = i % nsets
+            flush.fill_(i & 0xFF)
+            ev0.record(stream)
+            lg_dev.copy_(lg_h[j], non_blocking=True)
+            x_dev.copy_(x_h[j], non_blocking=True)
+            k3.k3moe_route(s, lg_dev, idx, w, st, stream=stream)
+            k3.k3moe_bucket(s, idx, counts, offsets, perm, inv, wsb, st, stream=stream)
+            k3.k3moe_expert_ffn(s, x_dev, W, offsets, perm, Y, a.mode, wsf, st, stream=stream)
+            k3.k3moe_combine(s, Y, w, inv, out, None, stream=stream)
+            out_h.copy_(out, non_blocking=True)
+            ev1.record(stream)
+            ev1.synchronize()
+            if i >= 3:
+                tot += ev0.elapsed_time(ev1)
+        e2e_val = s.T * n_e2e / (tot / 1e3)
+        if ws > 1:
+            t = torch.tensor([tot], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_val = ws * s.T * n_e2e / (float(t.item()) / 1e3)
+        e2e = {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": s.T * s.E * 4 + s.T * s.H * 2,
+               "d2h_bytes_per_step": s.T * s.H * 2, "steps": n_e2e}
+
+    cpu = None
+    if rank == 0 and not a.no_cpu_baseline:
+        v, sample = oracle_sample(a.config, s, sets, a.cpu_seconds)
+        cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample}
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": a.steps,
+                "warmup": a.warmup, "ms_per_step": tot_ms / a.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "e2m1*bf16->f32",
+                "data": "synthetic", "config": workload_config(a, s),
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+                "gpu_launches": launches_per_step * a.steps,
+                "step_us": {"median": float(np.median(step_ms) * 1e3), "min": float(step_ms.min() * 1e3),
+                            "max": float(step_ms.max() * 1e3)},
+                "wall_s_timed_region": t_wall}
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_gpu(a)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,152 @@
+/* k3moe.h -- C ABI of the GB300 (sm_103a) routed MoE expert FFN with MXFP4 experts.
+ *
+ * One MoE layer is four calls, each a set of hand-written CUDA kernels launched
+ * on the caller's stream:
+ *
+ *   k3moe_route       router logits -> top-k experts and routing weights
+ *   k3moe_bucket      assignments -> expert-major order (counts, offsets, perm, inv)
+ *   k3moe_expert_ffn  MXFP4 SwiGLU expert FFN over the bucketed assignments
+ *   k3moe_combine     routing-weighted sum of each token's k expert outputs
+ *
+ * The operation follows the kimi-k3-in-c engine as described by its CHANGELOG
+ * walkthrough (m.qwbw.cn): "[0.1.0] Added" (896 routed experts, top-16
+ * selection, a gated-linear-unit expert, native MXFP4 expert weights, a matmul
+ * that reads the packed nibbles directly and never materialises a dequantised
+ * expert), "[1.0.0] Added" (chunk-union prefill: the tokens of a chunk are
+ * grouped by routed expert so each unique expert's weights are read once, with
+ * results identical to the per-token path) and "[Unreleased] Fixed" (an expert
+ * that fails to load contributes zero, never uninitialised memory); and by the
+ * article "kimi-k3-in-c: pure C99 Kimi K3 inference engine" (chenxutan.com),
+ * section "01" (896 experts per layer, 16 woken per token).  MXFP4 is the OCP
+ * Microscaling v1.0 format: E2M1 4-bit elements, one E8M0 scale per 32.
+ *
+ * Conventions for every call:
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    allocates no device memory, never synchronises the host, and launches
+ *    only on `stream` (NULL = the legacy default stream).
+ *  - Row-major, densely packed layouts as documented per argument.
+ *  - Host-detectable errors (NULL required pointer, bad shape, misalignment,
+ *    short workspace, wrong GPU) return a negative k3moe_status and launch
+ *    nothing.  A launch failure returns K3MOE_ERR_LAUNCH.
+ *  - Conditions found on the device are OR-ed as K3MOE_DEV_* bits into the
+ *    caller's int32 `dev_status` word (device memory; zero it beforehand and
+ *    read it after synchronising).
+ *  - Outputs are overwritten, never accumulated into.  T = 0 is valid (no work).
+ *  - Results are deterministic: the same inputs give bitwise the same outputs.
+ */
+#ifndef K3MOE_H
+#define K3MOE_H
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *k3moe_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  K3MOE_OK = 0,
+  K3MOE_ERR_ARG = -1,         /* NULL required pointer or bad enum value         */
+  K3MOE_ERR_SHAPE = -2,       /* shape outside the supported range               */
+  K3MOE_ERR_ALIGN = -3,       /* pointer not 16-byte aligned                     */
+  K3MOE_ERR_WORKSPACE = -4,   /* workspace NULL or smaller than required         */
+  K3MOE_ERR_ARCH = -5,        /* current device is not compute capability 10.3   */
+  K3MOE_ERR_LAUNCH = -6,      /* a CUDA launch failed                            */
+  K3MOE_ERR_UNSUPPORTED = -7  /* valid request this build cannot serve           */
+} k3moe_status;
+
+/* Device-side status bits (OR-ed into *dev_status). */
+#define K3MOE_DEV_NONFINITE 1 /* a router logit row contained NaN                 */
+#define K3MOE_DEV_BOUNDS 2    /* an index read from device memory was out of range */
+#define K3MOE_DEV_TIMEOUT 4   /* a bounded device-side wait gave up               */
+
+/* T tokens, H hidden size, I expert intermediate size, E experts, k experts per
+ * token.  Supported: 0 <= T, 1 <= k <= min(E, 32), E <= 4096, H and I multiples
+ * of 32 in [32, 16384], T*k < 2^31. */
+typedef struct {
+  int32_t T, H, I, E, k;
+} k3moe_shape;
+
+/* MXFP4 expert weights of one layer.  Each member is a DEVICE array of E device
+ * pointers, one per expert.  Expert e is absent when any of its four pointers
+ * is NULL: its assignments then produce zero rows (never an error).
+ *   w13_codes[e]  : uint8 [2I][H/2]  rows 0..I-1 are the gate projection, rows
+ *                   I..2I-1 the up projection; byte c of a row holds column 2c in
+ *                   its low nibble and column 2c+1 in its high nibble; each
+ *                   nibble is an E2M1 code (bit 3 sign, bits 2-1 exponent, bit 0
+ *                   mantissa).  16-byte aligned.
+ *   w13_scales[e] : uint8 [2I][H/32] E8M0 scale of each 32-column block
+ *                   (value 2^(byte-127); 255 is NaN).
+ *   w2_codes[e]   : uint8 [H][I/2]   down projection, same nibble order. 16-byte aligned.
+ *   w2_scales[e]  : uint8 [H][I/32]
+ * Element (r, c) of a matrix = E2M1(code) * E8M0(scale[r][c/32]). */
+typedef struct {
+  const uint8_t *const *w13_codes;
+  const uint8_t *const *w13_scales;
+  const uint8_t *const *w2_codes;
+  const uint8_t *const *w2_scales;
+} k3moe_weights;
+
+/* Expert FFN modes. */
+#define K3MOE_FFN_AUTO 0 /* the library picks per call from the token count        */
+#define K3MOE_FFN_GEMV 1 /* CUDA-core streaming GEMV, bf16 activations (decode)   */
+
+/* Workspace queries (bytes; 0 when the call needs none).  op is one of: */
+#define K3MOE_OP_BUCKET 1
+#define K3MOE_OP_EXPERT_FFN 2
+size_t k3moe_workspace_bytes(k3moe_shape s, int op, int mode);
+
+/* Route: for each token t, the k experts with the largest logits, ordered by
+ * (logit descending, expert index ascending) -- ties go to the lower index, -0
+ * equals +0 -- and weights w[t][j] = exp(l_j - m) / sum_j' exp(l_j' - m) over
+ * the k picks (m = the row maximum), i.e. the softmax over all E experts
+ * renormalised to the top k.  A row holding a NaN sets K3MOE_DEV_NONFINITE
+ * and yields experts 0..k-1 with weights 1/k; an all -inf row yields weights
+ * 1/k; a row whose maximum is +inf splits the weight evenly over its +inf picks.
+ *   logits : float [T][E]      idx : int32 [T][k]      w : float [T][k]
+ *   dev_status : int32 device word (may be NULL: NaN rows are then unreported). */
+int k3moe_route(k3moe_shape s, const float *logits, int32_t *idx, float *w,
+                int32_t *dev_status, k3moe_stream_t stream);
+
+/* Bucket: a stable counting sort of the A = T*k assignments a = t*k + j by
+ * expert idx[a] (the chunk-union grouping).
+ *   counts  : int32 [E]    number of assignments per expert
+ *   offsets : int32 [E+1]  exclusive prefix sum of counts (offsets[E] = A)
+ *   perm    : int32 [A]    assignment ids in expert-major, then ascending, order
+ *   inv     : int32 [A]    inv[perm[p]] = p
+ *   ws      : workspace of k3moe_workspace_bytes(s, K3MOE_OP_BUCKET, 0) bytes
+ * An idx entry outside [0, E) sets K3MOE_DEV_BOUNDS (when dev_status is given)
+ * and that assignment is dropped from the counts. */
+int k3moe_bucket(k3moe_shape s, const int32_t *idx, int32_t *counts, int32_t *offsets,
+                 int32_t *perm, int32_t *inv, void *ws, size_t ws_bytes, int32_t *dev_status,
+                 k3moe_stream_t stream);
+
+/* Expert FFN: for each bucket position p (assignment a = perm[p], token t = a/k,
+ * expert e with offsets[e] <= p < offsets[e+1]):
+ *   g = W_gate,e x_t ;  u = W_up,e x_t ;  h = bf16_rne(silu(g) * u) ;
+ *   Y[p] = W_down,e h          (silu(z) = z / (1 + exp(-z)))
+ * Dot products accumulate in fp32 from exact products; h is rounded to bf16
+ * (round to nearest even) before the down projection.
+ *   x    : uint16 [T][H] bf16 bit patterns, 16-byte aligned
+ *   Y    : float  [A][H] in bucket order, 16-byte aligned
+ *   ws   : workspace of k3moe_workspace_bytes(s, K3MOE_OP_EXPERT_FFN, mode) bytes */
+int k3moe_expert_ffn(k3moe_shape s, const uint16_t *x, const k3moe_weights *w,
+                     const int32_t *offsets, const int32_t *perm, float *Y, int mode, void *ws,
+                     size_t ws_bytes, int32_t *dev_status, k3moe_stream_t stream);
+
+/* Combine: out_f32[t] = sum_{j=0..k-1} w[t][j] * Y[inv[t*k+j]], accumulated in
+ * fp32 in increasing j; out[t] = bf16_rne(out_f32[t]).
+ *   Y : float [A][H]   w : float [T][k]   inv : int32 [A]
+ *   out : uint16 [T][H] bf16 bit patterns (required); out_f32 : float [T][H] or NULL. */
+int k3moe_combine(k3moe_shape s, const float *Y, const float *w, const int32_t *inv, uint16_t *out,
+                  float *out_f32, k3moe_stream_t stream);
+
+/* Human-readable name of a k3moe_status value. */
+const char *k3moe_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

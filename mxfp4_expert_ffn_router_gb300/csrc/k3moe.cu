@@ -1,0 +1,128 @@
+// k3moe.cu -- the C ABI (include/k3moe.h): argument validation and dispatch.
+// Every entry point validates on the host, launches nothing on error, and
+// otherwise enqueues its kernels on the caller's stream without synchronising.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/k3moe.h"
+#include "k3moe_launch.h"
+
+namespace {
+
+using k3moe_stream = cudaStream_t;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(const k3moe_shape &s) {
+  if (s.T < 0 || s.E < 1 || s.E > 4096 || s.k < 1 || s.k > 32 || s.k > s.E) return K3MOE_ERR_SHAPE;
+  if (s.H < 32 || s.H > 16384 || s.H % 32 || s.I < 32 || s.I > 16384 || s.I % 32) return K3MOE_ERR_SHAPE;
+  if (static_cast<long long>(s.T) * s.k >= (1LL << 31)) return K3MOE_ERR_SHAPE;
+  return K3MOE_OK;
+}
+
+// The kernels use sm_103a instructions: refuse any other device.
+int check_arch() {
+  static std::mutex mu;
+  static int cached[64];
+  static bool init = false;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return K3MOE_ERR_ARCH;
+  std::lock_guard<std::mutex> g(mu);
+  if (!init) {
+    for (int i = 0; i < 64; ++i) cached[i] = 0;
+    init = true;
+  }
+  if (cached[dev] == 0) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cached[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  return cached[dev] == 1 ? K3MOE_OK : K3MOE_ERR_ARCH;
+}
+
+int launched(int rc) {
+  if (rc != 0) return K3MOE_ERR_LAUNCH;
+  return cudaPeekAtLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t k3moe_workspace_bytes(k3moe_shape s, int op, int mode) {
+  if (check_shape(s) != K3MOE_OK) return 0;
+  if (op == K3MOE_OP_BUCKET) return k3moe::bucket_workspace(s);
+  if (op == K3MOE_OP_EXPERT_FFN && (mode == K3MOE_FFN_AUTO || mode == K3MOE_FFN_GEMV))
+    return k3moe::ffn_gemv_workspace(s);
+  return 0;
+}
+
+int k3moe_route(k3moe_shape s, const float *logits, int32_t *idx, float *w, int32_t *dev_status,
+                k3moe_stream_t stream) {
+  int rc = check_shape(s);
+  if (rc) return rc;
+  if (s.T == 0) return K3MOE_OK;
+  if (!logits || !idx || !w) return K3MOE_ERR_ARG;
+  if ((rc = check_arch())) return rc;
+  return launched(k3moe::launch_route(s, logits, idx, w, dev_status, reinterpret_cast<k3moe_stream>(stream)));
+}
+
+int k3moe_bucket(k3moe_shape s, const int32_t *idx, int32_t *counts, int32_t *offsets, int32_t *perm,
+                 int32_t *inv, void *ws, size_t ws_bytes, int32_t *dev_status,
+                 k3moe_stream_t stream) {
+  int rc = check_shape(s);
+  if (rc) return rc;
+  if (!counts || !offsets) return K3MOE_ERR_ARG;
+  if (s.T > 0 && (!idx || !perm || !inv)) return K3MOE_ERR_ARG;
+  const size_t need = k3moe::bucket_workspace(s);
+  if (need && (!ws || ws_bytes < need || !aligned16(ws))) return K3MOE_ERR_WORKSPACE;
+  if ((rc = check_arch())) return rc;
+  return launched(k3moe::launch_bucket(s, idx, counts, offsets, perm, inv, ws, dev_status,
+                                       reinterpret_cast<k3moe_stream>(stream)));
+}
+
+int k3moe_expert_ffn(k3moe_shape s, const uint16_t *x, const k3moe_weights *w, const int32_t *offsets,
+                     const int32_t *perm, float *Y, int mode, void *ws, size_t ws_bytes,
+                     int32_t *dev_status, k3moe_stream_t stream) {
+  int rc = check_shape(s);
+  if (rc) return rc;
+  if (mode != K3MOE_FFN_AUTO && mode != K3MOE_FFN_GEMV) return K3MOE_ERR_ARG;
+  if (s.T == 0) return K3MOE_OK;
+  if (!x || !w || !offsets || !perm || !Y) return K3MOE_ERR_ARG;
+  if (!w->w13_codes || !w->w13_scales || !w->w2_codes || !w->w2_scales) return K3MOE_ERR_ARG;
+  if (!aligned16(x) || !aligned16(Y)) return K3MOE_ERR_ALIGN;
+  const size_t need = k3moe::ffn_gemv_workspace(s);
+  if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u)) return K3MOE_ERR_WORKSPACE;
+  if ((rc = check_arch())) return rc;
+  return launched(k3moe::launch_ffn_gemv(s, x, *w, offsets, perm, Y, ws, dev_status,
+                                         reinterpret_cast<k3moe_stream>(stream)));
+}
+
+int k3moe_combine(k3moe_shape s, const float *Y, const float *w, const int32_t *inv, uint16_t *out,
+                  float *out_f32, k3moe_stream_t stream) {
+  int rc = check_shape(s);
+  if (rc) return rc;
+  if (s.T == 0) return K3MOE_OK;
+  if (!Y || !w || !inv || !out) return K3MOE_ERR_ARG;
+  if (!aligned16(Y) || !aligned16(out) || (out_f32 && !aligned16(out_f32))) return K3MOE_ERR_ALIGN;
+  if ((rc = check_arch())) return rc;
+  return launched(k3moe::launch_combine(s, Y, w, inv, out, out_f32, reinterpret_cast<k3moe_stream>(stream)));
+}
+
+const char *k3moe_status_string(int code) {
+  switch (code) {
+    case K3MOE_OK: return "ok";
+    case K3MOE_ERR_ARG: return "invalid argument (NULL pointer or bad enum)";
+    case K3MOE_ERR_SHAPE: return "unsupported shape";
+    case K3MOE_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case K3MOE_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    case K3MOE_ERR_ARCH: return "current device is not sm_103 (GB300)";
+    case K3MOE_ERR_LAUNCH: return "CUDA launch failed";
+    case K3MOE_ERR_UNSUPPORTED: return "request not supported by this build";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,41 @@
+// k3moe_launch.h -- host-side launch helpers and the internal kernel entry points.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/k3moe.h"
+
+namespace k3moe {
+
+// Launch with programmatic stream serialization, so a kernel's prologue may
+// overlap the tail of its predecessor; every kernel calls pdl_wait() before it
+// reads anything a predecessor wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+int launch_route(const k3moe_shape &s, const float *logits, int32_t *idx, float *w,
+                 int32_t *status, cudaStream_t st);
+size_t bucket_workspace(const k3moe_shape &s);
+int launch_bucket(const k3moe_shape &s, const int32_t *idx, int32_t *counts, int32_t *offsets,
+                  int32_t *perm, int32_t *inv, void *ws, int32_t *status, cudaStream_t st);
+size_t ffn_gemv_workspace(const k3moe_shape &s);
+int launch_ffn_gemv(const k3moe_shape &s, const uint16_t *x, const k3moe_weights &w,
+                    const int32_t *offsets, const int32_t *perm, float *Y, void *ws,
+                    int32_t *status, cudaStream_t st);
+int launch_combine(const k3moe_shape &s, const float *Y, const float *w, const int32_t *inv,
+                   uint16_t *out, float *out_f32, cudaStream_t st);
+
+}  // namespace k3moe

@@ -1,0 +1,220 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
+
+Bars: expert indices, counts, offsets, perm and inv bit-exact; routing weights
+within 1 fp32 ulp of the oracle; Y and the fp32 output within
+max|err| <= 2e-3 * RMS(reference); the bf16 output equal to RNE(fp32 output)."""
+import numpy as np
+import pytest
+import torch
+
+import gen
+import mxfp4_expert_ffn_router_gb300 as k3
+import oracle
+from layer_run import alloc_layer, bf16_rne_bits_of, host, max_rel_err, run_layer
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-3
+
+
+def _experts_host(H, I, E, seed=gen.WEIGHT_SEED):
+    a, b, c, d = gen.expert_arrays(H, I, 0, E, seed=seed)
+    return a, b, c, d
+
+
+def _device_weights(arrs, present=None):
+    t = [torch.from_numpy(np.ascontiguousarray(z)).cuda() for z in arrs]
+    return k3.Weights.from_stacked(*t, present=present)
+
+
+def _check_route(s, logits, r):
+    idx, w, bad = oracle.route(s, logits)
+    np.testing.assert_array_equal(r["idx"], idx)
+    wr = w.astype(np.float32)
+    ulp = np.spacing(np.abs(wr))
+    assert np.all(np.abs(r["w"].astype(np.float64) - w) <= ulp + 1e-45)
+    return idx, w, bad
+
+
+def _check_bucket(s, idx, r):
+    counts, offsets, perm, inv = oracle.bucket(s, idx)
+    np.testing.assert_array_equal(r["counts"], counts)
+    np.testing.assert_array_equal(r["offsets"], offsets)
+    np.testing.assert_array_equal(r["perm"], perm)
+    np.testing.assert_array_equal(r["inv"], inv)
+    return counts, offsets, perm, inv
+
+
+def _full_check(s, logits, xbits, experts_np, r, a4=False, absent=()):
+    idx, w, _ = _check_route(s, logits, r)
+    counts, offsets, perm, inv = _check_bucket(s, idx, r)
+    exps = {e: tuple(z[e] for z in experts_np) for e in np.unique(idx) if e not in absent}
+    W = oracle.Weights(s.E, exps)
+    Y = oracle.expert_ffn(s, xbits, W, offsets, perm, a4=a4)
+    out, _ = oracle.combine(s, Y, w, inv)
+    assert max_rel_err(r["Y"], Y) <= TOL, max_rel_err(r["Y"], Y)
+    assert max_rel_err(r["out_f32"], out) <= TOL, max_rel_err(r["out_f32"], out)
+    np.testing.assert_array_equal(r["out"], bf16_rne_bits_of(r["out_f32"]))
+    return out
+
+
+CASES = [  # T, H, I, E, k: several tiles and ragged tails
+    (4, 128, 64, 8, 2),
+    (1, 64, 32, 8, 8),
+    (37, 256, 96, 24, 6),
+    (129, 128, 64, 33, 3),
+    (9, 7168, 64, 16, 4),
+    (5, 96, 2048, 7, 2),
+    (300, 64, 32, 5, 1),
+    (3, 64, 64, 40, 32),
+]
+
+
+@pytest.mark.parametrize("T,H,I,E,k", CASES)
+def test_small_shapes_match_oracle(T, H, I, E, k):
+    s = gen.Shape(T, H, I, E, k)
+    rng = np.random.default_rng(T * 1000 + E)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    xbits = gen.normal_bf16_bits(3, gen.stream(gen.KIND_X), T * H).reshape(T, H)
+    experts = _experts_host(H, I, E)
+    Wd = _device_weights(experts)
+    r = host(run_layer(s, torch.from_numpy(logits).cuda(), torch.from_numpy(xbits.view(np.int16)).cuda(), Wd))
+    assert r["status"][0] == 0
+    _full_check(s, logits, xbits, experts, r)
+
+
+def test_tiny_workload():
+    s = gen.CONFIGS["tiny"]
+    logits, xbits = gen.make_logits("tiny"), gen.make_x(s)
+    experts = _experts_host(s.H, s.I, s.E)
+    r = host(run_layer(s, torch.from_numpy(logits).cuda(), torch.from_numpy(xbits.view(np.int16)).cuda(),
+                       _device_weights(experts)))
+    _full_check(s, logits, xbits, experts, r)
+
+
+def test_ties_signed_zeros_and_all_equal_rows():
+    s = gen.Shape(6, 64, 32, 40, 5)
+    rng = np.random.default_rng(5)
+    logits = np.round(rng.standard_normal((6, 40)) * 2).astype(np.float32) / 2
+    logits[0] = 0.25
+    logits[1, :20] = -0.0
+    logits[1, 20:] = 0.0
+    logits[2, ::3] = 7.0
+    xbits = gen.normal_bf16_bits(4, gen.stream(gen.KIND_X), 6 * 64).reshape(6, 64)
+    experts = _experts_host(64, 32, 40)
+    r = host(run_layer(s, torch.from_numpy(logits).cuda(), torch.from_numpy(xbits.view(np.int16)).cuda(),
+                       _device_weights(experts)))
+    _full_check(s, logits, xbits, experts, r)
+    assert r["idx"][0].tolist() == [0, 1, 2, 3, 4]
+
+
+def test_nan_row_flagged_and_infinities():
+    s = gen.Shape(4, 64, 32, 16, 4)
+    logits = np.random.default_rng(1).standard_normal((4, 16)).astype(np.float32)
+    logits[1, 3] = np.nan
+    logits[2] = -np.inf
+    logits[3, 5] = np.inf
+    logits[3, 9] = np.inf
+    xbits = gen.normal_bf16_bits(4, gen.stream(gen.KIND_X), 4 * 64).reshape(4, 64)
+    experts = _experts_host(64, 32, 16)
+    r = host(run_layer(s, torch.from_numpy(logits).cuda(), torch.from_numpy(xbits.view(np.int16)).cuda(),
+                       _device_weights(experts)))
+    assert r["status"][0] & k3.K3MOE_DEV_NONFINITE
+    idx, w, bad = oracle.route(s, logits)
+    np.testing.assert_array_equal(r["idx"], idx)
+    np.testing.assert_allclose(r["w"], w, rtol=1e-7, atol=0)
+    assert bad.tolist() == [0, 1, 0, 0]
+    _full_check(s, logits, xbits, experts, r)
+
+
+def test_absent_expert_gives_zero_rows():
+    s = gen.Shape(16, 128, 64, 8, 2)
+    logits = np.random.default_rng(2).standard_normal((16, 8)).astype(np.float32)
+    xbits = gen.normal_bf16_bits(4, gen.stream(gen.KIND_X), 16 * 128).reshape(16, 128)
+    experts = _experts_host(128, 64, 8)
+    present = np.ones(8, bool)
+    present[3] = False
+    r = host(run_layer(s, torch.from_numpy(logits).cuda(), torch.from_numpy(xbits.view(np.int16)).cuda(),
+                       _device_weights(experts, present=torch.from_numpy(present))))
+    assert r["status"][0] == 0
+    _full_check(s, logits, xbits, experts, r, absent=(3,))
+    lo, hi = r["offsets"][3], r["offsets"][4]
+    assert hi > lo and not r["Y"][lo:hi].any()
+
+
+def test_one_expert_takes_every_token():
+    s = gen.Shape(45, 128, 64, 6, 2)
+    logits = np.random.default_rng(7).standard_normal((45, 6)).astype(np.float32)
+    logits[:, 4] += 50.0
+    xbits = gen.normal_bf16_bits(4, gen.stream(gen.KIND_X), 45 * 128).reshape(45, 128)
+    experts = _experts_host(128, 64, 6)
+    r = host(run_layer(s, torch.from_numpy(logits).cuda(), torch.from_numpy(xbits.view(np.int16)).cuda(),
+                       _device_weights(experts)))
+    assert r["counts"][4] == 45
+    _full_check(s, logits, xbits, experts, r)
+
+
+def test_empty_batch():
+    s = gen.Shape(0, 128, 64, 8, 2)
+    b = alloc_layer(s)
+    b["counts"].fill_(-5)
+    b["offsets"].fill_(-5)
+    k3.k3moe_route(s, torch.empty((0, 8), device="cuda"), b["idx"], b["w"], b["status"])
+    k3.k3moe_bucket(s, b["idx"], b["counts"], b["offsets"], b["perm"], b["inv"], b["ws_bucket"], b["status"])
+    torch.cuda.synchronize()
+    assert not b["counts"].any() and not b["offsets"].any()
+
+
+def test_maximum_hidden_and_intermediate():
+    s = gen.Shape(2, 16384, 16384, 2, 1)
+    logits = np.array([[1.0, 0.0], [0.0, 1.0]], np.float32)
+    xbits = gen.normal_bf16_bits(4, gen.stream(gen.KIND_X), 2 * 16384).reshape(2, 16384)
+    experts = _experts_host(16384, 16384, 2)
+    r = host(run_layer(s, torch.from_numpy(logits).cuda(), torch.from_numpy(xbits.view(np.int16)).cuda(),
+                       _device_weights(experts)))
+    _full_check(s, logits, xbits, experts, r)
+
+
+def test_maximum_experts_and_k():
+    s = gen.Shape(5, 64, 32, 4096, 32)
+    logits = np.random.default_rng(9).standard_normal((5, 4096)).astype(np.float32)
+    xbits = gen.normal_bf16_bits(4, gen.stream(gen.KIND_X), 5 * 64).reshape(5, 64)
+    experts = _experts_host(64, 32, 4096)
+    r = host(run_layer(s, torch.from_numpy(logits).cuda(), torch.from_numpy(xbits.view(np.int16)).cuda(),
+                       _device_weights(experts)))
+    _full_check(s, logits, xbits, experts, r)
+
+
+def test_large_bucket_multi_tile_bit_exact():
+    s = gen.Shape(5000, 32, 32, 300, 7)  # A = 35000: the tiled bucketing path
+    rng = np.random.default_rng(4)
+    logits = rng.standard_normal((5000, 300)).astype(np.float32)
+    logits[:, 17] += 2.0
+    b = alloc_layer(s, with_f32=False)
+    lg = torch.from_numpy(logits).cuda()
+    k3.k3moe_route(s, lg, b["idx"], b["w"], b["status"])
+    k3.k3moe_bucket(s, b["idx"], b["counts"], b["offsets"], b["perm"], b["inv"], b["ws_bucket"], b["status"])
+    r = host(b)
+    idx, _, _ = _check_route(s, logits, r)
+    _check_bucket(s, idx, r)
+
+
+def test_deterministic_repeat():
+    s = gen.Shape(33, 256, 128, 12, 4)
+    logits = np.random.default_rng(8).standard_normal((33, 12)).astype(np.float32)
+    xbits = gen.normal_bf16_bits(4, gen.stream(gen.KIND_X), 33 * 256).reshape(33, 256)
+    Wd = _device_weights(_experts_host(256, 128, 12))
+    lg, xd = torch.from_numpy(logits).cuda(), torch.from_numpy(xbits.view(np.int16)).cuda()
+    a = host(run_layer(s, lg, xd, Wd))
+    b = host(run_layer(s, lg, xd, Wd))
+    for key in ("idx", "w", "perm", "Y", "out", "out_f32"):
+        assert np.array_equal(a[key].view(np.uint8), b[key].view(np.uint8)), key
+
+
+def test_bad_expert_index_is_reported_not_read():
+    s = gen.Shape(3, 64, 32, 8, 2)
+    b = alloc_layer(s)
+    idx = torch.tensor([[0, 1], [9, 2], [-1, 3]], dtype=torch.int32, device="cuda")
+    k3.k3moe_bucket(s, idx, b["counts"], b["offsets"], b["perm"], b["inv"], b["ws_bucket"], b["status"])
+    r = host(b)
+    assert r["status"][0] & k3.K3MOE_DEV_BOUNDS
+    assert r["offsets"][-1] == 4 and r["inv"][2] == -1 and r["inv"][4] == -1

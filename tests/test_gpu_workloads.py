@@ -1,0 +1,103 @@
+"""GPU parity on the full-size workloads (896 experts, H=7168, I=2048; 21 GB of
+MXFP4 weights resident), in the launch configuration the benchmark times.
+
+Decode (T=1), the 8-token batch and the I=1536 decode layer are checked in
+full against the oracle.  For the 4096- and 2048-token prefill workloads the
+routing and bucketing are checked bit-exactly on every token, and the outputs
+of a sample of tokens (covering the most loaded experts, the first and the
+last token) are checked against the oracle's per-token path."""
+import numpy as np
+import pytest
+import torch
+
+import gen
+import oracle
+from gen.device import DeviceExperts, device_inputs
+from layer_run import bf16_rne_bits_of, host, max_rel_err, run_layer
+import mxfp4_expert_ffn_router_gb300 as k3
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def experts_2048():
+    dx = DeviceExperts(7168, 2048, 896)
+    yield dx
+    del dx
+    torch.cuda.empty_cache()
+
+
+def _weights(dx):
+    return k3.Weights.from_stacked(*dx.tensors)
+
+
+def _host_experts(s, ids):
+    out = {}
+    for e in ids:
+        a, b, c, d = gen.expert_arrays(s.H, s.I, int(e), int(e) + 1)
+        out[int(e)] = (a[0], b[0], c[0], d[0])
+    return oracle.Weights(s.E, out)
+
+
+def _route_bucket_exact(s, logits, r):
+    idx, w, _ = oracle.route(s, logits)
+    np.testing.assert_array_equal(r["idx"], idx)
+    assert np.all(np.abs(r["w"].astype(np.float64) - w) <= np.spacing(np.abs(w.astype(np.float32))) + 1e-45)
+    counts, offsets, perm, inv = oracle.bucket(s, idx)
+    for key, ref in (("counts", counts), ("offsets", offsets), ("perm", perm), ("inv", inv)):
+        np.testing.assert_array_equal(r[key], ref, err_msg=key)
+    return idx, w, counts, offsets, perm, inv
+
+
+def _full(name, dx, s=None):
+    s = s or gen.CONFIGS[name]
+    lg, xd, logits, xbits = device_inputs(name, s)
+    r = host(run_layer(s, lg, xd, _weights(dx)))
+    assert r["status"][0] == 0
+    idx, w, counts, offsets, perm, inv = _route_bucket_exact(s, logits, r)
+    W = _host_experts(s, np.unique(idx))
+    Y = oracle.expert_ffn(s, xbits, W, offsets, perm)
+    out, _ = oracle.combine(s, Y, w, inv)
+    assert max_rel_err(r["Y"], Y) <= TOL
+    assert max_rel_err(r["out_f32"], out) <= TOL
+    np.testing.assert_array_equal(r["out"], bf16_rne_bits_of(r["out_f32"]))
+    return r
+
+
+def test_decode(experts_2048):
+    r = _full("decode", experts_2048)
+    assert len(np.unique(r["idx"])) == 16
+
+
+def test_batch8_shared_experts(experts_2048):
+    r = _full("batch8", experts_2048)
+    shared = set(r["idx"][0, :8].tolist())
+    for t in range(1, 4):
+        assert set(r["idx"][t, :8].tolist()) == shared
+
+
+def test_decode_i1536():
+    dx = DeviceExperts(7168, 1536, 896)
+    _full("decode_i1536", dx, gen.CONFIGS["decode_i1536"])
+
+
+@pytest.mark.parametrize("name", ["prefill", "skewed"])
+def test_prefill_sampled(experts_2048, name):
+    s = gen.CONFIGS[name]
+    lg, xd, logits, xbits = device_inputs(name, s)
+    r = host(run_layer(s, lg, xd, _weights(experts_2048)))
+    assert r["status"][0] == 0
+    idx, w, counts, offsets, perm, inv = _route_bucket_exact(s, logits, r)
+    np.testing.assert_array_equal(r["out"], bf16_rne_bits_of(r["out_f32"]))
+    hot = np.argsort(-counts, kind="stable")[:3]
+    sample = {0, s.T - 1}
+    for e in hot:
+        sample.add(int(perm[offsets[e]] // s.k))
+    rng = np.random.default_rng(123)
+    sample |= set(int(t) for t in rng.integers(0, s.T, 3))
+    sample = sorted(sample)
+    W = _host_experts(s, np.unique(idx[sample]))
+    ref = np.stack([oracle.moe_token(s, xbits[t], idx[t], w[t], W) for t in sample])
+    got = r["out_f32"][sample]
+    assert max_rel_err(got, ref) <= TOL, max_rel_err(got, ref)
