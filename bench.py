@@ -47,6 +47,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle sample budget")
+    p.add_argument("--experts", type=int, default=0,
+                   help="override E (small cases for profiling; 0 = the workload's own)")
     return p.parse_args()
 
 
@@ -63,6 +65,7 @@ def expert_bytes(s) -> int:
 def input_set(name, s, i):
     seed = gen.INPUT_SEED + 1000 * i
     return gen.make_logits(name, s, seed=seed), gen.make_x(s, seed=seed)
+
 
 
 def routed_experts(s, logits):
@@ -199,11 +202,18 @@ def oracle_sample(name, s, sets, budget_s):
                            f"({name}), 1 thread")
 
 
+def workload_shape(a):
+    s = gen.CONFIGS[a.config]
+    if a.experts:
+        s = gen.Shape(s.T, s.H, s.I, a.experts, min(s.k, a.experts))
+    return s
+
+
 def run_reference(a):
     ws, rank, _ = dist_env()
     if rank != 0:
         return
-    s = gen.CONFIGS[a.config]
+    s = workload_shape(a)
     nsets = max(1, min(a.sets, a.steps + a.warmup)) if s.T <= 8 else 1
     sets = [input_set(a.config, s, i) for i in range(nsets)]
     import oracle
@@ -281,7 +291,7 @@ def run_gpu(a):
         k3build.build()
     if ws > 1:
         dist.barrier()
-    s = gen.CONFIGS[a.config]
+    s = workload_shape(a)
     A = s.T * s.k
     nsets = max(1, a.sets)
     sets = [input_set(a.config, s, i) for i in range(nsets)]

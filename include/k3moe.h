@@ -89,9 +89,13 @@ typedef struct {
   const uint8_t *const *w2_scales;
 } k3moe_weights;
 
-/* Expert FFN modes. */
-#define K3MOE_FFN_AUTO 0 /* the library picks per call from the token count        */
-#define K3MOE_FFN_GEMV 1 /* CUDA-core streaming GEMV, bf16 activations (decode)   */
+/* Expert FFN modes.  All compute the same function (bf16 activations, exact
+ * MXFP4 weights, fp32 accumulation); they differ in how weights are streamed. */
+#define K3MOE_FFN_AUTO 0   /* the library picks per call                              */
+#define K3MOE_FFN_GEMV 1   /* CUDA-core GEMV kernels, 128-bit register loads (any shape) */
+#define K3MOE_FFN_STREAM 2 /* one persistent CUDA-core kernel fed by 1-D TMA bulk copies
+                              into a shared-memory ring; needs H/32 and I/32 multiples of
+                              16 and H, I <= 8192 (else K3MOE_ERR_UNSUPPORTED)          */
 
 /* Workspace queries (bytes; 0 when the call needs none).  op is one of: */
 #define K3MOE_OP_BUCKET 1
@@ -145,6 +149,10 @@ int k3moe_combine(k3moe_shape s, const float *Y, const float *w, const int32_t *
 
 /* Human-readable name of a k3moe_status value. */
 const char *k3moe_status_string(int code);
+
+/* The CUDA error text behind the calling thread's most recent K3MOE_ERR_LAUNCH
+ * ("no error" if none).  The string is static; do not free it. */
+const char *k3moe_last_cuda_error(void);
 
 #ifdef __cplusplus
 }

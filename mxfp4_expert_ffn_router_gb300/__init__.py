@@ -22,13 +22,16 @@ _lib = None
 K3MOE_OK, K3MOE_ERR_ARG, K3MOE_ERR_SHAPE, K3MOE_ERR_ALIGN = 0, -1, -2, -3
 K3MOE_ERR_WORKSPACE, K3MOE_ERR_ARCH, K3MOE_ERR_LAUNCH, K3MOE_ERR_UNSUPPORTED = -4, -5, -6, -7
 K3MOE_DEV_NONFINITE, K3MOE_DEV_BOUNDS, K3MOE_DEV_TIMEOUT = 1, 2, 4
-K3MOE_FFN_AUTO, K3MOE_FFN_GEMV = 0, 1
+K3MOE_FFN_AUTO, K3MOE_FFN_GEMV, K3MOE_FFN_STREAM = 0, 1, 2
 K3MOE_OP_BUCKET, K3MOE_OP_EXPERT_FFN = 1, 2
 
 
 class K3moeError(RuntimeError):
     def __init__(self, fn: str, code: int):
-        super().__init__(f"{fn}: {status_string(code)} ({code})")
+        msg = f"{fn}: {status_string(code)} ({code})"
+        if code == K3MOE_ERR_LAUNCH:
+            msg += f": {lib().k3moe_last_cuda_error().decode()}"
+        super().__init__(msg)
         self.code = code
 
 
@@ -73,6 +76,8 @@ def lib():
             L.k3moe_combine.argtypes = [Shape, vp, vp, vp, vp, vp, vp]
             L.k3moe_status_string.restype = ctypes.c_char_p
             L.k3moe_status_string.argtypes = [i32]
+            L.k3moe_last_cuda_error.restype = ctypes.c_char_p
+            L.k3moe_last_cuda_error.argtypes = []
             _lib = L
     return _lib
 

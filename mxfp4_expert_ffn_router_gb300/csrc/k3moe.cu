@@ -42,20 +42,39 @@ int check_arch() {
   return cached[dev] == 1 ? K3MOE_OK : K3MOE_ERR_ARCH;
 }
 
+thread_local const char *t_last_cuda_error = "no error";
+
 int launched(int rc) {
-  if (rc != 0) return K3MOE_ERR_LAUNCH;
-  return cudaPeekAtLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_LAUNCH;
+  const cudaError_t e = cudaGetLastError();
+  if (rc == 0 && e == cudaSuccess) return K3MOE_OK;
+  t_last_cuda_error = cudaGetErrorString(e == cudaSuccess ? cudaErrorLaunchFailure : e);
+  return K3MOE_ERR_LAUNCH;
 }
 
 }  // namespace
 
 extern "C" {
 
+// The expert FFN path a mode resolves to for a shape (-1: unsupported).
+static int resolve_ffn_mode(const k3moe_shape &s, int mode) {
+  switch (mode) {
+    case K3MOE_FFN_AUTO: return k3moe::ffn_stream_supported(s) ? K3MOE_FFN_STREAM : K3MOE_FFN_GEMV;
+    case K3MOE_FFN_GEMV: return K3MOE_FFN_GEMV;
+    case K3MOE_FFN_STREAM: return k3moe::ffn_stream_supported(s) ? K3MOE_FFN_STREAM : -1;
+    default: return -1;
+  }
+}
+
+static size_t ffn_workspace(const k3moe_shape &s, int resolved) {
+  if (resolved == K3MOE_FFN_STREAM) return k3moe::ffn_stream_workspace(s);
+  if (resolved == K3MOE_FFN_GEMV) return k3moe::ffn_gemv_workspace(s);
+  return 0;
+}
+
 size_t k3moe_workspace_bytes(k3moe_shape s, int op, int mode) {
   if (check_shape(s) != K3MOE_OK) return 0;
   if (op == K3MOE_OP_BUCKET) return k3moe::bucket_workspace(s);
-  if (op == K3MOE_OP_EXPERT_FFN && (mode == K3MOE_FFN_AUTO || mode == K3MOE_FFN_GEMV))
-    return k3moe::ffn_gemv_workspace(s);
+  if (op == K3MOE_OP_EXPERT_FFN) return ffn_workspace(s, resolve_ffn_mode(s, mode));
   return 0;
 }
 
@@ -88,16 +107,20 @@ int k3moe_expert_ffn(k3moe_shape s, const uint16_t *x, const k3moe_weights *w, c
                      int32_t *dev_status, k3moe_stream_t stream) {
   int rc = check_shape(s);
   if (rc) return rc;
-  if (mode != K3MOE_FFN_AUTO && mode != K3MOE_FFN_GEMV) return K3MOE_ERR_ARG;
+  if (mode < K3MOE_FFN_AUTO || mode > K3MOE_FFN_STREAM) return K3MOE_ERR_ARG;
+  const int resolved = resolve_ffn_mode(s, mode);
+  if (resolved < 0) return K3MOE_ERR_UNSUPPORTED;
   if (s.T == 0) return K3MOE_OK;
   if (!x || !w || !offsets || !perm || !Y) return K3MOE_ERR_ARG;
   if (!w->w13_codes || !w->w13_scales || !w->w2_codes || !w->w2_scales) return K3MOE_ERR_ARG;
   if (!aligned16(x) || !aligned16(Y)) return K3MOE_ERR_ALIGN;
-  const size_t need = k3moe::ffn_gemv_workspace(s);
+  const size_t need = ffn_workspace(s, resolved);
   if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u)) return K3MOE_ERR_WORKSPACE;
   if ((rc = check_arch())) return rc;
-  return launched(k3moe::launch_ffn_gemv(s, x, *w, offsets, perm, Y, ws, dev_status,
-                                         reinterpret_cast<k3moe_stream>(stream)));
+  const cudaStream_t st = reinterpret_cast<k3moe_stream>(stream);
+  if (resolved == K3MOE_FFN_STREAM)
+    return launched(k3moe::launch_ffn_stream(s, x, *w, offsets, perm, Y, ws, dev_status, st));
+  return launched(k3moe::launch_ffn_gemv(s, x, *w, offsets, perm, Y, ws, dev_status, st));
 }
 
 int k3moe_combine(k3moe_shape s, const float *Y, const float *w, const int32_t *inv, uint16_t *out,
@@ -110,6 +133,8 @@ int k3moe_combine(k3moe_shape s, const float *Y, const float *w, const int32_t *
   if ((rc = check_arch())) return rc;
   return launched(k3moe::launch_combine(s, Y, w, inv, out, out_f32, reinterpret_cast<k3moe_stream>(stream)));
 }
+
+const char *k3moe_last_cuda_error(void) { return t_last_cuda_error; }
 
 const char *k3moe_status_string(int code) {
   switch (code) {

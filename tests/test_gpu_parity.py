@@ -69,6 +69,70 @@ CASES = [  # T, H, I, E, k: several tiles and ragged tails
 ]
 
 
+STREAM_CASES = [  # shapes the TMA-fed streaming kernel accepts (H/32, I/32 multiples of 16)
+    (1, 512, 512, 8, 2),
+    (5, 512, 512, 8, 2),
+    (37, 1024, 512, 24, 6),
+    (130, 512, 1024, 7, 3),
+    (3, 7168, 512, 40, 32),
+    (2, 4096, 4096, 3, 2),
+    (8, 7168, 2048, 12, 4),
+]
+
+
+def _run_case(T, H, I, E, k, mode):
+    s = gen.Shape(T, H, I, E, k)
+    rng = np.random.default_rng(T * 1000 + E)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    xbits = gen.normal_bf16_bits(3, gen.stream(gen.KIND_X), T * H).reshape(T, H)
+    experts = _experts_host(H, I, E)
+    Wd = _device_weights(experts)
+    b = alloc_layer(s, mode=mode)
+    r = host(run_layer(s, torch.from_numpy(logits).cuda(), torch.from_numpy(xbits.view(np.int16)).cuda(), Wd,
+                       bufs=b, mode=mode))
+    assert r["status"][0] == 0
+    _full_check(s, logits, xbits, experts, r)
+
+
+@pytest.mark.parametrize("T,H,I,E,k", STREAM_CASES)
+def test_stream_mode_matches_oracle(T, H, I, E, k):
+    _run_case(T, H, I, E, k, k3.K3MOE_FFN_STREAM)
+
+
+@pytest.mark.parametrize("T,H,I,E,k", STREAM_CASES[:3])
+def test_gemv_mode_on_stream_shapes(T, H, I, E, k):
+    _run_case(T, H, I, E, k, k3.K3MOE_FFN_GEMV)
+
+
+def test_stream_mode_refuses_unsupported_shape():
+    s = gen.Shape(2, 128, 64, 4, 1)
+    assert k3.k3moe_workspace_bytes(s, k3.K3MOE_OP_EXPERT_FFN, k3.K3MOE_FFN_STREAM) == 0
+    b = alloc_layer(s)
+    with pytest.raises(k3.K3moeError) as ei:
+        k3.k3moe_expert_ffn(s, torch.zeros((2, 128), dtype=torch.int16, device="cuda"),
+                            _device_weights(_experts_host(128, 64, 4)), b["offsets"], b["perm"], b["Y"],
+                            k3.K3MOE_FFN_STREAM, b["ws_ffn"], b["status"])
+    assert ei.value.code == k3.K3MOE_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("mode", [k3.K3MOE_FFN_STREAM, k3.K3MOE_FFN_GEMV])
+def test_absent_expert_and_hot_expert_both_modes(mode):
+    s = gen.Shape(45, 512, 512, 6, 2)
+    logits = np.random.default_rng(7).standard_normal((45, 6)).astype(np.float32)
+    logits[:, 4] += 50.0  # expert 4 takes every token: many token chunks
+    xbits = gen.normal_bf16_bits(4, gen.stream(gen.KIND_X), 45 * 512).reshape(45, 512)
+    experts = _experts_host(512, 512, 6)
+    present = np.ones(6, bool)
+    idx, _, _ = oracle.route(s, logits)
+    gone = int(idx[0, 1])
+    present[gone] = False
+    b = alloc_layer(s, mode=mode)
+    r = host(run_layer(s, torch.from_numpy(logits).cuda(), torch.from_numpy(xbits.view(np.int16)).cuda(),
+                       _device_weights(experts, present=torch.from_numpy(present)), bufs=b, mode=mode))
+    assert r["status"][0] == 0 and r["counts"][4] == 45
+    _full_check(s, logits, xbits, experts, r, absent=(gone,))
+
+
 @pytest.mark.parametrize("T,H,I,E,k", CASES)
 def test_small_shapes_match_oracle(T, H, I, E, k):
     s = gen.Shape(T, H, I, E, k)

@@ -13,7 +13,7 @@ import torch
 import gen
 import oracle
 from gen.device import DeviceExperts, device_inputs
-from layer_run import bf16_rne_bits_of, host, max_rel_err, run_layer
+from layer_run import alloc_layer, bf16_rne_bits_of, host, max_rel_err, run_layer
 import mxfp4_expert_ffn_router_gb300 as k3
 
 pytestmark = pytest.mark.gpu
@@ -50,10 +50,10 @@ def _route_bucket_exact(s, logits, r):
     return idx, w, counts, offsets, perm, inv
 
 
-def _full(name, dx, s=None):
+def _full(name, dx, s=None, mode=k3.K3MOE_FFN_AUTO):
     s = s or gen.CONFIGS[name]
     lg, xd, logits, xbits = device_inputs(name, s)
-    r = host(run_layer(s, lg, xd, _weights(dx)))
+    r = host(run_layer(s, lg, xd, _weights(dx), bufs=alloc_layer(s, mode=mode), mode=mode))
     assert r["status"][0] == 0
     idx, w, counts, offsets, perm, inv = _route_bucket_exact(s, logits, r)
     W = _host_experts(s, np.unique(idx))
@@ -65,8 +65,9 @@ def _full(name, dx, s=None):
     return r
 
 
-def test_decode(experts_2048):
-    r = _full("decode", experts_2048)
+@pytest.mark.parametrize("mode", [k3.K3MOE_FFN_AUTO, k3.K3MOE_FFN_GEMV])
+def test_decode(experts_2048, mode):
+    r = _full("decode", experts_2048, mode=mode)
     assert len(np.unique(r["idx"])) == 16
 
 
