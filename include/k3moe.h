@@ -54,7 +54,9 @@ typedef enum {
   K3MOE_ERR_WORKSPACE = -4,   /* workspace NULL or smaller than required         */
   K3MOE_ERR_ARCH = -5,        /* current device is not compute capability 10.3   */
   K3MOE_ERR_LAUNCH = -6,      /* a CUDA launch failed                            */
-  K3MOE_ERR_UNSUPPORTED = -7  /* valid request this build cannot serve           */
+  K3MOE_ERR_UNSUPPORTED = -7, /* valid request this build cannot serve           */
+  K3MOE_ERR_NOALLOC_LIMIT = -8 /* problem needs more scratch than the fixed array of
+                                  k3moe_expert_ffn_noalloc holds                  */
 } k3moe_status;
 
 /* Device-side status bits (OR-ed into *dev_status). */
@@ -139,6 +141,30 @@ int k3moe_bucket(k3moe_shape s, const int32_t *idx, int32_t *counts, int32_t *of
 int k3moe_expert_ffn(k3moe_shape s, const uint16_t *x, const k3moe_weights *w,
                      const int32_t *offsets, const int32_t *perm, float *Y, int mode, void *ws,
                      size_t ws_bytes, int32_t *dev_status, k3moe_stream_t stream);
+
+/* Expert FFN without a workspace argument (no counterpart on the pages: it exists
+ * for callers of this library that cannot allocate device memory).  Some callers
+ * cannot call cudaMalloc around the layer: cudaMalloc/cudaFree may synchronise
+ * the whole device and stall other streams, a host framework may own all device
+ * memory through its own pool, or the code may run where CUDA allocation calls
+ * are not allowed.  This entry point computes exactly what k3moe_expert_ffn does,
+ * with the same arguments minus ws/ws_bytes; its scratch is a file-scope device
+ * array of K3MOE_NOALLOC_SCRATCH_BYTES that every GPU loading the library keeps
+ * until the process exits.  It calls no allocation routine.
+ *  - Limit: problems whose scratch (k3moe_workspace_bytes(s, K3MOE_OP_EXPERT_FFN,
+ *    mode)) exceeds K3MOE_NOALLOC_SCRATCH_BYTES return K3MOE_ERR_NOALLOC_LIMIT and
+ *    launch nothing (decode-sized batches fit; large prefill chunks do not).
+ *  - The first call on a device looks up the array's device address with that
+ *    device current (one-time set-up); make that first call before any stream
+ *    capture.
+ *  - Every call on a device uses the same array, which keeps the previous call's
+ *    contents; each call re-initialises whatever it reads.  Calls whose kernels
+ *    overlap on the GPU (different streams, no ordering between them) race on the
+ *    array and give wrong results: order them on one stream or with events. */
+#define K3MOE_NOALLOC_SCRATCH_BYTES (8u << 20)
+int k3moe_expert_ffn_noalloc(k3moe_shape s, const uint16_t *x, const k3moe_weights *w,
+                             const int32_t *offsets, const int32_t *perm, float *Y, int mode,
+                             int32_t *dev_status, k3moe_stream_t stream);
 
 /* Combine: out_f32[t] = sum_{j=0..k-1} w[t][j] * Y[inv[t*k+j]], accumulated in
  * fp32 in increasing j; out[t] = bf16_rne(out_f32[t]).

@@ -21,6 +21,8 @@ _lib = None
 
 K3MOE_OK, K3MOE_ERR_ARG, K3MOE_ERR_SHAPE, K3MOE_ERR_ALIGN = 0, -1, -2, -3
 K3MOE_ERR_WORKSPACE, K3MOE_ERR_ARCH, K3MOE_ERR_LAUNCH, K3MOE_ERR_UNSUPPORTED = -4, -5, -6, -7
+K3MOE_ERR_NOALLOC_LIMIT = -8
+K3MOE_NOALLOC_SCRATCH_BYTES = 8 << 20
 K3MOE_DEV_NONFINITE, K3MOE_DEV_BOUNDS, K3MOE_DEV_TIMEOUT = 1, 2, 4
 K3MOE_FFN_AUTO, K3MOE_FFN_GEMV, K3MOE_FFN_STREAM = 0, 1, 2
 K3MOE_OP_BUCKET, K3MOE_OP_EXPERT_FFN = 1, 2
@@ -72,6 +74,9 @@ def lib():
             L.k3moe_expert_ffn.restype = i32
             L.k3moe_expert_ffn.argtypes = [Shape, vp, ctypes.POINTER(_WeightsC), vp, vp, vp, i32, vp,
                                            sz, vp, vp]
+            L.k3moe_expert_ffn_noalloc.restype = i32
+            L.k3moe_expert_ffn_noalloc.argtypes = [Shape, vp, ctypes.POINTER(_WeightsC), vp, vp, vp, i32,
+                                                   vp, vp]
             L.k3moe_combine.restype = i32
             L.k3moe_combine.argtypes = [Shape, vp, vp, vp, vp, vp, vp]
             L.k3moe_status_string.restype = ctypes.c_char_p
@@ -173,6 +178,18 @@ def k3moe_expert_ffn(shape, x, weights: Weights, offsets, perm, Y, mode=K3MOE_FF
                                 _ptr(Y, torch.float32, "Y"), mode, _ptr(ws, None, "ws"), ws_bytes,
                                 _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
     _check("k3moe_expert_ffn", rc)
+
+
+def k3moe_expert_ffn_noalloc(shape, x, weights: Weights, offsets, perm, Y, mode=K3MOE_FFN_AUTO,
+                             dev_status=None, stream=None):
+    """k3moe_expert_ffn with its scratch in the library's fixed device array (no
+    workspace argument), for callers that cannot allocate device memory."""
+    rc = lib().k3moe_expert_ffn_noalloc(Shape.of(shape), _ptr(x, _BF16, "x"), weights.cstruct(),
+                                        _ptr(offsets, torch.int32, "offsets"),
+                                        _ptr(perm, torch.int32, "perm"), _ptr(Y, torch.float32, "Y"),
+                                        mode, _ptr(dev_status, torch.int32, "dev_status"),
+                                        _stream(stream))
+    _check("k3moe_expert_ffn_noalloc", rc)
 
 
 def k3moe_combine(shape, Y, w, inv, out, out_f32=None, stream=None):

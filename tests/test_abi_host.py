@@ -105,7 +105,7 @@ def test_no_gpu_means_arch_error_not_a_launch(L):
 
 
 def test_status_strings(L):
-    for code in range(-7, 1):
+    for code in range(-8, 1):
         assert k3.status_string(code) and "unknown" not in k3.status_string(code)
     assert "unknown" in k3.status_string(-99)
 
