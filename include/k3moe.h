@@ -98,6 +98,11 @@ typedef struct {
 #define K3MOE_FFN_STREAM 2 /* one persistent CUDA-core kernel fed by 1-D TMA bulk copies
                               into a shared-memory ring; needs H/32 and I/32 multiples of
                               16 and H, I <= 8192 (else K3MOE_ERR_UNSUPPORTED)          */
+#define K3MOE_FFN_GEMM 3   /* grouped GEMMs on the tcgen05 tensor cores (weights dequantised
+                              exactly to bf16, fp32 accumulators in tensor memory) for
+                              token chunks; needs H and 2I multiples of 128 and I a
+                              multiple of 64 (else K3MOE_ERR_UNSUPPORTED).  AUTO picks it
+                              when A = T*k >= 8 * min(A, E).                            */
 
 /* Workspace queries (bytes; 0 when the call needs none).  op is one of: */
 #define K3MOE_OP_BUCKET 1

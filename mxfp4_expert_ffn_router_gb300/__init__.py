@@ -24,7 +24,7 @@ K3MOE_ERR_WORKSPACE, K3MOE_ERR_ARCH, K3MOE_ERR_LAUNCH, K3MOE_ERR_UNSUPPORTED = -
 K3MOE_ERR_NOALLOC_LIMIT = -8
 K3MOE_NOALLOC_SCRATCH_BYTES = 8 << 20
 K3MOE_DEV_NONFINITE, K3MOE_DEV_BOUNDS, K3MOE_DEV_TIMEOUT = 1, 2, 4
-K3MOE_FFN_AUTO, K3MOE_FFN_GEMV, K3MOE_FFN_STREAM = 0, 1, 2
+K3MOE_FFN_AUTO, K3MOE_FFN_GEMV, K3MOE_FFN_STREAM, K3MOE_FFN_GEMM = 0, 1, 2, 3
 K3MOE_OP_BUCKET, K3MOE_OP_EXPERT_FFN = 1, 2
 
 

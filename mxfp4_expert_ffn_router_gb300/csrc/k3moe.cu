@@ -58,9 +58,17 @@ extern "C" {
 // The expert FFN path a mode resolves to for a shape (-1: unsupported).
 static int resolve_ffn_mode(const k3moe_shape &s, int mode) {
   switch (mode) {
-    case K3MOE_FFN_AUTO: return k3moe::ffn_stream_supported(s) ? K3MOE_FFN_STREAM : K3MOE_FFN_GEMV;
+    case K3MOE_FFN_AUTO: {
+      // tensor cores once the assignments give each routed expert a real token
+      // block (mean >= 8 tokens per expert that can be active); otherwise stream
+      const long long A = static_cast<long long>(s.T) * s.k;
+      const long long experts = A < s.E ? A : s.E;
+      if (k3moe::ffn_gemm_supported(s) && A >= 8 * experts) return K3MOE_FFN_GEMM;
+      return k3moe::ffn_stream_supported(s) ? K3MOE_FFN_STREAM : K3MOE_FFN_GEMV;
+    }
     case K3MOE_FFN_GEMV: return K3MOE_FFN_GEMV;
     case K3MOE_FFN_STREAM: return k3moe::ffn_stream_supported(s) ? K3MOE_FFN_STREAM : -1;
+    case K3MOE_FFN_GEMM: return k3moe::ffn_gemm_supported(s) ? K3MOE_FFN_GEMM : -1;
     default: return -1;
   }
 }
@@ -68,6 +76,7 @@ static int resolve_ffn_mode(const k3moe_shape &s, int mode) {
 static size_t ffn_workspace(const k3moe_shape &s, int resolved) {
   if (resolved == K3MOE_FFN_STREAM) return k3moe::ffn_stream_workspace(s);
   if (resolved == K3MOE_FFN_GEMV) return k3moe::ffn_gemv_workspace(s);
+  if (resolved == K3MOE_FFN_GEMM) return k3moe::ffn_gemm_workspace(s);
   return 0;
 }
 
@@ -107,7 +116,7 @@ int k3moe_expert_ffn(k3moe_shape s, const uint16_t *x, const k3moe_weights *w, c
                      int32_t *dev_status, k3moe_stream_t stream) {
   int rc = check_shape(s);
   if (rc) return rc;
-  if (mode < K3MOE_FFN_AUTO || mode > K3MOE_FFN_STREAM) return K3MOE_ERR_ARG;
+  if (mode < K3MOE_FFN_AUTO || mode > K3MOE_FFN_GEMM) return K3MOE_ERR_ARG;
   const int resolved = resolve_ffn_mode(s, mode);
   if (resolved < 0) return K3MOE_ERR_UNSUPPORTED;
   if (s.T == 0) return K3MOE_OK;
@@ -120,6 +129,8 @@ int k3moe_expert_ffn(k3moe_shape s, const uint16_t *x, const k3moe_weights *w, c
   const cudaStream_t st = reinterpret_cast<k3moe_stream>(stream);
   if (resolved == K3MOE_FFN_STREAM)
     return launched(k3moe::launch_ffn_stream(s, x, *w, offsets, perm, Y, ws, dev_status, st));
+  if (resolved == K3MOE_FFN_GEMM)
+    return launched(k3moe::launch_ffn_gemm(s, x, *w, offsets, perm, Y, ws, dev_status, st));
   return launched(k3moe::launch_ffn_gemv(s, x, *w, offsets, perm, Y, ws, dev_status, st));
 }
 

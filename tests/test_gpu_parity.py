@@ -99,6 +99,20 @@ def test_stream_mode_matches_oracle(T, H, I, E, k):
     _run_case(T, H, I, E, k, k3.K3MOE_FFN_STREAM)
 
 
+GEMM_CASES = [  # shapes the tcgen05 grouped GEMM accepts (H, 2I multiples of 128; I of 64)
+    (8, 256, 128, 4, 2),
+    (37, 512, 256, 8, 3),
+    (300, 256, 128, 3, 2),      # experts with more than one 128-token tile
+    (5, 7168, 2048, 16, 4),
+    (130, 1024, 512, 6, 1),
+]
+
+
+@pytest.mark.parametrize("T,H,I,E,k", GEMM_CASES)
+def test_gemm_mode_matches_oracle(T, H, I, E, k):
+    _run_case(T, H, I, E, k, k3.K3MOE_FFN_GEMM)
+
+
 @pytest.mark.parametrize("T,H,I,E,k", STREAM_CASES[:3])
 def test_gemv_mode_on_stream_shapes(T, H, I, E, k):
     _run_case(T, H, I, E, k, k3.K3MOE_FFN_GEMV)
@@ -115,7 +129,7 @@ def test_stream_mode_refuses_unsupported_shape():
     assert ei.value.code == k3.K3MOE_ERR_UNSUPPORTED
 
 
-@pytest.mark.parametrize("mode", [k3.K3MOE_FFN_STREAM, k3.K3MOE_FFN_GEMV])
+@pytest.mark.parametrize("mode", [k3.K3MOE_FFN_STREAM, k3.K3MOE_FFN_GEMV, k3.K3MOE_FFN_GEMM])
 def test_absent_expert_and_hot_expert_both_modes(mode):
     s = gen.Shape(45, 512, 512, 6, 2)
     logits = np.random.default_rng(7).standard_normal((45, 6)).astype(np.float32)
