@@ -12,13 +12,24 @@
 // the GEMMs compute the same products as the CUDA-core path, summed in another
 // (fixed) order.
 //
-// One CTA (4 warps) per tile (active expert, 128 weight rows, <= 128 tokens).
-// Per K step of 64: all threads dequantise the weight tile and gather the token
-// tile into a 128B-swizzled K-major shared-memory stage; thread 0 issues four
-// tcgen05.mma (K = 16 each) and commits them to the stage's mbarrier; the next
-// stage is filled while the tensor core works (two stages).  The epilogue reads
-// the accumulator with tcgen05.ld and writes h (bf16) or Y (fp32) rows through
-// shared memory so the global stores are coalesced.
+// Operands are f16 (kind::f16, fp32 accumulation):
+//  * weights: e2m1 (exact in f16) times 2^(s - s_ref), where s_ref is the
+//    largest block-scale byte of the weight row; exact for every block within
+//    2^23 of the row's largest (smaller blocks round to f16 subnormals, below
+//    2^-24 of the row's scale); the factor 2^(s_ref - 127) is applied in the
+//    epilogue, exactly;
+//  * activations: x (gate/up) and h (down) as f16 after an exact power-of-two
+//    prescale per row (max|v| * 2^-p in [2^14, 2^15)), laid out in bucket order
+//    by two small pre-pass kernels so that a 2-D TMA tile load fetches them.
+//
+// One CTA per tile (active expert, 128 weight rows, <= 128 tokens), 10 warps:
+// warps 0-7 dequantise the weight tile rows into 128B-swizzled K-major shared
+// memory (two threads per row), warp 8 issues the TMA loads of the activation
+// tile, warp 9 owns tensor memory and issues tcgen05.mma (M=128, K=16 each),
+// committing every stage back to the producers; three stages; two CTAs per SM.
+// The epilogue (warps 0-7) reads the accumulator with tcgen05.ld and writes h
+// (bf16, the fixed rounding point) or Y (fp32) rows through shared memory.
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
 
@@ -29,11 +40,14 @@ namespace k3moe {
 
 namespace {
 
-constexpr int kThreadsG = 128;  // 4 warps: all load/dequantise, thread 0 issues MMAs
+constexpr int kDqWarps = 8;                     // dequantisation + epilogue warps
+constexpr int kTmaWarp = kDqWarps;              // activation-tile TMA producer
+constexpr int kMmaWarp = kDqWarps + 1;          // tensor-memory owner, MMA issuer
+constexpr int kThreadsG = (kDqWarps + 2) * 32;  // 320
 constexpr int kTileM = 128;     // weight rows per tile
 constexpr int kTileN = 128;     // tokens per tile (max)
-constexpr int kTileK = 64;      // K per stage: one 128-byte swizzle atom of bf16
-constexpr int kStagesG = 2;
+constexpr int kTileK = 64;      // K per stage: one 128-byte swizzle atom of 16-bit values
+constexpr int kStagesG = 3;
 constexpr int kStageA = kTileM * kTileK * 2;  // 16 KiB
 constexpr int kStageB = kTileN * kTileK * 2;  // 16 KiB
 constexpr long long kSpinG = 1LL << 22;
@@ -51,6 +65,22 @@ __device__ __forceinline__ bool mb_try(uint64_t *b, uint32_t parity) {
                : "r"(su32(b)), "r"(parity)
                : "memory");
   return ok != 0;
+}
+__device__ __forceinline__ void mb_arrive(uint64_t *b) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(su32(b)) : "memory");
+}
+__device__ __forceinline__ void mb_arrive_tx(uint64_t *b, uint32_t bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(su32(b)),
+               "r"(bytes)
+               : "memory");
+}
+// 2-D TMA tile load (tensor map in kernel-parameter space) completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(su32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(su32(bar))
+      : "memory");
 }
 __device__ __forceinline__ bool mb_wait(uint64_t *b, uint32_t parity) {
   for (long long i = 0; i < kSpinG; ++i) {
@@ -76,16 +106,16 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator, both K-major.
-__device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
+// Instruction descriptor, kind::f16: f16 A and B, fp32 accumulator, both K-major.
+__device__ __forceinline__ uint32_t idesc_f16(int M, int N) {
   return (1u << 4)                                   // D format: f32
-         | (1u << 7)                                 // A format: bf16
-         | (1u << 10)                                // B format: bf16
+         | (0u << 7)                                 // A format: f16
+         | (0u << 10)                                // B format: f16
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
-__device__ __forceinline__ void tc_mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+__device__ __forceinline__ void tc_mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                             uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
@@ -116,16 +146,28 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int c) {
   return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
-// e2m1 pair byte -> two bf16 (packed) times 2^(s-127), exact.
-__device__ __forceinline__ uint32_t e2m1x2_to_bf16x2_scaled(uint32_t f16x2, float scale) {
-  const __half2 h = *reinterpret_cast<const __half2 *>(&f16x2);
-  const float2 f = __half22float2(h);
-  const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
-  return *reinterpret_cast<const uint32_t *>(&b);
+// multiply by 2^p for |p| <= 252 (two exact steps)
+__device__ __forceinline__ float mul_pow2(float v, int p) {
+  const int p1 = p / 2, p2 = p - p1;
+  return v * exp2i(p1) * exp2i(p2);
+}
+
+// Power-of-two exponent p such that max_abs * 2^-p lies in [2^14, 2^15); 0 for 0.
+__device__ __forceinline__ int prescale_exp16(float max_abs) {
+  if (!(max_abs > 0.f) || max_abs == INFINITY) return 0;
+  int e;
+  frexpf(max_abs, &e);
+  return max(-100, min(100, (e - 1) - 14));
+}
+
+// f16 bit pattern of 2^d for d <= 0 (subnormal down to 2^-24, zero below).
+__device__ __forceinline__ uint32_t f16_pow2_bits(int d) {
+  if (d >= -14) return static_cast<uint32_t>(d + 15) << 10;
+  if (d >= -24) return 1u << (d + 24);
+  return 0u;
 }
 
 struct GemmTile {
-  int kind;  // 0 gate/up, 1 down
   int u, e, p0, n, m0;  // active slot, expert, first bucket position, tokens, first weight row of the tile
 };
 
@@ -149,7 +191,7 @@ __device__ __forceinline__ bool decode_tile(const int32_t *pref, const int32_t *
 }
 
 struct GemmWs {
-  size_t active, meta, sp0, scnt, pref_gu, pref_dn, hrow, total;
+  size_t active, meta, sp0, scnt, pref_gu, pref_dn, xg, xexp, hrow, h16, hexp, total;
 };
 __host__ __device__ inline size_t g256(size_t v) { return (v + 255) & ~size_t(255); }
 __host__ __device__ inline GemmWs gemm_ws(int T, int H, int I, int E, int k) {
@@ -162,7 +204,11 @@ __host__ __device__ inline GemmWs gemm_ws(int T, int H, int I, int E, int k) {
   w.scnt = o;    o = g256(o + sizeof(int32_t) * E);
   w.pref_gu = o; o = g256(o + sizeof(int32_t) * E);
   w.pref_dn = o; o = g256(o + sizeof(int32_t) * E);
-  w.hrow = o;    o = g256(o + sizeof(uint16_t) * A * I);
+  w.xg = o;      o = g256(o + sizeof(uint16_t) * A * H);  // x rows in bucket order, prescaled f16
+  w.xexp = o;    o = g256(o + sizeof(int32_t) * (A ? A : 1));
+  w.hrow = o;    o = g256(o + sizeof(uint16_t) * A * I);  // h, bf16 (the rounding point)
+  w.h16 = o;     o = g256(o + sizeof(uint16_t) * A * I);  // h prescaled to f16
+  w.hexp = o;    o = g256(o + sizeof(int32_t) * (A ? A : 1));
   w.total = o;
   return w;
 }
@@ -217,71 +263,114 @@ __global__ void __launch_bounds__(32)
   }
 }
 
+// Row p of `dst` (f16) = row of `src` (bf16, K values) times 2^-e, e chosen per
+// row so the largest magnitude lands in [2^14, 2^15): exact for bf16 inputs.
+// Gate/up: src row = x[perm[p] / k]; down: src row = h[p].
+__global__ void __launch_bounds__(256)
+    gemm_rows_to_f16_kernel(const uint16_t *__restrict__ src, const int32_t *__restrict__ perm, int k, int A,
+                            int K, uint16_t *__restrict__ dst, int32_t *__restrict__ exps, int32_t *status) {
+  pdl_wait();
+  pdl_trigger();
+  const int p = blockIdx.x;
+  int row = p;
+  if (perm) {
+    const int a = perm[p];
+    row = (a >= 0 && a < A) ? a / k : -1;
+    if (row < 0) set_status(status, K3MOE_DEV_BOUNDS);
+  }
+  uint16_t *d = dst + static_cast<size_t>(p) * K;
+  if (row < 0) {
+    for (int c = threadIdx.x * 8; c < K; c += 256 * 8) *reinterpret_cast<uint4 *>(d + c) = make_uint4(0, 0, 0, 0);
+    if (threadIdx.x == 0) exps[p] = 0;
+    return;
+  }
+  const uint16_t *s = src + static_cast<size_t>(row) * K;
+  __shared__ float red[8];
+  float mx = 0.f;
+  for (int c = threadIdx.x * 8; c < K; c += 256 * 8) {
+    const uint4 v = *reinterpret_cast<const uint4 *>(s + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+      mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[m] << 16)), fabsf(__uint_as_float(w[m] & 0xFFFF0000u))));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  mx = red[0];
+  for (int i = 1; i < 8; ++i) mx = fmaxf(mx, red[i]);
+  const int e = prescale_exp16(mx);
+  if (threadIdx.x == 0) exps[p] = e;
+  const float sc = mul_pow2(1.0f, -e);
+  for (int c = threadIdx.x * 8; c < K; c += 256 * 8) {
+    const uint4 v = *reinterpret_cast<const uint4 *>(s + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const __half2 h = __floats2half2_rn(__uint_as_float(w[m] << 16) * sc, __uint_as_float(w[m] & 0xFFFF0000u) * sc);
+      o[m] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    *reinterpret_cast<uint4 *>(d + c) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 // ----------------------------------------------------------------------------
 struct GemmParams {
   k3moe_weights w;
-  int T, H, I, E, k, A;
-  const int32_t *perm;
-  const uint16_t *x;          // [T][H] bf16
+  int H, I, A;
   const int32_t *active, *meta, *slot_p0, *slot_cnt, *pref;
-  uint16_t *hrow;             // [A][I] bf16 (gate/up output, down input)
+  const int32_t *bexp;        // per bucket position: prescale exponent of the activation row
+  uint16_t *hrow;             // [A][I] bf16 (gate/up output)
   float *Y;                   // [A][H]
   int kind;                   // 0 gate/up, 1 down
   int32_t *status;
 };
 
-// dynamic shared memory: 1024 bytes of alignment slack, then max(stages, epilogue transpose buffer)
+// dynamic shared memory: 1024 bytes of alignment slack + the stages (the epilogue
+// transpose buffer [kTileN][kTileM + 1] fp32 reuses them)
 constexpr int kEpiBytes = kTileN * (kTileM + 1) * 4;
-constexpr int kGemmSmem = 1024 + (kStagesG * (kStageA + kStageB) > kEpiBytes ? kStagesG * (kStageA + kStageB)
-                                                                                 : kEpiBytes);
+constexpr int kStageBytes = kStagesG * (kStageA + kStageB);
+constexpr int kGemmSmem = 1024 + (kStageBytes > kEpiBytes ? kStageBytes : kEpiBytes);
 
-__global__ void __launch_bounds__(kThreadsG, 1) ffn_gemm_kernel(GemmParams P) {
+__global__ void __launch_bounds__(kThreadsG, 1)
+    ffn_gemm_kernel(const __grid_constant__ CUtensorMap bmap, GemmParams P) {
   extern __shared__ __align__(1024) uint8_t gsm_raw[];
   // the 128B-swizzle atoms need 1024-byte aligned shared addresses: align explicitly
   uint8_t *gsm = gsm_raw + ((1024u - (su32(gsm_raw) & 1023u)) & 1023u);
-  // stage s: A tile at gsm + s * (kStageA + kStageB), B tile right after (both 1024-aligned)
-  __shared__ uint64_t mma_done[kStagesG];
+  __shared__ uint64_t full_bar[kStagesG], empty_bar[kStagesG], acc_bar;
   __shared__ uint32_t tmem_holder;
-  __shared__ int tok_of_row[kTileN];
-  const int tid = threadIdx.x, warp = tid >> 5;
+  __shared__ int sref_s[kTileM];  // largest scale byte of each tile row
+  __shared__ int bexp_s[kTileN];  // activation prescale exponent of each token column
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_wait();
   pdl_trigger();
 
   const int kind = P.kind;
-  const int K = kind == 0 ? P.H : P.I;          // reduction length
+  const int K = kind == 0 ? P.H : P.I;  // reduction length
   const int mtiles = kind == 0 ? (2 * P.I) / kTileM : P.H / kTileM;
   GemmTile g;
-  const int na = P.meta[0];
-  if (!decode_tile(P.pref, P.active, P.slot_p0, P.slot_cnt, na, mtiles, blockIdx.x, g)) return;
+  if (!decode_tile(P.pref, P.active, P.slot_p0, P.slot_cnt, P.meta[0], mtiles, blockIdx.x, g)) return;
   const int Npad = (g.n + 15) & ~15;  // MMA N: multiple of 16
+  const int ksteps = K / kTileK;
 
-  const uint8_t *codes, *scales;
-  const uintptr_t al = reinterpret_cast<uintptr_t>(P.w.w13_codes[g.e]) | reinterpret_cast<uintptr_t>(P.w.w2_codes[g.e]);
-  const bool present = P.w.w13_codes[g.e] && P.w.w13_scales[g.e] && P.w.w2_codes[g.e] && P.w.w2_scales[g.e] &&
-                       (al & 15u) == 0;  // 16-byte code loads
-  codes = kind == 0 ? P.w.w13_codes[g.e] : P.w.w2_codes[g.e];
-  scales = kind == 0 ? P.w.w13_scales[g.e] : P.w.w2_scales[g.e];
+  const uint8_t *c13 = P.w.w13_codes[g.e], *s13 = P.w.w13_scales[g.e];
+  const uint8_t *c2 = P.w.w2_codes[g.e], *s2 = P.w.w2_scales[g.e];
+  const uintptr_t al = reinterpret_cast<uintptr_t>(c13) | reinterpret_cast<uintptr_t>(c2);
+  const bool present = c13 && s13 && c2 && s2 && (al & 15u) == 0;  // 16-byte code loads
+  const uint8_t *codes = kind == 0 ? c13 : c2, *scales = kind == 0 ? s13 : s2;
 
-  // token rows of this tile (gate/up gathers x rows by token id; down reads h rows in bucket order)
-  for (int i = tid; i < kTileN; i += kThreadsG) {
-    int t = -1;
-    if (i < g.n) {
-      const int p = g.p0 + i;
-      if (kind == 0) {
-        const int a = P.perm[p];
-        t = (a >= 0 && a < P.A) ? a / P.k : -1;
-        if (t < 0) set_status(P.status, K3MOE_DEV_BOUNDS);
-      } else {
-        t = p;
-      }
-    }
-    tok_of_row[i] = t;
-  }
+  if (tid < kTileN) bexp_s[tid] = tid < g.n ? P.bexp[g.p0 + tid] : 0;
   if (tid == 0) {
-    for (int s = 0; s < kStagesG; ++s) mb_init(&mma_done[s], 1);
+    for (int s = 0; s < kStagesG; ++s) {
+      mb_init(&full_bar[s], kDqWarps * 32 + 1);  // every dequantising thread + the TMA producer
+      mb_init(&empty_bar[s], 1);                 // tcgen05.commit
+    }
+    mb_init(&acc_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 0) {  // tensor memory: 128 lanes x 128 fp32 columns
+  if (warp == kMmaWarp) {  // tensor memory: 128 lanes x 128 fp32 columns
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&tmem_holder)),
                  "r"(kTileN)
                  : "memory");
@@ -291,128 +380,191 @@ __global__ void __launch_bounds__(kThreadsG, 1) ffn_gemm_kernel(GemmParams P) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_holder;
-  const uint32_t idesc = idesc_bf16(kTileM, Npad);
-  const int ksteps = K / kTileK;
-  const int kbytes = K / 2, sbytes = K / 32;
   bool timeout = false;
 
-  // Weight row held by tile row r: gate/up interleaves gate row i (even r) and
-  // up row i (odd r) so the epilogue pairs g and u in neighbouring lanes.
-  const int tile_row = tid;  // each thread fills one A row per stage
-  int wrow;
-  if (kind == 0) {
-    const int i = (g.m0 >> 1) + (tile_row >> 1);
-    wrow = (tile_row & 1) ? P.I + i : i;
-  } else {
-    wrow = g.m0 + tile_row;
-  }
-
-  for (int ks = 0; ks < ksteps; ++ks) {
-    const int s = ks % kStagesG;
-    uint8_t *sa = gsm + s * (kStageA + kStageB);
-    uint8_t *sb = sa + kStageA;
-    if (ks >= kStagesG) {  // the MMAs that last read this stage are done
-      if (!mb_wait(&mma_done[s], static_cast<uint32_t>((ks / kStagesG) - 1) & 1u)) timeout = true;
-      tc_fence_after();
+  if (warp < kDqWarps) {
+    // ---------------------------------------------------- dequantisation
+    // thread pair (2r, 2r+1) fills tile row r; gate/up interleaves gate row i
+    // (even r) and up row i (odd r) so the epilogue pairs g and u.
+    const int r = tid >> 1, hf = tid & 1;
+    int wrow;
+    if (kind == 0) {
+      const int i = (g.m0 >> 1) + (r >> 1);
+      wrow = (r & 1) ? P.I + i : i;
+    } else {
+      wrow = g.m0 + r;
     }
-    // A: weight row `wrow`, columns ks*64 .. +63 -> bf16, exact
-    {
-      uint4 c0 = make_uint4(0, 0, 0, 0), c1 = make_uint4(0, 0, 0, 0);
-      float s0 = 0.f, s1 = 0.f;
-      if (present) {
-        const uint8_t *rp = codes + static_cast<size_t>(wrow) * kbytes + ks * 32;
-        c0 = *reinterpret_cast<const uint4 *>(rp);
-        c1 = *reinterpret_cast<const uint4 *>(rp + 16);
-        const uint8_t *sp = scales + static_cast<size_t>(wrow) * sbytes + ks * 2;
-        s0 = e8m0_to_f32(sp[0]);
-        s1 = e8m0_to_f32(sp[1]);
+    const int kbytes = K / 2, sbytes = K / 32;
+    const uint8_t *crow = present ? codes + static_cast<size_t>(wrow) * kbytes : nullptr;
+    const uint8_t *srow = present ? scales + static_cast<size_t>(wrow) * sbytes : nullptr;
+    int smax = 0;
+    if (present)
+      for (int b = hf; b < sbytes; b += 2) smax = max(smax, static_cast<int>(srow[b]));
+    smax = max(smax, __shfl_xor_sync(0xFFFFFFFFu, smax, 1));
+    if (hf == 0) sref_s[r] = smax;
+    uint4 cw = make_uint4(0, 0, 0, 0);
+    int sb = 0;
+    if (present) {  // first K step
+      cw = *reinterpret_cast<const uint4 *>(crow + hf * 16);
+      sb = srow[hf];
+    }
+    for (int ks = 0; ks < ksteps; ++ks) {
+      const int s = ks % kStagesG;
+      const uint32_t lap = static_cast<uint32_t>(ks / kStagesG);
+      // prefetch the next K step while this one is converted
+      uint4 cw_n = make_uint4(0, 0, 0, 0);
+      int sb_n = 0;
+      if (present && ks + 1 < ksteps) {
+        cw_n = *reinterpret_cast<const uint4 *>(crow + (ks + 1) * 32 + hf * 16);
+        sb_n = srow[(ks + 1) * 2 + hf];
       }
-      const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+      if (!mb_wait(&empty_bar[s], (lap & 1u) ^ 1u)) timeout = true;
+      uint8_t *sa = gsm + s * (kStageA + kStageB);
+      const uint32_t mulbits = f16_pow2_bits(sb - smax);
+      const uint32_t mul2 = mulbits | (mulbits << 16);
+      const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {  // 16-byte chunk c = columns 8c .. 8c+7 of the 64
+      for (int c = 0; c < 4; ++c) {  // 16-byte chunk (4*hf + c) = columns 8(4hf+c) .. +7 of the 64
         uint32_t h[4];
         e2m1x8_to_f16x2(words[c], h);
-        const float sc = c < 4 ? s0 : s1;
         uint4 o;
-        o.x = e2m1x2_to_bf16x2_scaled(h[0], sc);
-        o.y = e2m1x2_to_bf16x2_scaled(h[1], sc);
-        o.z = e2m1x2_to_bf16x2_scaled(h[2], sc);
-        o.w = e2m1x2_to_bf16x2_scaled(h[3], sc);
-        *reinterpret_cast<uint4 *>(sa + sw128_off(tile_row, c)) = o;
-      }
-    }
-    // B: token rows, columns ks*64 .. +63 (bf16), zero for padding rows
-    for (int i = tid; i < kTileN * 8; i += kThreadsG) {
-      const int r = i >> 3, c = i & 7;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      const int t = tok_of_row[r];
-      if (t >= 0) {
-        const uint16_t *src = kind == 0 ? P.x + static_cast<size_t>(t) * P.H : P.hrow + static_cast<size_t>(t) * P.I;
-        v = *reinterpret_cast<const uint4 *>(src + ks * kTileK + c * 8);
-      }
-      *reinterpret_cast<uint4 *>(sb + sw128_off(r, c)) = v;
-    }
-    // make the generic-proxy stores visible to the tensor core, then issue
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (tid == 0) {
-      const uint32_t a0 = su32(sa), b0 = su32(sb);
+        uint32_t *op = reinterpret_cast<uint32_t *>(&o);
 #pragma unroll
-      for (int kk = 0; kk < kTileK / 16; ++kk)  // K = 16 per MMA: +32 bytes inside the swizzle atom
-        tc_mma_bf16(tmem, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32), idesc,
-                    (ks > 0 || kk > 0) ? 1u : 0u);
-      tc_commit(&mma_done[s]);
+        for (int m = 0; m < 4; ++m) {
+          const __half2 a = *reinterpret_cast<const __half2 *>(&h[m]);
+          const __half2 b = *reinterpret_cast<const __half2 *>(&mul2);
+          const __half2 prod = __hmul2(a, b);
+          op[m] = *reinterpret_cast<const uint32_t *>(&prod);
+        }
+        *reinterpret_cast<uint4 *>(sa + sw128_off(r, 4 * hf + c)) = o;
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic stores -> tensor core
+      mb_arrive(&full_bar[s]);
+      cw = cw_n;
+      sb = sb_n;
     }
-  }
-  // wait for the last MMAs
-  {
-    const int last = ksteps - 1;
-    if (!mb_wait(&mma_done[last % kStagesG], static_cast<uint32_t>(last / kStagesG) & 1u)) timeout = true;
-    tc_fence_after();
-  }
-  if (timeout) set_status(P.status, K3MOE_DEV_TIMEOUT);
-
-  // ---- epilogue: thread tid holds tile row tid (TMEM lane tid), columns 0..Npad-1
-  float *stage = reinterpret_cast<float *>(gsm);  // [kTileN][kTileM + 1] fp32 transpose buffer (fits in stage 0+1)
-  const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-  for (int c0 = 0; c0 < Npad; c0 += 16) {
-    float v[16];
-    tc_ld16(lane_addr + c0, v);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) stage[(c0 + j) * (kTileM + 1) + tid] = present ? v[j] : 0.f;
-  }
-  __syncthreads();
-  if (kind == 0) {
-    // h[p0 + n][m0/2 + i] = bf16(silu(g) * u), g = row 2i, u = row 2i+1
-    const int ncols = kTileM / 2;
-    for (int idx = tid; idx < g.n * ncols; idx += kThreadsG) {
-      const int n = idx / ncols, i = idx % ncols;
-      const float gg = stage[n * (kTileM + 1) + 2 * i];
-      const float uu = stage[n * (kTileM + 1) + 2 * i + 1];
-      const float hv = (gg / (1.0f + expf(-gg))) * uu;
-      P.hrow[static_cast<size_t>(g.p0 + n) * P.I + (g.m0 >> 1) + i] = f32_to_bf16_rne(hv);
+  } else if (warp == kTmaWarp) {
+    // ---------------------------------------------------- activation tiles (TMA)
+    if (lane == 0) {
+      for (int ks = 0; ks < ksteps; ++ks) {
+        const int s = ks % kStagesG;
+        const uint32_t lap = static_cast<uint32_t>(ks / kStagesG);
+        if (!mb_wait(&empty_bar[s], (lap & 1u) ^ 1u)) timeout = true;
+        uint8_t *sbuf = gsm + s * (kStageA + kStageB) + kStageA;
+        mb_arrive_tx(&full_bar[s], kStageB);
+        tma_load_2d(sbuf, &bmap, ks * kTileK, g.p0, &full_bar[s]);
+      }
     }
   } else {
-    for (int idx = tid; idx < g.n * kTileM; idx += kThreadsG) {
-      const int n = idx / kTileM, r = idx % kTileM;
-      P.Y[static_cast<size_t>(g.p0 + n) * P.H + g.m0 + r] = stage[n * (kTileM + 1) + r];
+    // ---------------------------------------------------- MMA issue
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16(kTileM, Npad);
+      for (int ks = 0; ks < ksteps; ++ks) {
+        const int s = ks % kStagesG;
+        const uint32_t lap = static_cast<uint32_t>(ks / kStagesG);
+        if (!mb_wait(&full_bar[s], lap & 1u)) timeout = true;
+        tc_fence_after();
+        const uint32_t a0 = su32(gsm + s * (kStageA + kStageB)), b0 = a0 + kStageA;
+#pragma unroll
+        for (int kk = 0; kk < kTileK / 16; ++kk)  // K = 16 per MMA: +32 bytes inside the swizzle atom
+          tc_mma_f16(tmem, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32), idesc,
+                     (ks > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&empty_bar[s]);
+      }
+      tc_commit(&acc_bar);
     }
   }
+
+  // ---- epilogue (dequantisation warps): TMEM lane quadrant = warp % 4,
+  //      warps 0-3 take columns [0, 64), warps 4-7 columns [64, 128)
+  if (warp < kDqWarps) {
+    if (!mb_wait(&acc_bar, 0)) timeout = true;
+    tc_fence_after();
+    float *stage = reinterpret_cast<float *>(gsm);  // [kTileN][kTileM + 1]
+    const int q = warp & 3, row = 32 * q + lane;
+    const int cbeg = (warp >> 2) * 64;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * q) << 16);
+    for (int c0 = cbeg; c0 < cbeg + 64 && c0 < Npad; c0 += 16) {
+      float v[16];
+      tc_ld16(lane_addr + c0, v);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) stage[(c0 + j) * (kTileM + 1) + row] = v[j];
+    }
+    tc_fence_before();
+    asm volatile("bar.sync 1, %0;" ::"r"(kDqWarps * 32) : "memory");
+    if (kind == 0) {
+      // h[p0 + n][m0/2 + i] = bf16(silu(g) * u), g = row 2i, u = row 2i+1
+      const int ncols = kTileM / 2;
+      for (int idx = tid; idx < g.n * ncols; idx += kDqWarps * 32) {
+        const int n = idx / ncols, i = idx % ncols;
+        float hv = 0.f;
+        if (present) {
+          const float gg = mul_pow2(stage[n * (kTileM + 1) + 2 * i], sref_s[2 * i] - 127 + bexp_s[n]);
+          const float uu = mul_pow2(stage[n * (kTileM + 1) + 2 * i + 1], sref_s[2 * i + 1] - 127 + bexp_s[n]);
+          hv = (gg / (1.0f + expf(-gg))) * uu;
+        }
+        P.hrow[static_cast<size_t>(g.p0 + n) * P.I + (g.m0 >> 1) + i] = f32_to_bf16_rne(hv);
+      }
+    } else {
+      for (int idx = tid; idx < g.n * kTileM; idx += kDqWarps * 32) {
+        const int n = idx / kTileM, r = idx % kTileM;
+        P.Y[static_cast<size_t>(g.p0 + n) * P.H + g.m0 + r] =
+            present ? mul_pow2(stage[n * (kTileM + 1) + r], sref_s[r] - 127 + bexp_s[n]) : 0.f;
+      }
+    }
+  }
+  if (timeout) set_status(P.status, K3MOE_DEV_TIMEOUT);
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTileN) : "memory");
   }
 }
 
 // ----------------------------------------------------------------------------
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D map over rows x K of 16-bit values: box = 64 (K) x 128 rows, 128B swizzle,
+// rows past the end read as zero.
+bool make_row_map(CUtensorMap *m, void *base, int rows, int K) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  const cuuint32_t box[2] = {kTileK, kTileN};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 size_t ffn_gemm_workspace(const k3moe_shape &s) { return gemm_ws(s.T, s.H, s.I, s.E, s.k).total; }
 
 bool ffn_gemm_supported(const k3moe_shape &s) {
-  return (2 * s.I) % kTileM == 0 && s.H % kTileM == 0 && s.H % kTileK == 0 && s.I % kTileK == 0;
+  return (2 * s.I) % kTileM == 0 && s.H % kTileM == 0 && s.H % kTileK == 0 && s.I % kTileK == 0 &&
+         encode_tiled() != nullptr;
 }
 
 int launch_ffn_gemm(const k3moe_shape &s, const uint16_t *x, const k3moe_weights &w, const int32_t *offsets,
@@ -428,36 +580,52 @@ int launch_ffn_gemm(const k3moe_shape &s, const uint16_t *x, const k3moe_weights
   int32_t *scnt = reinterpret_cast<int32_t *>(base + L.scnt);
   int32_t *pgu = reinterpret_cast<int32_t *>(base + L.pref_gu);
   int32_t *pdn = reinterpret_cast<int32_t *>(base + L.pref_dn);
+  uint16_t *xg = reinterpret_cast<uint16_t *>(base + L.xg);
+  int32_t *xexp = reinterpret_cast<int32_t *>(base + L.xexp);
+  uint16_t *hrow = reinterpret_cast<uint16_t *>(base + L.hrow);
+  uint16_t *h16 = reinterpret_cast<uint16_t *>(base + L.h16);
+  int32_t *hexp = reinterpret_cast<int32_t *>(base + L.hexp);
+  CUtensorMap xmap, hmap;
+  if (!make_row_map(&xmap, xg, A, s.H) || !make_row_map(&hmap, h16, A, s.I)) return -1;
   if (launch_pdl(gemm_prep_kernel, dim3(1), dim3(32), 0, st, offsets, s.E, A, mt_gu, mt_dn, active, meta, sp0,
                  scnt, pgu, pdn, status) != cudaSuccess)
     return -1;
-  // upper bound of the token tiles: sum_e ceil(n_e / 128) <= A / 128 + min(A, E)
-  const long long ntile_max = A / kTileN + (A < s.E ? A : s.E);
-  const size_t smem = kGemmSmem;
-  if (cudaFuncSetAttribute(ffn_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+  if (launch_pdl(gemm_rows_to_f16_kernel, dim3(A), dim3(256), 0, st, x, perm, s.k, A, s.H, xg, xexp, status) !=
       cudaSuccess)
     return -1;
+  // upper bound of the token tiles: sum_e ceil(n_e / 128) <= A / 128 + min(A, E)
+  const long long ntile_max = A / kTileN + (A < s.E ? A : s.E);
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(ffn_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem) !=
+        cudaSuccess)
+      return -1;
+    attr = true;
+  }
   GemmParams P;
   P.w = w;
-  P.T = s.T; P.H = s.H; P.I = s.I; P.E = s.E; P.k = s.k; P.A = A;
-  P.perm = perm;
-  P.x = x;
+  P.H = s.H; P.I = s.I; P.A = A;
   P.active = active;
   P.meta = meta;
   P.slot_p0 = sp0;
   P.slot_cnt = scnt;
-  P.hrow = reinterpret_cast<uint16_t *>(base + L.hrow);
+  P.hrow = hrow;
   P.Y = Y;
   P.status = status;
   P.kind = 0;
   P.pref = pgu;
-  if (launch_pdl(ffn_gemm_kernel, dim3(static_cast<unsigned>(ntile_max * mt_gu)), dim3(kThreadsG), smem, st, P) !=
-      cudaSuccess)
+  P.bexp = xexp;
+  if (launch_pdl(ffn_gemm_kernel, dim3(static_cast<unsigned>(ntile_max * mt_gu)), dim3(kThreadsG), kGemmSmem, st,
+                 xmap, P) != cudaSuccess)
+    return -1;
+  if (launch_pdl(gemm_rows_to_f16_kernel, dim3(A), dim3(256), 0, st, static_cast<const uint16_t *>(hrow),
+                 static_cast<const int32_t *>(nullptr), 1, A, s.I, h16, hexp, status) != cudaSuccess)
     return -1;
   P.kind = 1;
   P.pref = pdn;
-  if (launch_pdl(ffn_gemm_kernel, dim3(static_cast<unsigned>(ntile_max * mt_dn)), dim3(kThreadsG), smem, st, P) !=
-      cudaSuccess)
+  P.bexp = hexp;
+  if (launch_pdl(ffn_gemm_kernel, dim3(static_cast<unsigned>(ntile_max * mt_dn)), dim3(kThreadsG), kGemmSmem, st,
+                 hmap, P) != cudaSuccess)
     return -1;
   return 0;
 }
