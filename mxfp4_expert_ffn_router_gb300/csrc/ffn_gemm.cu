@@ -48,8 +48,9 @@ constexpr int kTileM = 128;     // weight rows per tile
 constexpr int kTileN = 128;     // tokens per tile (max)
 constexpr int kTileK = 64;      // K per stage: one 128-byte swizzle atom of 16-bit values
 constexpr int kStagesG = 3;
-constexpr int kStageA = kTileM * kTileK * 2;  // 16 KiB
-constexpr int kStageB = kTileN * kTileK * 2;  // 16 KiB
+constexpr int kStageB = kTileN * kTileK * 2;  // 16 KiB of shared memory per stage (activation tile)
+constexpr int kAcols = kTileK / 2;             // tensor-memory columns of one A stage (f16 pairs)
+constexpr int kTmemCols = 256;                 // accumulator (kTileN columns) + kStagesG A stages
 constexpr long long kSpinG = 1LL << 22;
 
 __device__ __forceinline__ uint32_t su32(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
@@ -115,13 +116,24 @@ __device__ __forceinline__ uint32_t idesc_f16(int M, int N) {
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
-__device__ __forceinline__ void tc_mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                            uint32_t accumulate) {
+// A operand from tensor memory (M lanes x K/2 columns of f16 pairs), B from shared memory.
+__device__ __forceinline__ void tc_mma_f16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+// 32 lanes x 32 bit, 16 consecutive columns per thread, registers -> tensor memory.
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void tc_commit(uint64_t *bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
@@ -141,10 +153,6 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Byte offset of 16-byte chunk c (0..7) of row r in a 128B-swizzled K-major tile.
-__device__ __forceinline__ uint32_t sw128_off(int r, int c) {
-  return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
-}
 
 // multiply by 2^p for |p| <= 252 (two exact steps)
 __device__ __forceinline__ float mul_pow2(float v, int p) {
@@ -328,10 +336,11 @@ struct GemmParams {
   int32_t *status;
 };
 
-// dynamic shared memory: 1024 bytes of alignment slack + the stages (the epilogue
-// transpose buffer [kTileN][kTileM + 1] fp32 reuses them)
+// dynamic shared memory: 1024 bytes of alignment slack + the activation stages
+// (the epilogue transpose buffer [kTileN][kTileM + 1] fp32 reuses them)
 constexpr int kEpiBytes = kTileN * (kTileM + 1) * 4;
-constexpr int kStageBytes = kStagesG * (kStageA + kStageB);
+constexpr int kStageBytes = kStagesG * kStageB;
+static_assert(kTileN + kStagesG * kAcols <= kTmemCols, "tensor-memory budget");
 constexpr int kGemmSmem = 1024 + (kStageBytes > kEpiBytes ? kStageBytes : kEpiBytes);
 
 __global__ void __launch_bounds__(kThreadsG, 1)
@@ -342,6 +351,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
   __shared__ uint64_t full_bar[kStagesG], empty_bar[kStagesG], acc_bar;
   __shared__ uint32_t tmem_holder;
   __shared__ int sref_s[kTileM];  // largest scale byte of each tile row
+  __shared__ int smax_s[kTileM];  // partial maxima (second K half)
   __shared__ int bexp_s[kTileN];  // activation prescale exponent of each token column
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_wait();
@@ -370,9 +380,9 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     mb_init(&acc_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == kMmaWarp) {  // tensor memory: 128 lanes x 128 fp32 columns
+  if (warp == kMmaWarp) {  // tensor memory: accumulator columns [0, 128), A stages after
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&tmem_holder)),
-                 "r"(kTileN)
+                 "r"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -384,9 +394,10 @@ __global__ void __launch_bounds__(kThreadsG, 1)
 
   if (warp < kDqWarps) {
     // ---------------------------------------------------- dequantisation
-    // thread pair (2r, 2r+1) fills tile row r; gate/up interleaves gate row i
-    // (even r) and up row i (odd r) so the epilogue pairs g and u.
-    const int r = tid >> 1, hf = tid & 1;
+    // warp w fills tensor-memory lane quadrant w % 4 (tile rows 32(w%4) + lane)
+    // for K half w / 4 of each stage; gate/up interleaves gate row i (even tile
+    // row) and up row i (odd) so the epilogue pairs g and u.
+    const int r = 32 * (warp & 3) + lane, hf = warp >> 2;
     int wrow;
     if (kind == 0) {
       const int i = (g.m0 >> 1) + (r >> 1);
@@ -400,48 +411,73 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     int smax = 0;
     if (present)
       for (int b = hf; b < sbytes; b += 2) smax = max(smax, static_cast<int>(srow[b]));
-    smax = max(smax, __shfl_xor_sync(0xFFFFFFFFu, smax, 1));
-    if (hf == 0) sref_s[r] = smax;
-    uint4 cw = make_uint4(0, 0, 0, 0);
-    int sb = 0;
-    if (present) {  // first K step
-      cw = *reinterpret_cast<const uint4 *>(crow + hf * 16);
-      sb = srow[hf];
+    if (hf == 1) smax_s[r] = smax;  // combine the two K halves of the row
+    asm volatile("bar.sync 2, %0;" ::"r"(kDqWarps * 32) : "memory");
+    if (hf == 0) {
+      smax = max(smax, smax_s[r]);
+      sref_s[r] = smax;
     }
-    for (int ks = 0; ks < ksteps; ++ks) {
-      const int s = ks % kStagesG;
-      const uint32_t lap = static_cast<uint32_t>(ks / kStagesG);
-      // prefetch the next K step while this one is converted
-      uint4 cw_n = make_uint4(0, 0, 0, 0);
-      int sb_n = 0;
-      if (present && ks + 1 < ksteps) {
-        cw_n = *reinterpret_cast<const uint4 *>(crow + (ks + 1) * 32 + hf * 16);
-        sb_n = srow[(ks + 1) * 2 + hf];
+    asm volatile("bar.sync 2, %0;" ::"r"(kDqWarps * 32) : "memory");
+    smax = sref_s[r];
+    const uint32_t a_lane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    // weight codes are prefetched kPf K steps ahead (two register batches), so
+    // each thread keeps 4-8 sixteen-byte loads in flight
+    constexpr int kPf = 4;
+    uint4 cur[kPf], nxt[kPf];
+    int scur[kPf], snxt[kPf];
+#pragma unroll
+    for (int j = 0; j < kPf; ++j) {
+      cur[j] = make_uint4(0, 0, 0, 0);
+      scur[j] = 0;
+      if (present && j < ksteps) {
+        cur[j] = *reinterpret_cast<const uint4 *>(crow + j * 32 + hf * 16);
+        scur[j] = srow[j * 2 + hf];
       }
-      if (!mb_wait(&empty_bar[s], (lap & 1u) ^ 1u)) timeout = true;
-      uint8_t *sa = gsm + s * (kStageA + kStageB);
-      const uint32_t mulbits = f16_pow2_bits(sb - smax);
-      const uint32_t mul2 = mulbits | (mulbits << 16);
-      const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+    }
+    for (int kb = 0; kb < ksteps; kb += kPf) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {  // 16-byte chunk (4*hf + c) = columns 8(4hf+c) .. +7 of the 64
-        uint32_t h[4];
-        e2m1x8_to_f16x2(words[c], h);
-        uint4 o;
-        uint32_t *op = reinterpret_cast<uint32_t *>(&o);
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const __half2 a = *reinterpret_cast<const __half2 *>(&h[m]);
-          const __half2 b = *reinterpret_cast<const __half2 *>(&mul2);
-          const __half2 prod = __hmul2(a, b);
-          op[m] = *reinterpret_cast<const uint32_t *>(&prod);
+      for (int j = 0; j < kPf; ++j) {
+        const int k2 = kb + kPf + j;
+        nxt[j] = make_uint4(0, 0, 0, 0);
+        snxt[j] = 0;
+        if (present && k2 < ksteps) {
+          nxt[j] = *reinterpret_cast<const uint4 *>(crow + k2 * 32 + hf * 16);
+          snxt[j] = srow[k2 * 2 + hf];
         }
-        *reinterpret_cast<uint4 *>(sa + sw128_off(r, 4 * hf + c)) = o;
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic stores -> tensor core
-      mb_arrive(&full_bar[s]);
-      cw = cw_n;
-      sb = sb_n;
+#pragma unroll
+      for (int j = 0; j < kPf; ++j) {
+        const int ks = kb + j;
+        if (ks < ksteps) {
+          const int s = ks % kStagesG;
+          const uint32_t lap = static_cast<uint32_t>(ks / kStagesG);
+          if (!mb_wait(&empty_bar[s], (lap & 1u) ^ 1u)) timeout = true;
+          const uint32_t mulbits = f16_pow2_bits(scur[j] - smax);
+          const uint32_t mul2 = mulbits | (mulbits << 16);
+          const uint32_t words[4] = {cur[j].x, cur[j].y, cur[j].z, cur[j].w};
+          uint32_t o[16];  // 32 f16 = columns 16*hf .. 16*hf+15 of the stage (two K values per column)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t h[4];
+            e2m1x8_to_f16x2(words[c], h);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              const __half2 a = *reinterpret_cast<const __half2 *>(&h[m]);
+              const __half2 b = *reinterpret_cast<const __half2 *>(&mul2);
+              const __half2 prod = __hmul2(a, b);
+              o[4 * c + m] = *reinterpret_cast<const uint32_t *>(&prod);
+            }
+          }
+          tc_st16(a_lane + kTileN + s * kAcols + 16 * hf, o);
+          tc_fence_before();
+          mb_arrive(&full_bar[s]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kPf; ++j) {
+        cur[j] = nxt[j];
+        scur[j] = snxt[j];
+      }
     }
   } else if (warp == kTmaWarp) {
     // ---------------------------------------------------- activation tiles (TMA)
@@ -450,7 +486,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         const int s = ks % kStagesG;
         const uint32_t lap = static_cast<uint32_t>(ks / kStagesG);
         if (!mb_wait(&empty_bar[s], (lap & 1u) ^ 1u)) timeout = true;
-        uint8_t *sbuf = gsm + s * (kStageA + kStageB) + kStageA;
+        uint8_t *sbuf = gsm + s * kStageB;
         mb_arrive_tx(&full_bar[s], kStageB);
         tma_load_2d(sbuf, &bmap, ks * kTileK, g.p0, &full_bar[s]);
       }
@@ -464,11 +500,11 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         const uint32_t lap = static_cast<uint32_t>(ks / kStagesG);
         if (!mb_wait(&full_bar[s], lap & 1u)) timeout = true;
         tc_fence_after();
-        const uint32_t a0 = su32(gsm + s * (kStageA + kStageB)), b0 = a0 + kStageA;
+        const uint32_t b0 = su32(gsm + s * kStageB);
+        const uint32_t a0 = tmem + kTileN + s * kAcols;
 #pragma unroll
-        for (int kk = 0; kk < kTileK / 16; ++kk)  // K = 16 per MMA: +32 bytes inside the swizzle atom
-          tc_mma_f16(tmem, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32), idesc,
-                     (ks > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kTileK / 16; ++kk)  // K = 16 per MMA: A +8 columns, B +32 bytes in the atom
+          tc_mma_f16_ta(tmem, a0 + kk * 8, smem_desc_sw128(b0 + kk * 32), idesc, (ks > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&empty_bar[s]);
       }
       tc_commit(&acc_bar);
@@ -518,7 +554,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
   __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTileN) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
 }
 
