@@ -47,7 +47,7 @@ constexpr int kThreadsG = (kDqWarps + 2) * 32;  // 320
 constexpr int kTileM = 128;     // weight rows per tile
 constexpr int kTileN = 128;     // tokens per tile (max)
 constexpr int kTileK = 64;      // K per stage: one 128-byte swizzle atom of 16-bit values
-constexpr int kStagesG = 3;
+constexpr int kStagesG = 4;
 constexpr int kStageB = kTileN * kTileK * 2;  // 16 KiB of shared memory per stage (activation tile)
 constexpr int kAcols = kTileK / 2;             // tensor-memory columns of one A stage (f16 pairs)
 constexpr int kTmemCols = 256;                 // accumulator (kTileN columns) + kStagesG A stages
@@ -408,9 +408,27 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     const int kbytes = K / 2, sbytes = K / 32;
     const uint8_t *crow = present ? codes + static_cast<size_t>(wrow) * kbytes : nullptr;
     const uint8_t *srow = present ? scales + static_cast<size_t>(wrow) * sbytes : nullptr;
+    // largest block-scale byte of the row (each K half scans half of the row's
+    // scale bytes; 16-byte loads when the row is 16-byte aligned)
     int smax = 0;
-    if (present)
-      for (int b = hf; b < sbytes; b += 2) smax = max(smax, static_cast<int>(srow[b]));
+    if (present) {
+      const int half = sbytes / 2, b0 = hf * half, b1 = hf ? sbytes : half;
+      if ((reinterpret_cast<uintptr_t>(srow + b0) & 15u) == 0 && (half & 15) == 0) {
+        for (int b = b0; b < b1; b += 16) {
+          const uint4 v = *reinterpret_cast<const uint4 *>(srow + b);
+          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            smax = max(smax, static_cast<int>(w4[m] & 0xFFu));
+            smax = max(smax, static_cast<int>((w4[m] >> 8) & 0xFFu));
+            smax = max(smax, static_cast<int>((w4[m] >> 16) & 0xFFu));
+            smax = max(smax, static_cast<int>(w4[m] >> 24));
+          }
+        }
+      } else {
+        for (int b = b0; b < b1; ++b) smax = max(smax, static_cast<int>(srow[b]));
+      }
+    }
     if (hf == 1) smax_s[r] = smax;  // combine the two K halves of the row
     asm volatile("bar.sync 2, %0;" ::"r"(kDqWarps * 32) : "memory");
     if (hf == 0) {
