@@ -51,6 +51,15 @@ constexpr int kStagesG = 4;
 constexpr int kStageB = kTileN * kTileK * 2;  // 16 KiB of shared memory per stage (activation tile)
 constexpr int kAcols = kTileK / 2;             // tensor-memory columns of one A stage (f16 pairs)
 constexpr int kTmemCols = 256;                 // accumulator (kTileN columns) + kStagesG A stages
+// weight codes reach shared memory by 2-D TMA boxes of 128 code bytes (256 K
+// values) x 64 rows, 128-byte swizzled: 16-byte chunk c of tile row r sits at
+// r * 128 + 16 * (c ^ (r % 8)), so the reads of 8 consecutive rows hit distinct banks
+constexpr int kWK = 256;
+constexpr int kWSteps = kWK / kTileK;           // MMA K steps per weight stage
+constexpr int kWStages = 2;
+constexpr int kWBoxRows = 64;
+constexpr int kWStageB = kTileM * (kWK / 2);    // 16 KiB
+constexpr int kMapBytes = 128;                  // one CUtensorMap
 constexpr long long kSpinG = 1LL << 22;
 
 __device__ __forceinline__ uint32_t su32(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
@@ -199,7 +208,7 @@ __device__ __forceinline__ bool decode_tile(const int32_t *pref, const int32_t *
 }
 
 struct GemmWs {
-  size_t active, meta, sp0, scnt, pref_gu, pref_dn, xg, xexp, hrow, h16, hexp, total;
+  size_t active, meta, sp0, scnt, pref_gu, pref_dn, maps, xg, xexp, hrow, h16, hexp, total;
 };
 __host__ __device__ inline size_t g256(size_t v) { return (v + 255) & ~size_t(255); }
 __host__ __device__ inline GemmWs gemm_ws(int T, int H, int I, int E, int k) {
@@ -212,6 +221,7 @@ __host__ __device__ inline GemmWs gemm_ws(int T, int H, int I, int E, int k) {
   w.scnt = o;    o = g256(o + sizeof(int32_t) * E);
   w.pref_gu = o; o = g256(o + sizeof(int32_t) * E);
   w.pref_dn = o; o = g256(o + sizeof(int32_t) * E);
+  w.maps = o;    o = g256(o + static_cast<size_t>(kMapBytes) * 2 * E);  // weight-code tensor maps per active slot
   w.xg = o;      o = g256(o + sizeof(uint16_t) * A * H);  // x rows in bucket order, prescaled f16
   w.xexp = o;    o = g256(o + sizeof(int32_t) * (A ? A : 1));
   w.hrow = o;    o = g256(o + sizeof(uint16_t) * A * I);  // h, bf16 (the rounding point)
@@ -269,6 +279,34 @@ __global__ void __launch_bounds__(32)
     meta[2] = bad ? 0 : sd;
     if (bad) set_status(status, K3MOE_DEV_BOUNDS);
   }
+}
+
+// Tensor maps of the active experts' weight codes: maps[u] (w13) and
+// maps[E + u] (w2) for active slot u, each the host-encoded template with its
+// global address replaced by the expert's code pointer.  Experts whose code
+// pointers are NULL or not 16-byte aligned keep the template's address; the
+// GEMM treats them as absent and never loads through their map.
+__global__ void __launch_bounds__(128)
+    gemm_maps_kernel(const __grid_constant__ CUtensorMap t13, const __grid_constant__ CUtensorMap t2,
+                     k3moe_weights w, const int32_t *__restrict__ active, const int32_t *__restrict__ meta, int E,
+                     uint8_t *__restrict__ maps) {
+  pdl_wait();
+  pdl_trigger();
+  const int na = meta[0];
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= 2 * na) return;
+  const int which = t >= na, u = which ? t - na : t;
+  const int e = active[u];
+  const uint4 *tmpl = reinterpret_cast<const uint4 *>(which ? &t2 : &t13);
+  uint8_t *dst = maps + static_cast<size_t>(which * E + u) * kMapBytes;
+  uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+  for (int i = 0; i < kMapBytes / 16; ++i) d4[i] = tmpl[i];
+  const uint8_t *codes = which ? w.w2_codes[e] : w.w13_codes[e];
+  if (codes && (reinterpret_cast<uintptr_t>(codes) & 15u) == 0)
+    asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;" ::"l"(dst), "l"(codes)
+                 : "memory");
+  asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
 }
 
 // Row p of `dst` (f16) = row of `src` (bf16, K values) times 2^-e, e chosen per
@@ -329,6 +367,8 @@ struct GemmParams {
   k3moe_weights w;
   int H, I, A;
   const int32_t *active, *meta, *slot_p0, *slot_cnt, *pref;
+  const uint8_t *maps;        // weight-code tensor maps per active slot (w13 at u, w2 at E + u)
+  int E;
   const int32_t *bexp;        // per bucket position: prescale exponent of the activation row
   uint16_t *hrow;             // [A][I] bf16 (gate/up output)
   float *Y;                   // [A][H]
@@ -336,12 +376,21 @@ struct GemmParams {
   int32_t *status;
 };
 
-// dynamic shared memory: 1024 bytes of alignment slack + the activation stages
-// (the epilogue transpose buffer [kTileN][kTileM + 1] fp32 reuses them)
+// dynamic shared memory: 1024 bytes of alignment slack, the activation stages,
+// then the weight stages (the epilogue transpose buffer [kTileN][kTileM + 1]
+// fp32 reuses them once every stage has been consumed)
 constexpr int kEpiBytes = kTileN * (kTileM + 1) * 4;
-constexpr int kStageBytes = kStagesG * kStageB;
+constexpr int kStageBytes = kStagesG * kStageB + kWStages * kWStageB;
 static_assert(kTileN + kStagesG * kAcols <= kTmemCols, "tensor-memory budget");
+static_assert(kWStages >= 2 && kTileM == 2 * kWBoxRows, "weight ring");
 constexpr int kGemmSmem = 1024 + (kStageBytes > kEpiBytes ? kStageBytes : kEpiBytes);
+
+// weight row of tile row r: a gate/up tile holds gate rows m0/2 + [0, 64) in
+// tile rows [0, 64) and the matching up rows I + m0/2 + [0, 64) in [64, 128)
+__device__ __forceinline__ int tile_wrow(int kind, int m0, int r, int I) {
+  if (kind == 0) return (r < kWBoxRows ? 0 : I - kWBoxRows) + (m0 >> 1) + r;
+  return m0 + r;
+}
 
 __global__ void __launch_bounds__(kThreadsG, 1)
     ffn_gemm_kernel(const __grid_constant__ CUtensorMap bmap, GemmParams P) {
@@ -349,6 +398,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
   // the 128B-swizzle atoms need 1024-byte aligned shared addresses: align explicitly
   uint8_t *gsm = gsm_raw + ((1024u - (su32(gsm_raw) & 1023u)) & 1023u);
   __shared__ uint64_t full_bar[kStagesG], empty_bar[kStagesG], acc_bar;
+  __shared__ uint64_t wfull_bar[kWStages], wempty_bar[kWStages];
   __shared__ uint32_t tmem_holder;
   __shared__ int sref_s[kTileM];  // largest scale byte of each tile row
   __shared__ int smax_s[kTileM];  // partial maxima (second K half)
@@ -368,8 +418,8 @@ __global__ void __launch_bounds__(kThreadsG, 1)
   const uint8_t *c13 = P.w.w13_codes[g.e], *s13 = P.w.w13_scales[g.e];
   const uint8_t *c2 = P.w.w2_codes[g.e], *s2 = P.w.w2_scales[g.e];
   const uintptr_t al = reinterpret_cast<uintptr_t>(c13) | reinterpret_cast<uintptr_t>(c2);
-  const bool present = c13 && s13 && c2 && s2 && (al & 15u) == 0;  // 16-byte code loads
-  const uint8_t *codes = kind == 0 ? c13 : c2, *scales = kind == 0 ? s13 : s2;
+  const bool present = c13 && s13 && c2 && s2 && (al & 15u) == 0;  // TMA needs 16-byte aligned code rows
+  const uint8_t *scales = kind == 0 ? s13 : s2;
 
   if (tid < kTileN) bexp_s[tid] = tid < g.n ? P.bexp[g.p0 + tid] : 0;
   if (tid == 0) {
@@ -378,6 +428,10 @@ __global__ void __launch_bounds__(kThreadsG, 1)
       mb_init(&empty_bar[s], 1);                 // tcgen05.commit
     }
     mb_init(&acc_bar, 1);
+    for (int s = 0; s < kWStages; ++s) {
+      mb_init(&wfull_bar[s], 1);          // producer arrive + bulk-copy bytes
+      mb_init(&wempty_bar[s], kDqWarps);  // one arrival per dequantising warp
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == kMmaWarp) {  // tensor memory: accumulator columns [0, 128), A stages after
@@ -398,36 +452,28 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     // for K half w / 4 of each stage; gate/up interleaves gate row i (even tile
     // row) and up row i (odd) so the epilogue pairs g and u.
     const int r = 32 * (warp & 3) + lane, hf = warp >> 2;
-    int wrow;
-    if (kind == 0) {
-      const int i = (g.m0 >> 1) + (r >> 1);
-      wrow = (r & 1) ? P.I + i : i;
-    } else {
-      wrow = g.m0 + r;
-    }
-    const int kbytes = K / 2, sbytes = K / 32;
-    const uint8_t *crow = present ? codes + static_cast<size_t>(wrow) * kbytes : nullptr;
+    const int wrow = tile_wrow(kind, g.m0, r, P.I);
+    const int sbytes = K / 32;
     const uint8_t *srow = present ? scales + static_cast<size_t>(wrow) * sbytes : nullptr;
-    // largest block-scale byte of the row (each K half scans half of the row's
-    // scale bytes; 16-byte loads when the row is 16-byte aligned)
+    // the row's scale bytes come 16 at a time (8 K steps) when the row is 16-byte aligned
+    const bool svec = present && (sbytes & 15) == 0 && (reinterpret_cast<uintptr_t>(srow) & 15u) == 0;
+    // largest block-scale byte of the row (the two K halves scan alternate
+    // 16-byte chunks of the row's scale bytes)
     int smax = 0;
-    if (present) {
-      const int half = sbytes / 2, b0 = hf * half, b1 = hf ? sbytes : half;
-      if ((reinterpret_cast<uintptr_t>(srow + b0) & 15u) == 0 && (half & 15) == 0) {
-        for (int b = b0; b < b1; b += 16) {
-          const uint4 v = *reinterpret_cast<const uint4 *>(srow + b);
-          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+    if (svec) {
+      for (int b = 16 * hf; b < sbytes; b += 32) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(srow + b);
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            smax = max(smax, static_cast<int>(w4[m] & 0xFFu));
-            smax = max(smax, static_cast<int>((w4[m] >> 8) & 0xFFu));
-            smax = max(smax, static_cast<int>((w4[m] >> 16) & 0xFFu));
-            smax = max(smax, static_cast<int>(w4[m] >> 24));
-          }
+        for (int m = 0; m < 4; ++m) {
+          smax = max(smax, static_cast<int>(w4[m] & 0xFFu));
+          smax = max(smax, static_cast<int>((w4[m] >> 8) & 0xFFu));
+          smax = max(smax, static_cast<int>((w4[m] >> 16) & 0xFFu));
+          smax = max(smax, static_cast<int>(w4[m] >> 24));
         }
-      } else {
-        for (int b = b0; b < b1; ++b) smax = max(smax, static_cast<int>(srow[b]));
       }
+    } else if (present) {
+      for (int b = hf; b < sbytes; b += 2) smax = max(smax, static_cast<int>(srow[b]));
     }
     if (hf == 1) smax_s[r] = smax;  // combine the two K halves of the row
     asm volatile("bar.sync 2, %0;" ::"r"(kDqWarps * 32) : "memory");
@@ -438,69 +484,86 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     asm volatile("bar.sync 2, %0;" ::"r"(kDqWarps * 32) : "memory");
     smax = sref_s[r];
     const uint32_t a_lane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-    // weight codes are prefetched kPf K steps ahead (two register batches), so
-    // each thread keeps 4-8 sixteen-byte loads in flight
-    constexpr int kPf = 4;
-    uint4 cur[kPf], nxt[kPf];
-    int scur[kPf], snxt[kPf];
+    const uint8_t *wsm = gsm + kStagesG * kStageB + r * (kWK / 2);
+    // K steps in groups of 8 (a 16-byte window of the row's scale bytes, two
+    // weight stages); the next window's scales are loaded one group ahead
+    uint4 scv = make_uint4(0, 0, 0, 0);
+    if (svec) scv = *reinterpret_cast<const uint4 *>(srow);
+    for (int kb = 0; kb < ksteps; kb += 8) {
+      uint4 scn = make_uint4(0, 0, 0, 0);
+      if (svec && kb + 8 < ksteps) scn = *reinterpret_cast<const uint4 *>(srow + 2 * (kb + 8));
+      const uint32_t sw[4] = {scv.x, scv.y, scv.z, scv.w};
 #pragma unroll
-    for (int j = 0; j < kPf; ++j) {
-      cur[j] = make_uint4(0, 0, 0, 0);
-      scur[j] = 0;
-      if (present && j < ksteps) {
-        cur[j] = *reinterpret_cast<const uint4 *>(crow + j * 32 + hf * 16);
-        scur[j] = srow[j * 2 + hf];
-      }
-    }
-    for (int kb = 0; kb < ksteps; kb += kPf) {
-#pragma unroll
-      for (int j = 0; j < kPf; ++j) {
-        const int k2 = kb + kPf + j;
-        nxt[j] = make_uint4(0, 0, 0, 0);
-        snxt[j] = 0;
-        if (present && k2 < ksteps) {
-          nxt[j] = *reinterpret_cast<const uint4 *>(crow + k2 * 32 + hf * 16);
-          snxt[j] = srow[k2 * 2 + hf];
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < kPf; ++j) {
+      for (int j = 0; j < 8; ++j) {
         const int ks = kb + j;
-        if (ks < ksteps) {
-          const int s = ks % kStagesG;
-          const uint32_t lap = static_cast<uint32_t>(ks / kStagesG);
-          if (!mb_wait(&empty_bar[s], (lap & 1u) ^ 1u)) timeout = true;
-          const uint32_t mulbits = f16_pow2_bits(scur[j] - smax);
-          const uint32_t mul2 = mulbits | (mulbits << 16);
-          const uint32_t words[4] = {cur[j].x, cur[j].y, cur[j].z, cur[j].w};
-          uint32_t o[16];  // 32 f16 = columns 16*hf .. 16*hf+15 of the stage (two K values per column)
+        if (ks >= ksteps) break;
+        const int wst = ks / kWSteps, ws = wst % kWStages;
+        if ((j % kWSteps) == 0 && !mb_wait(&wfull_bar[ws], static_cast<uint32_t>(wst / kWStages) & 1u)) timeout = true;
+        int sbyte = 0;
+        if (svec) sbyte = static_cast<int>((sw[j >> 1] >> (16 * (j & 1) + 8 * hf)) & 0xFFu);
+        else if (present) sbyte = srow[2 * ks + hf];
+        const int s = ks % kStagesG;
+        const uint32_t lap = static_cast<uint32_t>(ks / kStagesG);
+        if (!mb_wait(&empty_bar[s], (lap & 1u) ^ 1u)) timeout = true;
+        uint4 cw = make_uint4(0, 0, 0, 0);
+        if (present)
+          cw = *reinterpret_cast<const uint4 *>(wsm + ws * kWStageB + ((((j % kWSteps) * 2 + hf) ^ (r & 7)) << 4));
+        const uint32_t mulbits = f16_pow2_bits(sbyte - smax);
+        const uint32_t mul2 = mulbits | (mulbits << 16);
+        const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+        uint32_t o[16];  // 32 f16 = columns 16*hf .. 16*hf+15 of the stage (two K values per column)
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t h[4];
-            e2m1x8_to_f16x2(words[c], h);
+        for (int c = 0; c < 4; ++c) {
+          uint32_t h[4];
+          e2m1x8_to_f16x2(words[c], h);
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-              const __half2 a = *reinterpret_cast<const __half2 *>(&h[m]);
-              const __half2 b = *reinterpret_cast<const __half2 *>(&mul2);
-              const __half2 prod = __hmul2(a, b);
-              o[4 * c + m] = *reinterpret_cast<const uint32_t *>(&prod);
-            }
+          for (int m = 0; m < 4; ++m) {
+            const __half2 a = *reinterpret_cast<const __half2 *>(&h[m]);
+            const __half2 b = *reinterpret_cast<const __half2 *>(&mul2);
+            const __half2 prod = __hmul2(a, b);
+            o[4 * c + m] = *reinterpret_cast<const uint32_t *>(&prod);
           }
-          tc_st16(a_lane + kTileN + s * kAcols + 16 * hf, o);
-          tc_fence_before();
-          mb_arrive(&full_bar[s]);
         }
+        // the weight stage is free once this warp has read its last K step
+        if ((j % kWSteps) == kWSteps - 1 || ks == ksteps - 1) {
+          __syncwarp();
+          if (lane == 0) mb_arrive(&wempty_bar[ws]);
+        }
+        tc_st16(a_lane + kTileN + s * kAcols + 16 * hf, o);
+        tc_fence_before();
+        mb_arrive(&full_bar[s]);
       }
-#pragma unroll
-      for (int j = 0; j < kPf; ++j) {
-        cur[j] = nxt[j];
-        scur[j] = snxt[j];
-      }
+      scv = scn;
     }
   } else if (warp == kTmaWarp) {
-    // ---------------------------------------------------- activation tiles (TMA)
-    if (lane == 0) {
-      for (int ks = 0; ks < ksteps; ++ks) {
+    // ---------------------------------------------------- TMA: weight codes + activation tiles
+    const int nws = (ksteps + kWSteps - 1) / kWSteps;
+    uint8_t *wbase = gsm + kStagesG * kStageB;
+    const CUtensorMap *wmap =
+        reinterpret_cast<const CUtensorMap *>(P.maps + static_cast<size_t>(kind * P.E + g.u) * kMapBytes);
+    // the map was written by the previous kernel: order its reads after those writes
+    if (present && lane == 0)
+      asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(wmap) : "memory");
+    const int y0 = tile_wrow(kind, g.m0, 0, P.I), y1 = tile_wrow(kind, g.m0, kWBoxRows, P.I);
+    auto issue_weights = [&](int wst) {
+      const int ws = wst % kWStages;
+      if (lane == 0) {
+        if (!mb_wait(&wempty_bar[ws], (static_cast<uint32_t>(wst / kWStages) & 1u) ^ 1u)) timeout = true;
+        mb_arrive_tx(&wfull_bar[ws], present ? static_cast<uint32_t>(kWStageB) : 0u);
+        if (present) {
+          uint8_t *dst = wbase + ws * kWStageB;
+          tma_load_2d(dst, wmap, wst * (kWK / 2), y0, &wfull_bar[ws]);
+          tma_load_2d(dst + kWStageB / 2, wmap, wst * (kWK / 2), y1, &wfull_bar[ws]);
+        }
+      }
+    };
+    for (int wst = 0; wst < kWStages - 1 && wst < nws; ++wst) issue_weights(wst);
+    for (int ks = 0; ks < ksteps; ++ks) {
+      if (ks % kWSteps == 0) {
+        const int wn = ks / kWSteps + kWStages - 1;
+        if (wn < nws) issue_weights(wn);
+      }
+      if (lane == 0) {
         const int s = ks % kStagesG;
         const uint32_t lap = static_cast<uint32_t>(ks / kStagesG);
         if (!mb_wait(&empty_bar[s], (lap & 1u) ^ 1u)) timeout = true;
@@ -508,6 +571,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         mb_arrive_tx(&full_bar[s], kStageB);
         tma_load_2d(sbuf, &bmap, ks * kTileK, g.p0, &full_bar[s]);
       }
+      __syncwarp();
     }
   } else {
     // ---------------------------------------------------- MMA issue
@@ -547,14 +611,14 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     tc_fence_before();
     asm volatile("bar.sync 1, %0;" ::"r"(kDqWarps * 32) : "memory");
     if (kind == 0) {
-      // h[p0 + n][m0/2 + i] = bf16(silu(g) * u), g = row 2i, u = row 2i+1
+      // h[p0 + n][m0/2 + i] = bf16(silu(g) * u), g = tile row i, u = tile row 64 + i
       const int ncols = kTileM / 2;
       for (int idx = tid; idx < g.n * ncols; idx += kDqWarps * 32) {
         const int n = idx / ncols, i = idx % ncols;
         float hv = 0.f;
         if (present) {
-          const float gg = mul_pow2(stage[n * (kTileM + 1) + 2 * i], sref_s[2 * i] - 127 + bexp_s[n]);
-          const float uu = mul_pow2(stage[n * (kTileM + 1) + 2 * i + 1], sref_s[2 * i + 1] - 127 + bexp_s[n]);
+          const float gg = mul_pow2(stage[n * (kTileM + 1) + i], sref_s[i] - 127 + bexp_s[n]);
+          const float uu = mul_pow2(stage[n * (kTileM + 1) + ncols + i], sref_s[ncols + i] - 127 + bexp_s[n]);
           hv = (gg / (1.0f + expf(-gg))) * uu;
         }
         P.hrow[static_cast<size_t>(g.p0 + n) * P.I + (g.m0 >> 1) + i] = f32_to_bf16_rne(hv);
@@ -612,6 +676,21 @@ bool make_row_map(CUtensorMap *m, void *base, int rows, int K) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D map over the weight codes of one expert (rows x K/2 bytes): box = 128
+// bytes x 64 rows, 128B swizzle.  `base` is a placeholder address that the
+// device replaces per expert.
+bool make_code_map(CUtensorMap *m, void *base, int rows, int kbytes) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kbytes), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kbytes)};
+  const cuuint32_t box[2] = {kWK / 2, kWBoxRows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 size_t ffn_gemm_workspace(const k3moe_shape &s) { return gemm_ws(s.T, s.H, s.I, s.E, s.k).total; }
@@ -639,10 +718,15 @@ int launch_ffn_gemm(const k3moe_shape &s, const uint16_t *x, const k3moe_weights
   uint16_t *hrow = reinterpret_cast<uint16_t *>(base + L.hrow);
   uint16_t *h16 = reinterpret_cast<uint16_t *>(base + L.h16);
   int32_t *hexp = reinterpret_cast<int32_t *>(base + L.hexp);
-  CUtensorMap xmap, hmap;
+  uint8_t *maps = reinterpret_cast<uint8_t *>(base + L.maps);
+  CUtensorMap xmap, hmap, t13, t2;
   if (!make_row_map(&xmap, xg, A, s.H) || !make_row_map(&hmap, h16, A, s.I)) return -1;
+  if (!make_code_map(&t13, maps, 2 * s.I, s.H / 2) || !make_code_map(&t2, maps, s.H, s.I / 2)) return -1;
   if (launch_pdl(gemm_prep_kernel, dim3(1), dim3(32), 0, st, offsets, s.E, A, mt_gu, mt_dn, active, meta, sp0,
                  scnt, pgu, pdn, status) != cudaSuccess)
+    return -1;
+  if (launch_pdl(gemm_maps_kernel, dim3((2 * s.E + 127) / 128), dim3(128), 0, st, t13, t2, w,
+                 static_cast<const int32_t *>(active), static_cast<const int32_t *>(meta), s.E, maps) != cudaSuccess)
     return -1;
   if (launch_pdl(gemm_rows_to_f16_kernel, dim3(A), dim3(256), 0, st, x, perm, s.k, A, s.H, xg, xexp, status) !=
       cudaSuccess)
@@ -661,6 +745,8 @@ int launch_ffn_gemm(const k3moe_shape &s, const uint16_t *x, const k3moe_weights
   P.H = s.H; P.I = s.I; P.A = A;
   P.active = active;
   P.meta = meta;
+  P.maps = maps;
+  P.E = s.E;
   P.slot_p0 = sp0;
   P.slot_cnt = scnt;
   P.hrow = hrow;
