@@ -22,14 +22,25 @@
 //    prescale per row (max|v| * 2^-p in [2^14, 2^15)), laid out in bucket order
 //    by two small pre-pass kernels so that a 2-D TMA tile load fetches them.
 //
-// One CTA per tile (active expert, 128 weight rows, <= 128 tokens), 10 warps:
-// warps 0-7 dequantise the weight tile rows into 128B-swizzled K-major shared
-// memory (two threads per row), warp 8 issues the TMA loads of the activation
-// tile, warp 9 owns tensor memory and issues tcgen05.mma (M=128, K=16 each),
-// committing every stage back to the producers; three stages; two CTAs per SM.
-// The epilogue (warps 0-7) reads the accumulator with tcgen05.ld and writes h
-// (bf16, the fixed rounding point) or Y (fp32) rows through shared memory.
+// One CTA per tile (active expert, 128 weight rows, <= 128 tokens), 10 warps,
+// two CTAs per SM:
+//  * warp 8 (TMA): per weight stage (256 K values) two 2-D boxes of weight
+//    codes, 64 rows x 128 bytes each, 128B-swizzled, through the expert's tensor
+//    map (built on the device by gemm_sched_kernel); per K step of 64 one
+//    128-row box of the activation tile;
+//  * warps 0-7 (dequantisation): thread = one weight row (tensor-memory lane)
+//    and one K half; reads 16 code bytes from shared memory, converts e2m1 pairs
+//    to f16, multiplies by 2^(s - s_ref) and stores the 128 x 64 A stage to
+//    tensor memory with tcgen05.st; one mbarrier arrival per warp and stage;
+//  * warp 9 (MMA): owns tensor memory, issues tcgen05.mma kind::f16 with A from
+//    tensor memory and B (activations) from shared memory, M=128, K=16 each,
+//    and commits every stage back to the producers.
+// Four A/activation stages and two weight stages.  The epilogue (warps 0-7)
+// reads the accumulator with tcgen05.ld and writes h (bf16, the fixed rounding
+// point) or Y (fp32) rows through shared memory.
 #include <cuda.h>
+
+#include <algorithm>
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
 
@@ -208,7 +219,7 @@ __device__ __forceinline__ bool decode_tile(const int32_t *pref, const int32_t *
 }
 
 struct GemmWs {
-  size_t active, meta, sp0, scnt, pref_gu, pref_dn, maps, xg, xexp, hrow, h16, hexp, total;
+  size_t active, meta, sp0, scnt, pref_gu, pref_dn, maps, tab_gu, tab_dn, xg, xexp, hrow, h16, hexp, total;
 };
 __host__ __device__ inline size_t g256(size_t v) { return (v + 255) & ~size_t(255); }
 __host__ __device__ inline GemmWs gemm_ws(int T, int H, int I, int E, int k) {
@@ -222,6 +233,10 @@ __host__ __device__ inline GemmWs gemm_ws(int T, int H, int I, int E, int k) {
   w.pref_gu = o; o = g256(o + sizeof(int32_t) * E);
   w.pref_dn = o; o = g256(o + sizeof(int32_t) * E);
   w.maps = o;    o = g256(o + static_cast<size_t>(kMapBytes) * 2 * E);  // weight-code tensor maps per active slot
+  // tile tables: an upper bound of the token tiles, sum_e ceil(n_e / 128) <= A / 128 + min(A, E), times the row tiles
+  const size_t ntl = A / kTileN + (A < static_cast<size_t>(E) ? A : static_cast<size_t>(E));
+  w.tab_gu = o;  o = g256(o + sizeof(int4) * ntl * ((2 * static_cast<size_t>(I)) / kTileM));
+  w.tab_dn = o;  o = g256(o + sizeof(int4) * ntl * (static_cast<size_t>(H) / kTileM));
   w.xg = o;      o = g256(o + sizeof(uint16_t) * A * H);  // x rows in bucket order, prescaled f16
   w.xexp = o;    o = g256(o + sizeof(int32_t) * (A ? A : 1));
   w.hrow = o;    o = g256(o + sizeof(uint16_t) * A * I);  // h, bf16 (the rounding point)
@@ -286,14 +301,29 @@ __global__ void __launch_bounds__(32)
 // global address replaced by the expert's code pointer.  Experts whose code
 // pointers are NULL or not 16-byte aligned keep the template's address; the
 // GEMM treats them as absent and never loads through their map.
+//
+// The same launch writes the tile tables of both GEMMs: entry t of a table is
+// {active slot, expert, first bucket position, (tokens << 16) | row tile} of
+// tile t, so that a GEMM CTA finds its tile with one load.
+__device__ __forceinline__ void write_tile(const int32_t *pref, const int32_t *active, const int32_t *slot_p0,
+                                           const int32_t *slot_cnt, int na, int mtiles, int t, int4 *tab) {
+  GemmTile g;
+  if (decode_tile(pref, active, slot_p0, slot_cnt, na, mtiles, t, g))
+    tab[t] = make_int4(g.u, g.e, g.p0, (g.n << 16) | (g.m0 / kTileM));
+}
+
 __global__ void __launch_bounds__(128)
-    gemm_maps_kernel(const __grid_constant__ CUtensorMap t13, const __grid_constant__ CUtensorMap t2,
-                     k3moe_weights w, const int32_t *__restrict__ active, const int32_t *__restrict__ meta, int E,
-                     uint8_t *__restrict__ maps) {
+    gemm_sched_kernel(const __grid_constant__ CUtensorMap t13, const __grid_constant__ CUtensorMap t2,
+                      k3moe_weights w, const int32_t *__restrict__ active, const int32_t *__restrict__ meta, int E,
+                      const int32_t *__restrict__ slot_p0, const int32_t *__restrict__ slot_cnt,
+                      const int32_t *__restrict__ pref_gu, const int32_t *__restrict__ pref_dn, int mt_gu, int mt_dn,
+                      int4 *__restrict__ tab_gu, int4 *__restrict__ tab_dn, uint8_t *__restrict__ maps) {
   pdl_wait();
   pdl_trigger();
   const int na = meta[0];
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t < meta[1]) write_tile(pref_gu, active, slot_p0, slot_cnt, na, mt_gu, t, tab_gu);
+  if (t < meta[2]) write_tile(pref_dn, active, slot_p0, slot_cnt, na, mt_dn, t, tab_dn);
   if (t >= 2 * na) return;
   const int which = t >= na, u = which ? t - na : t;
   const int e = active[u];
@@ -366,7 +396,8 @@ __global__ void __launch_bounds__(256)
 struct GemmParams {
   k3moe_weights w;
   int H, I, A;
-  const int32_t *active, *meta, *slot_p0, *slot_cnt, *pref;
+  const int32_t *meta;
+  const int4 *tab;            // tile table of this GEMM
   const uint8_t *maps;        // weight-code tensor maps per active slot (w13 at u, w2 at E + u)
   int E;
   const int32_t *bexp;        // per bucket position: prescale exponent of the activation row
@@ -409,9 +440,16 @@ __global__ void __launch_bounds__(kThreadsG, 1)
 
   const int kind = P.kind;
   const int K = kind == 0 ? P.H : P.I;  // reduction length
-  const int mtiles = kind == 0 ? (2 * P.I) / kTileM : P.H / kTileM;
+  if (static_cast<int>(blockIdx.x) >= P.meta[1 + kind]) return;
   GemmTile g;
-  if (!decode_tile(P.pref, P.active, P.slot_p0, P.slot_cnt, P.meta[0], mtiles, blockIdx.x, g)) return;
+  {
+    const int4 te = P.tab[blockIdx.x];
+    g.u = te.x;
+    g.e = te.y;
+    g.p0 = te.z;
+    g.n = te.w >> 16;
+    g.m0 = (te.w & 0xFFFF) * kTileM;
+  }
   const int Npad = (g.n + 15) & ~15;  // MMA N: multiple of 16
   const int ksteps = K / kTileK;
 
@@ -424,7 +462,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
   if (tid < kTileN) bexp_s[tid] = tid < g.n ? P.bexp[g.p0 + tid] : 0;
   if (tid == 0) {
     for (int s = 0; s < kStagesG; ++s) {
-      mb_init(&full_bar[s], kDqWarps * 32 + 1);  // every dequantising thread + the TMA producer
+      mb_init(&full_bar[s], kDqWarps + 1);  // one arrival per dequantising warp + the TMA producer
       mb_init(&empty_bar[s], 1);                 // tcgen05.commit
     }
     mb_init(&acc_bar, 1);
@@ -524,14 +562,14 @@ __global__ void __launch_bounds__(kThreadsG, 1)
             o[4 * c + m] = *reinterpret_cast<const uint32_t *>(&prod);
           }
         }
-        // the weight stage is free once this warp has read its last K step
-        if ((j % kWSteps) == kWSteps - 1 || ks == ksteps - 1) {
-          __syncwarp();
-          if (lane == 0) mb_arrive(&wempty_bar[ws]);
-        }
-        tc_st16(a_lane + kTileN + s * kAcols + 16 * hf, o);
+        tc_st16(a_lane + kTileN + s * kAcols + 16 * hf, o);  // waits for the warp's stores
         tc_fence_before();
-        mb_arrive(&full_bar[s]);
+        __syncwarp();
+        if (lane == 0) {
+          mb_arrive(&full_bar[s]);
+          // the weight stage is free once this warp has read its last K step
+          if ((j % kWSteps) == kWSteps - 1 || ks == ksteps - 1) mb_arrive(&wempty_bar[ws]);
+        }
       }
       scv = scn;
     }
@@ -713,6 +751,8 @@ int launch_ffn_gemm(const k3moe_shape &s, const uint16_t *x, const k3moe_weights
   int32_t *scnt = reinterpret_cast<int32_t *>(base + L.scnt);
   int32_t *pgu = reinterpret_cast<int32_t *>(base + L.pref_gu);
   int32_t *pdn = reinterpret_cast<int32_t *>(base + L.pref_dn);
+  int4 *tab_gu = reinterpret_cast<int4 *>(base + L.tab_gu);
+  int4 *tab_dn = reinterpret_cast<int4 *>(base + L.tab_dn);
   uint16_t *xg = reinterpret_cast<uint16_t *>(base + L.xg);
   int32_t *xexp = reinterpret_cast<int32_t *>(base + L.xexp);
   uint16_t *hrow = reinterpret_cast<uint16_t *>(base + L.hrow);
@@ -725,14 +765,18 @@ int launch_ffn_gemm(const k3moe_shape &s, const uint16_t *x, const k3moe_weights
   if (launch_pdl(gemm_prep_kernel, dim3(1), dim3(32), 0, st, offsets, s.E, A, mt_gu, mt_dn, active, meta, sp0,
                  scnt, pgu, pdn, status) != cudaSuccess)
     return -1;
-  if (launch_pdl(gemm_maps_kernel, dim3((2 * s.E + 127) / 128), dim3(128), 0, st, t13, t2, w,
-                 static_cast<const int32_t *>(active), static_cast<const int32_t *>(meta), s.E, maps) != cudaSuccess)
+  // upper bound of the token tiles: sum_e ceil(n_e / 128) <= A / 128 + min(A, E)
+  const long long ntile_max = A / kTileN + (A < s.E ? A : s.E);
+  const long long sched_threads = std::max<long long>(2LL * s.E, ntile_max * std::max(mt_gu, mt_dn));
+  if (launch_pdl(gemm_sched_kernel, dim3(static_cast<unsigned>((sched_threads + 127) / 128)), dim3(128), 0, st, t13,
+                 t2, w, static_cast<const int32_t *>(active), static_cast<const int32_t *>(meta), s.E,
+                 static_cast<const int32_t *>(sp0), static_cast<const int32_t *>(scnt),
+                 static_cast<const int32_t *>(pgu), static_cast<const int32_t *>(pdn), mt_gu, mt_dn, tab_gu, tab_dn,
+                 maps) != cudaSuccess)
     return -1;
   if (launch_pdl(gemm_rows_to_f16_kernel, dim3(A), dim3(256), 0, st, x, perm, s.k, A, s.H, xg, xexp, status) !=
       cudaSuccess)
     return -1;
-  // upper bound of the token tiles: sum_e ceil(n_e / 128) <= A / 128 + min(A, E)
-  const long long ntile_max = A / kTileN + (A < s.E ? A : s.E);
   static bool attr = false;
   if (!attr) {
     if (cudaFuncSetAttribute(ffn_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem) !=
@@ -743,17 +787,14 @@ int launch_ffn_gemm(const k3moe_shape &s, const uint16_t *x, const k3moe_weights
   GemmParams P;
   P.w = w;
   P.H = s.H; P.I = s.I; P.A = A;
-  P.active = active;
   P.meta = meta;
   P.maps = maps;
   P.E = s.E;
-  P.slot_p0 = sp0;
-  P.slot_cnt = scnt;
   P.hrow = hrow;
   P.Y = Y;
   P.status = status;
   P.kind = 0;
-  P.pref = pgu;
+  P.tab = tab_gu;
   P.bexp = xexp;
   if (launch_pdl(ffn_gemm_kernel, dim3(static_cast<unsigned>(ntile_max * mt_gu)), dim3(kThreadsG), kGemmSmem, st,
                  xmap, P) != cudaSuccess)
@@ -762,7 +803,7 @@ int launch_ffn_gemm(const k3moe_shape &s, const uint16_t *x, const k3moe_weights
                  static_cast<const int32_t *>(nullptr), 1, A, s.I, h16, hexp, status) != cudaSuccess)
     return -1;
   P.kind = 1;
-  P.pref = pdn;
+  P.tab = tab_dn;
   P.bexp = hexp;
   if (launch_pdl(ffn_gemm_kernel, dim3(static_cast<unsigned>(ntile_max * mt_dn)), dim3(kThreadsG), kGemmSmem, st,
                  hmap, P) != cudaSuccess)
