@@ -1,21 +1,33 @@
-// ffn_gemv.cu -- MXFP4 SwiGLU expert FFN as streaming GEMVs on the CUDA cores.
+// ffn_gemv.cu -- MXFP4 SwiGLU expert FFN for few tokens per expert (decode) as
+// streaming matrix-vector products on the CUDA cores.
 //
 // The kimi-k3-in-c CHANGELOG walkthrough ("[0.1.0] Added") describes a matmul that
 // reads the packed MXFP4 nibbles directly and never materialises a dequantised
 // expert, and a gated-linear-unit expert.  Here every weight byte is read once
-// per (expert, token chunk) with 128-bit coalesced loads, decoded in registers
+// per (expert, token group) with 16-byte coalesced loads, decoded in registers
 // (cvt e2m1x2 -> f16x2, exact), multiplied by f16 activations with exact
 // products accumulated in fp32, scaled per 32-block by the e8m0 scale, and
 // reduced across the warp with shuffles.  The order of every sum is fixed.
 //
-// Activations are staged as f16 after an exact power-of-two prescale per row
-// (x' = x * 2^-p with max|x'| in [2^14, 2^15)), so bf16 values convert to f16
-// without rounding except for elements below 2^-28 * max|x| (error < 2^-25 of max).
+// Activations are f16 after an exact power-of-two prescale per row (x' = x * 2^-p
+// with max|x'| in [2^14, 2^15)), so bf16 values convert to f16 without rounding
+// except for elements below 2^-28 * max|x| (error < 2^-25 of max).
 //
-// Kernels (one expert FFN call):
-//   ffn_prep     active-expert list, offsets check, x -> prescaled f16 (piece-major)
-//   ffn_gateup   h[p] = bf16(silu(Wg x) * (Wu x)) for every bucket position p
-//   ffn_down     Y[p] = Wd h[p]
+// Kernels of one call:
+//   gemv_prep    active-expert slots (block-parallel scan of the offsets),
+//                x -> prescaled f16 (piece-major), zeroed per-row maxima of h
+//   gemv_rows<0> item = (active slot u, row pair i): for each token p of u,
+//                h[p][i] = bf16(silu(Wg_i x_p) * (Wu_i x_p)), max|h[p]| by atomicMax
+//   gemv_h16     h rows -> prescaled f16 (exponent from the row's max |h|)
+//   gemv_rows<1> item = (active slot u, 4 rows of W2; 2 with 4 tokens): Y[p][rows] = W2 rows . h[p]
+//
+// Work is spread over warps, not blocks: warp w of the grid takes items w, w + W,
+// w + 2W, ... (W = warps in the grid).  An item is streamed in steps of B chunks
+// (32 K values = 16 code bytes) per lane and row; the next step's code and scale
+// loads are issued before the current step is computed, so each warp keeps about
+// one step of weight bytes in flight at all times, with no block-wide barrier.
+// Activations (x16, h16), the slot table and the token ids are small and come
+// through L1; weight codes bypass it.
 #include <cuda_fp16.h>
 
 #include "k3moe_dev.cuh"
@@ -25,29 +37,30 @@ namespace k3moe {
 
 namespace {
 
-constexpr int kWarps = 8;  // warps per block
-constexpr int kNT = 4;     // tokens per pass over a weight tile
+constexpr int kGvWarps = 8;   // warps per block
+constexpr int kGvMaxNT = 4;   // tokens per pass over an item's weights
+constexpr int kDnRows = 4;    // W2 rows per down item
 
 // Workspace layout (byte offsets, 256-aligned pieces).
 struct GemvWs {
-  size_t active, nactive, xexp, x16, hrow, total;
+  size_t slots, meta, xexp, x16, hrow, hmax, h16, hexp, total;
 };
 
 __host__ __device__ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 __host__ __device__ inline GemvWs gemv_ws(int T, int H, int I, int E, int k) {
   GemvWs w;
+  const size_t A = static_cast<size_t>(T) * k;
+  const size_t a1 = A ? A : 1;
   size_t o = 0;
-  w.active = o;
-  o = align256(o + sizeof(int32_t) * E);
-  w.nactive = o;
-  o = align256(o + sizeof(int32_t));
-  w.xexp = o;
-  o = align256(o + sizeof(int32_t) * (T > 0 ? T : 1));
-  w.x16 = o;
-  o = align256(o + sizeof(uint16_t) * static_cast<size_t>(T) * H);
-  w.hrow = o;
-  o = align256(o + sizeof(uint16_t) * static_cast<size_t>(T) * k * I);
+  w.slots = o; o = align256(o + sizeof(int4) * E);                  // {e, p0, count, present} per active slot
+  w.meta = o;  o = align256(o + sizeof(int32_t) * 4);              // active-slot count
+  w.xexp = o;  o = align256(o + sizeof(int32_t) * (T > 0 ? T : 1));
+  w.x16 = o;   o = align256(o + sizeof(uint16_t) * static_cast<size_t>(T) * H);
+  w.hrow = o;  o = align256(o + sizeof(uint16_t) * A * I);          // h, bf16 (the rounding point)
+  w.hmax = o;  o = align256(o + sizeof(int32_t) * a1);              // max |h| per row, as float bits
+  w.h16 = o;   o = align256(o + sizeof(uint16_t) * A * I);          // h, prescaled f16, piece-major
+  w.hexp = o;  o = align256(o + sizeof(int32_t) * a1);
   w.total = o;
   return w;
 }
@@ -74,6 +87,33 @@ __device__ __forceinline__ float scale_pow2(float v, int p) {
   return v * exp2i(p1) * exp2i(p2);
 }
 
+// bf16 row (K values) -> prescaled f16, piece-major: uint4 index q * (K/32) + c
+// holds columns 32c + 8q .. 32c + 8q + 7, so a warp's lanes read consecutive 16 B.
+__device__ __forceinline__ void row_to_f16_piece_major(const uint16_t *__restrict__ src, int K, float s,
+                                                       uint4 *__restrict__ dst) {
+  const int nch = K / 32;
+  for (int piece = threadIdx.x; piece < K / 8; piece += blockDim.x) {  // piece = c * 4 + q (source order)
+    const int c = piece >> 2, q = piece & 3;
+    const uint4 v = *reinterpret_cast<const uint4 *>(src + 8 * piece);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+      o[m] = pack_f16x2_scaled(__uint_as_float(w[m] << 16), __uint_as_float(w[m] & 0xFFFF0000u), s);
+    dst[q * nch + c] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+__device__ __forceinline__ float block_max_256(float mx, float *red) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  mx = red[0];
+  for (int i = 1; i < 8; ++i) mx = fmaxf(mx, red[i]);
+  return mx;
+}
+
 }  // namespace
 
 // An expert takes part when its four pointers are non-NULL and its code arrays
@@ -84,39 +124,70 @@ __device__ __forceinline__ bool expert_present(const k3moe_weights &w, int e) {
 }
 
 // ----------------------------------------------------------------------------
-// prep: block 0 builds the active-expert list; block 1 + t converts x[t].
-// x16 layout per token: piece-major, uint4 index q * (H/32) + c holds the f16 of
-// columns 32c + 8q .. 32c + 8q + 7 (so a warp's lanes read consecutive 16 B).
+// prep.  Block 0: slots of the active experts in expert order, from a
+// block-parallel scan of the bucket offsets (thread i reads experts
+// [i*m, (i+1)*m), m = ceil(E/256) <= 16), and zeroed per-row maxima of h.
+// Block 1 + t: x[t] -> prescaled f16.
 __global__ void __launch_bounds__(256)
-    ffn_prep_kernel(k3moe_weights w, const uint16_t *__restrict__ x, int T, int H, int E, int A,
-                    const int32_t *__restrict__ offsets, int32_t *__restrict__ active,
-                    int32_t *__restrict__ nactive, int32_t *__restrict__ xexp,
-                    uint4 *__restrict__ x16, int32_t *status) {
+    gemv_prep_kernel(k3moe_weights w, const uint16_t *__restrict__ x, int T, int H, int E, int A,
+                     const int32_t *__restrict__ offsets, int4 *__restrict__ slots, int32_t *__restrict__ meta,
+                     int32_t *__restrict__ xexp, uint4 *__restrict__ x16, int32_t *__restrict__ hmax,
+                     int32_t *status) {
   pdl_wait();
   pdl_trigger();
   if (blockIdx.x == 0) {
-    if (threadIdx.x >= 32) return;
-    const int lane = threadIdx.x;
-    int run = 0;
-    bool bad = offsets[0] != 0 || offsets[E] > A;
-    for (int base = 0; base < E; base += 32) {
-      const int e = base + lane;
-      int cnt = 0;
-      if (e < E) {
-        cnt = offsets[e + 1] - offsets[e];
-        if (cnt < 0) bad = true;
+    __shared__ int wsum[8];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int m = (E + 255) / 256;
+    const int e0 = tid * m;
+    int cnt[16], beg[16];
+    int nf = 0;
+    bool bad = false;
+    int prev = e0 <= E ? offsets[e0 < E ? e0 : E] : 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      cnt[i] = 0;
+      beg[i] = prev;
+      const int e = e0 + i;
+      if (i < m && e < E) {
+        const int nx = offsets[e + 1];
+        cnt[i] = nx - prev;
+        if (cnt[i] < 0) bad = true;
+        nf += cnt[i] > 0;
+        prev = nx;
       }
-      const bool f = cnt > 0 && !bad;
-      if (f && !expert_present(w, e) && w.w13_codes[e] && w.w13_scales[e] && w.w2_codes[e] &&
-          w.w2_scales[e])
-        set_status(status, K3MOE_DEV_BOUNDS);  // non-NULL but misaligned: treated as absent
-      const unsigned m = __ballot_sync(0xFFFFFFFFu, f);
-      if (f) active[run + __popc(m & ((1u << lane) - 1u))] = e;
-      run += __popc(m);
     }
-    bad = __any_sync(0xFFFFFFFFu, bad);
-    if (lane == 0) {
-      *nactive = bad ? 0 : run;
+    if (tid == 0 && (offsets[0] != 0 || offsets[E] > A)) bad = true;
+    bad = __syncthreads_or(bad) != 0;
+    int inc = nf;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, inc, off);
+      if (lane >= off) inc += v;
+    }
+    if (lane == 31) wsum[warp] = inc;
+    __syncthreads();
+    int base = 0, total = 0;
+    for (int i = 0; i < 8; ++i) {
+      base += i < warp ? wsum[i] : 0;
+      total += wsum[i];
+    }
+    int slot = base + inc - nf;
+    if (!bad) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int e = e0 + i;
+        if (i < m && e < E && cnt[i] > 0) {
+          const bool pr = expert_present(w, e);
+          if (!pr && w.w13_codes[e] && w.w13_scales[e] && w.w2_codes[e] && w.w2_scales[e])
+            set_status(status, K3MOE_DEV_BOUNDS);  // non-NULL but misaligned: treated as absent
+          slots[slot++] = make_int4(e, beg[i], cnt[i], pr ? 1 : 0);
+        }
+      }
+    }
+    for (int p = tid; p < A; p += 256) hmax[p] = 0;
+    if (tid == 0) {
+      meta[0] = bad ? 0 : total;
       if (bad) set_status(status, K3MOE_DEV_BOUNDS);
     }
     return;
@@ -124,293 +195,197 @@ __global__ void __launch_bounds__(256)
   const int t = blockIdx.x - 1;
   if (t >= T) return;
   const uint16_t *xr = x + static_cast<size_t>(t) * H;
-  __shared__ float red[kWarps];
+  __shared__ float red[8];
   float mx = 0.f;
   for (int c = threadIdx.x; c < H; c += 256) mx = fmaxf(mx, fabsf(bf16_bits_to_f32(xr[c])));
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
-  __syncthreads();
-  mx = red[0];
-  for (int i = 1; i < kWarps; ++i) mx = fmaxf(mx, red[i]);
-  const int p = prescale_exp(mx);
+  const int p = prescale_exp(block_max_256(mx, red));
   if (threadIdx.x == 0) xexp[t] = p;
-  const float s = scale_pow2(1.0f, -p);
-  const int nch = H / 32;
-  uint4 *dst = x16 + static_cast<size_t>(t) * (H / 8);
-  for (int piece = threadIdx.x; piece < H / 8; piece += 256) {  // piece = c*4 + q (source order)
-    const int c = piece >> 2, q = piece & 3;
-    const uint4 src = *reinterpret_cast<const uint4 *>(xr + 8 * piece);
-    const uint32_t w[4] = {src.x, src.y, src.z, src.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int m = 0; m < 4; ++m)
-      o[m] = pack_f16x2_scaled(__uint_as_float(w[m] << 16), __uint_as_float(w[m] & 0xFFFF0000u), s);
-    dst[q * nch + c] = make_uint4(o[0], o[1], o[2], o[3]);
-  }
+  row_to_f16_piece_major(xr, H, scale_pow2(1.0f, -p), x16 + static_cast<size_t>(t) * (H / 8));
+}
+
+// h row p -> prescaled f16 (piece-major), exponent from the row's max |h|.
+__global__ void __launch_bounds__(256)
+    gemv_h16_kernel(const uint16_t *__restrict__ hrow, const int32_t *__restrict__ hmax, int I,
+                    uint4 *__restrict__ h16, int32_t *__restrict__ hexp) {
+  pdl_wait();
+  pdl_trigger();
+  const int p = blockIdx.x;
+  const int e = prescale_exp(__int_as_float(hmax[p]));
+  if (threadIdx.x == 0) hexp[p] = e;
+  row_to_f16_piece_major(hrow + static_cast<size_t>(p) * I, I, scale_pow2(1.0f, -e),
+                         h16 + static_cast<size_t>(p) * (I / 8));
 }
 
 // ----------------------------------------------------------------------------
-// R rows of one expert matrix against NT staged activation rows.
-// codes[r], scales[r]: row pointers; nch = K/32 chunks; xs: smem piece-major f16,
-// NT rows of K/8 uint4 each.  acc[r][t] accumulates the lane's partial sums.
-template <int R, int NT, int B>
-__device__ __forceinline__ void mx_rows_dot(const uint8_t *const (&codes)[R],
-                                            const uint8_t *const (&scales)[R], int nch,
-                                            const uint4 *__restrict__ xs, float (&acc)[R][NT]) {
+struct RowsParams {
+  k3moe_weights w;
+  int H, I, k, A;
+  const int32_t *perm;
+  const int4 *slots;
+  const int32_t *meta;
+  const int32_t *aexp;   // activation prescale exponent: per token (gate/up) or per bucket position (down)
+  const uint4 *act;      // activations, f16 piece-major: x16 [T][H] (gate/up) or h16 [A][I] (down)
+  uint16_t *hrow;        // gate/up output, bf16 [A][I]
+  int32_t *hmax;         // gate/up output, max |h| per row
+  float *Y;              // down output, [A][H]
+  int32_t *status;
+};
+
+__device__ __forceinline__ const uint8_t *ldg_ptr(const uint8_t *const *arr, int e) {
+  return reinterpret_cast<const uint8_t *>(__ldg(reinterpret_cast<const unsigned long long *>(arr) + e));
+}
+
+// KIND 0 (gate/up): an item is one row pair (gate row i, up row I + i), K = H.
+// KIND 1 (down):    an item is R consecutive rows of W2 (4, or 2 with 4 tokens), K = I.
+// A warp issues every 16-byte code load of its item's K segment (NJ chunks per
+// lane and row, one segment when K <= 32 * 32 * NJ) before it computes, and many
+// warps per SM keep loads in flight while others compute.  EXACT instances serve
+// K = 1024 * NJ exactly (every lane has NJ chunks, no guards in the loop).
+template <int KIND, int R, int NT, int NJ, bool EXACT>
+__global__ void __launch_bounds__(kGvWarps * 32, 2) gemv_rows_kernel(RowsParams P) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
-  for (int c0 = lane; c0 < nch; c0 += 32 * B) {
-    uint4 cw[B][R];
-    uint32_t sb[B][R];
-#pragma unroll
-    for (int b = 0; b < B; ++b) {
-      const int c = c0 + 32 * b;
+  const int K = EXACT ? 1024 * NJ : (KIND == 0 ? P.H : P.I);
+  const int nch = K / 32;                                  // 32-value chunks per row (a constant when EXACT)
+  const int nseg = EXACT ? 1 : (nch + 32 * NJ - 1) / (32 * NJ);  // K segments
+  const int per_slot = KIND == 0 ? P.I : (P.H + R - 1) / R;
+  const long long nitems = static_cast<long long>(P.meta[0]) * per_slot;
+  const long long stride = static_cast<long long>(gridDim.x) * kGvWarps;
+  const size_t cbytes = static_cast<size_t>(K) / 2, sbytes = static_cast<size_t>(nch);
+  for (long long item = static_cast<long long>(blockIdx.x) * kGvWarps + (threadIdx.x >> 5); item < nitems;
+       item += stride) {
+    const int4 sl = __ldg(P.slots + static_cast<int>(item / per_slot));  // {expert, first position, tokens, present}
+    const int rb = static_cast<int>(item % per_slot);
+    const bool present = sl.w != 0;
+    // row pointers, advanced to the lane's first chunk
+    const uint8_t *cr[R], *sr[R];
+    if (present) {
+      const uint8_t *cb = ldg_ptr(KIND == 0 ? P.w.w13_codes : P.w.w2_codes, sl.x);
+      const uint8_t *sb = ldg_ptr(KIND == 0 ? P.w.w13_scales : P.w.w2_scales, sl.x);
 #pragma unroll
       for (int r = 0; r < R; ++r) {
-        if (c < nch) {
-          cw[b][r] = ldg_nc_v4(codes[r] + 16 * static_cast<size_t>(c));
-          sb[b][r] = __ldg(scales[r] + c);
-        } else {
-          cw[b][r] = make_uint4(0, 0, 0, 0);
-          sb[b][r] = 0;
-        }
+        int row;
+        if (KIND == 0) row = r == 0 ? rb : P.I + rb;
+        else row = min(rb * R + r, P.H - 1);  // rows past H are computed (duplicates), not stored
+        cr[r] = cb + row * cbytes + 16 * lane;
+        sr[r] = sb + row * sbytes + lane;
       }
     }
+    uint4 cw[R][NJ];
+    uint32_t sc[R][NJ];
+    for (int g = 0; g * NT < sl.z; ++g) {
+      const int p0 = sl.y + g * NT;
+      const int nt = min(NT, sl.z - g * NT);
+      const uint4 *arow[NT];
+      int aexp[NT];
+      float acc[R][NT];
 #pragma unroll
-    for (int b = 0; b < B; ++b) {
-      const int c = c0 + 32 * b;
-      if (c >= nch) break;
-      float d[R][NT];
+      for (int t = 0; t < NT; ++t) {
+        int row = 0, ex = 0;
+        if (t < nt) {
+          if (KIND == 0) {
+            const int a = __ldg(P.perm + p0 + t);
+            const bool ok = a >= 0 && a < P.A;
+            if (!ok) set_status(P.status, K3MOE_DEV_BOUNDS);
+            row = ok ? a / P.k : 0;
+          } else {
+            row = p0 + t;
+          }
+          ex = __ldg(P.aexp + row);
+        }
+        arow[t] = P.act + static_cast<size_t>(row) * (K / 8) + lane;
+        aexp[t] = ex;
+#pragma unroll
+        for (int r = 0; r < R; ++r) acc[r][t] = 0.f;
+      }
+      for (int seg = 0; present && seg < nseg; ++seg) {
+        const int c0 = seg * 32 * NJ;  // first chunk of the segment (lane 0)
+        if (seg > 0 || g == 0 || nseg > 1) {
+          // every code and scale load of the segment, then the arithmetic
+#pragma unroll
+          for (int j = 0; j < NJ; ++j) {
+            const bool ok = EXACT || c0 + 32 * j + lane < nch;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+              cw[r][j] = ok ? ldg_nc_v4(cr[r] + 16 * (c0 + 32 * j)) : make_uint4(0, 0, 0, 0);
+              sc[r][j] = ok ? __ldg(sr[r] + c0 + 32 * j) : 127u;
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+          const int cj = c0 + 32 * j;  // chunk of lane 0; the lane's chunk is cj + lane
+          if (EXACT || cj + lane < nch) {
+            constexpr int kP = NT == 1 ? 2 : 1;  // partial sums per (row, token)
+            float d[kP][R][NT];
+#pragma unroll
+            for (int i = 0; i < kP; ++i)
+#pragma unroll
+              for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int t = 0; t < NT; ++t) d[i][r][t] = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t wh[R][4];
+#pragma unroll
+              for (int r = 0; r < R; ++r) {
+                const uint32_t word = q == 0 ? cw[r][j].x : q == 1 ? cw[r][j].y : q == 2 ? cw[r][j].z : cw[r][j].w;
+                e2m1x8_to_f16x2(word, wh[r]);
+              }
+#pragma unroll
+              for (int t = 0; t < NT; ++t) {
+                if (t == 0 || t < nt) {  // a group has at least one token
+                  const uint4 xv = __ldg(arow[t] + q * nch + cj);
+#pragma unroll
+                  for (int r = 0; r < R; ++r) {
+                    d[0][r][t] = fma2_f16_f32(wh[r][0], xv.x, d[0][r][t]);
+                    d[kP - 1][r][t] = fma2_f16_f32(wh[r][1], xv.y, d[kP - 1][r][t]);
+                    d[0][r][t] = fma2_f16_f32(wh[r][2], xv.z, d[0][r][t]);
+                    d[kP - 1][r][t] = fma2_f16_f32(wh[r][3], xv.w, d[kP - 1][r][t]);
+                  }
+                }
+              }
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+              const float sf = e8m0_to_f32(sc[r][j]);
+#pragma unroll
+              for (int t = 0; t < NT; ++t)
+                acc[r][t] = fmaf(kP == 2 ? d[0][r][t] + d[kP - 1][r][t] : d[0][r][t], sf, acc[r][t]);
+            }
+          }
+        }
+      }
+      // reduce across the warp and write
 #pragma unroll
       for (int r = 0; r < R; ++r)
 #pragma unroll
-        for (int t = 0; t < NT; ++t) d[r][t] = 0.f;
+        for (int t = 0; t < NT; ++t)
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t wh[R][4];  // decoded once, used for all NT tokens
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const uint32_t word = q == 0 ? cw[b][r].x : q == 1 ? cw[b][r].y : q == 2 ? cw[b][r].z : cw[b][r].w;
-          e2m1x8_to_f16x2(word, wh[r]);
-        }
+          for (int off = 16; off > 0; off >>= 1) acc[r][t] += __shfl_xor_sync(0xFFFFFFFFu, acc[r][t], off);
+      if (KIND == 0) {
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
-          const uint4 xv = xs[static_cast<size_t>(t) * (nch * 4) + q * nch + c];
-          const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-          for (int r = 0; r < R; ++r)
-#pragma unroll
-            for (int m = 0; m < 4; ++m) d[r][t] = fma2_f16_f32(wh[r][m], xw[m], d[r][t]);
+          if (lane == t && t < nt) {
+            float hv = 0.f;
+            if (present) {
+              const float gg = scale_pow2(acc[0][t], aexp[t]);
+              const float uu = scale_pow2(acc[R - 1][t], aexp[t]);
+              hv = (gg / (1.0f + expf(-gg))) * uu;
+            }
+            const uint16_t hb = f32_to_bf16_rne(hv);
+            P.hrow[static_cast<size_t>(p0 + t) * P.I + rb] = hb;
+            atomicMax(P.hmax + p0 + t, static_cast<int>(__float_as_uint(fabsf(bf16_bits_to_f32(hb)))));
+          }
         }
-      }
+      } else {
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const float sf = e8m0_to_f32(sb[b][r]);
+        for (int r = 0; r < R; ++r)
 #pragma unroll
-        for (int t = 0; t < NT; ++t) acc[r][t] = fmaf(d[r][t], sf, acc[r][t]);
-      }
-    }
-  }
-}
-
-template <int R, int NT>
-__device__ __forceinline__ void warp_allreduce(float (&acc)[R][NT]) {
-#pragma unroll
-  for (int r = 0; r < R; ++r)
-#pragma unroll
-    for (int t = 0; t < NT; ++t)
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) acc[r][t] += __shfl_xor_sync(0xFFFFFFFFu, acc[r][t], off);
-}
-
-// ----------------------------------------------------------------------------
-// gate/up: item = (active slot u, block of kWarps * RPW row pairs).
-template <int NT>
-__device__ void gateup_item_tokens(const uint8_t *__restrict__ w13c, const uint8_t *__restrict__ w13s,
-                                   int H, int I, int r0, int rows, const uint4 *xs, const int *ptok_p,
-                                   const int *ptok_exp, uint16_t *__restrict__ hrow) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nch = H / 32;
-  for (int rr = warp; rr < rows; rr += kWarps) {
-    const int r = r0 + rr;
-    const uint8_t *codes[2] = {w13c + static_cast<size_t>(r) * (H / 2),
-                               w13c + static_cast<size_t>(I + r) * (H / 2)};
-    const uint8_t *scales[2] = {w13s + static_cast<size_t>(r) * nch,
-                                w13s + static_cast<size_t>(I + r) * nch};
-    float acc[2][NT];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) acc[0][t] = acc[1][t] = 0.f;
-    mx_rows_dot<2, NT, 4>(codes, scales, nch, xs, acc);
-    warp_allreduce<2, NT>(acc);
-    if (lane < NT) {
-#pragma unroll
-      for (int t = 0; t < NT; ++t)
-        if (t == lane) {
-          const float g = scale_pow2(acc[0][t], ptok_exp[t]);
-          const float u = scale_pow2(acc[1][t], ptok_exp[t]);
-          const float hv = (g / (1.0f + expf(-g))) * u;
-          hrow[static_cast<size_t>(ptok_p[t]) * I + r] = f32_to_bf16_rne(hv);
-        }
-    }
-  }
-}
-
-__global__ void __launch_bounds__(kWarps * 32)
-    ffn_gateup_kernel(k3moe_weights w, int T, int H, int I, int k, int E, int A,
-                      const int32_t *__restrict__ offsets, const int32_t *__restrict__ perm,
-                      const int32_t *__restrict__ active, const int32_t *__restrict__ nactive,
-                      const int32_t *__restrict__ xexp, const uint4 *__restrict__ x16,
-                      uint16_t *__restrict__ hrow, int rows_per_item, int ntmax, int32_t *status) {
-  extern __shared__ uint4 xs[];  // ntmax tokens x H/8 uint4
-  __shared__ int tok_p[kNT], tok_t[kNT], tok_exp[kNT];
-  pdl_wait();
-  pdl_trigger();
-  const int n_act = *nactive;
-  const int items_per_e = (I + rows_per_item - 1) / rows_per_item;
-  const long long n_items = static_cast<long long>(n_act) * items_per_e;
-  for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const int u = static_cast<int>(item / items_per_e);
-    const int r0 = static_cast<int>(item % items_per_e) * rows_per_item;
-    const int rows = min(rows_per_item, I - r0);
-    const int e = active[u];
-    const int p0 = offsets[e], p1 = offsets[e + 1];
-    const bool present = expert_present(w, e);
-    for (int pc = p0; pc < p1; pc += ntmax) {
-      const int nt = min(ntmax, p1 - pc);
-      __syncthreads();  // previous users of xs / tok_* are done
-      if (threadIdx.x < nt) {
-        const int p = pc + threadIdx.x;
-        const int a = perm[p];
-        int t = a / k;
-        if (a < 0 || a >= A) {
-          set_status(status, K3MOE_DEV_BOUNDS);
-          t = -1;
-        }
-        tok_p[threadIdx.x] = p;
-        tok_t[threadIdx.x] = t;
-        tok_exp[threadIdx.x] = t >= 0 ? xexp[t] : 0;
-      }
-      __syncthreads();
-      if (!present) {
-        for (int i = threadIdx.x; i < nt * rows; i += blockDim.x)
-          hrow[static_cast<size_t>(tok_p[i / rows]) * I + r0 + i % rows] = 0;
-        continue;
-      }
-      const int row_u4 = H / 8;
-      for (int i = threadIdx.x; i < nt * row_u4; i += blockDim.x) {
-        const int tt = i / row_u4, j = i % row_u4;
-        const int t = tok_t[tt];
-        xs[i] = t >= 0 ? x16[static_cast<size_t>(t) * row_u4 + j] : make_uint4(0, 0, 0, 0);
-      }
-      __syncthreads();
-      const uint8_t *w13c = w.w13_codes[e], *w13s = w.w13_scales[e];
-      switch (nt) {
-        case 1: gateup_item_tokens<1>(w13c, w13s, H, I, r0, rows, xs, tok_p, tok_exp, hrow); break;
-        case 2: gateup_item_tokens<2>(w13c, w13s, H, I, r0, rows, xs, tok_p, tok_exp, hrow); break;
-        case 3: gateup_item_tokens<3>(w13c, w13s, H, I, r0, rows, xs, tok_p, tok_exp, hrow); break;
-        default: gateup_item_tokens<4>(w13c, w13s, H, I, r0, rows, xs, tok_p, tok_exp, hrow); break;
-      }
-    }
-  }
-}
-
-// ----------------------------------------------------------------------------
-// down: item = (active slot u, block of rows of W2).  Each warp takes 4 rows at a time.
-template <int NT>
-__device__ void down_item_tokens(const uint8_t *__restrict__ w2c, const uint8_t *__restrict__ w2s,
-                                 int H, int I, int r0, int rows, const uint4 *xs, const int *ptok_p,
-                                 const int *ptok_exp, float *__restrict__ Y) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nch = I / 32;
-  for (int rr = warp * 4; rr < rows; rr += kWarps * 4) {
-    const uint8_t *codes[4], *scales[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int r = r0 + min(rr + i, rows - 1);  // clamp: duplicate rows are computed, not stored
-      codes[i] = w2c + static_cast<size_t>(r) * (I / 2);
-      scales[i] = w2s + static_cast<size_t>(r) * nch;
-    }
-    float acc[4][NT];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int t = 0; t < NT; ++t) acc[i][t] = 0.f;
-    mx_rows_dot<4, NT, 2>(codes, scales, nch, xs, acc);
-    warp_allreduce<4, NT>(acc);
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int t = 0; t < NT; ++t)
-        if (lane == i * NT + t && rr + i < rows)
-          Y[static_cast<size_t>(ptok_p[t]) * H + r0 + rr + i] = scale_pow2(acc[i][t], ptok_exp[t]);
-  }
-}
-
-__global__ void __launch_bounds__(kWarps * 32)
-    ffn_down_kernel(k3moe_weights w, int H, int I, int E, const int32_t *__restrict__ offsets,
-                    const int32_t *__restrict__ active, const int32_t *__restrict__ nactive,
-                    const uint16_t *__restrict__ hrow, float *__restrict__ Y, int rows_per_item,
-                    int ntmax) {
-  extern __shared__ uint4 xs[];  // ntmax rows x I/8 uint4
-  __shared__ int tok_p[kNT], tok_exp[kNT];
-  __shared__ float red[kNT][kWarps];
-  pdl_wait();
-  pdl_trigger();
-  const int n_act = *nactive;
-  const int items_per_e = (H + rows_per_item - 1) / rows_per_item;
-  const long long n_items = static_cast<long long>(n_act) * items_per_e;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const int u = static_cast<int>(item / items_per_e);
-    const int r0 = static_cast<int>(item % items_per_e) * rows_per_item;
-    const int rows = min(rows_per_item, H - r0);
-    const int e = active[u];
-    const int p0 = offsets[e], p1 = offsets[e + 1];
-    const bool present = expert_present(w, e);
-    for (int pc = p0; pc < p1; pc += ntmax) {
-      const int nt = min(ntmax, p1 - pc);
-      __syncthreads();
-      if (!present) {
-        for (int i = threadIdx.x; i < nt * rows; i += blockDim.x)
-          Y[static_cast<size_t>(pc + i / rows) * H + r0 + i % rows] = 0.f;
-        continue;
-      }
-      // per-row max |h| (exact prescale), warp tt handles token tt's max
-      for (int tt = 0; tt < nt; ++tt) {
-        const uint16_t *hr = hrow + static_cast<size_t>(pc + tt) * I;
-        float mx = 0.f;
-        for (int c = threadIdx.x; c < I; c += blockDim.x) mx = fmaxf(mx, fabsf(bf16_bits_to_f32(hr[c])));
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-        if (lane == 0) red[tt][warp] = mx;
-      }
-      __syncthreads();
-      if (threadIdx.x < nt) {
-        float mx = red[threadIdx.x][0];
-        for (int i = 1; i < kWarps; ++i) mx = fmaxf(mx, red[threadIdx.x][i]);
-        tok_exp[threadIdx.x] = prescale_exp(mx);
-        tok_p[threadIdx.x] = pc + threadIdx.x;
-      }
-      __syncthreads();
-      const int nch = I / 32, row_u4 = I / 8;
-      for (int i = threadIdx.x; i < nt * row_u4; i += blockDim.x) {
-        const int tt = i / row_u4, piece = i % row_u4, c = piece >> 2, q = piece & 3;
-        const float s = scale_pow2(1.0f, -tok_exp[tt]);
-        const uint4 src = *reinterpret_cast<const uint4 *>(hrow + static_cast<size_t>(pc + tt) * I + 8 * piece);
-        const uint32_t wv[4] = {src.x, src.y, src.z, src.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m)
-          o[m] = pack_f16x2_scaled(__uint_as_float(wv[m] << 16), __uint_as_float(wv[m] & 0xFFFF0000u), s);
-        xs[static_cast<size_t>(tt) * row_u4 + q * nch + c] = make_uint4(o[0], o[1], o[2], o[3]);
-      }
-      __syncthreads();
-      const uint8_t *w2c = w.w2_codes[e], *w2s = w.w2_scales[e];
-      switch (nt) {
-        case 1: down_item_tokens<1>(w2c, w2s, H, I, r0, rows, xs, tok_p, tok_exp, Y); break;
-        case 2: down_item_tokens<2>(w2c, w2s, H, I, r0, rows, xs, tok_p, tok_exp, Y); break;
-        case 3: down_item_tokens<3>(w2c, w2s, H, I, r0, rows, xs, tok_p, tok_exp, Y); break;
-        default: down_item_tokens<4>(w2c, w2s, H, I, r0, rows, xs, tok_p, tok_exp, Y); break;
+          for (int t = 0; t < NT; ++t)
+            if (lane == r * NT + t && t < nt && rb * R + r < P.H)
+              P.Y[static_cast<size_t>(p0 + t) * P.H + rb * R + r] = present ? scale_pow2(acc[r][t], aexp[t]) : 0.f;
       }
     }
   }
@@ -419,65 +394,115 @@ __global__ void __launch_bounds__(kWarps * 32)
 // ----------------------------------------------------------------------------
 size_t ffn_gemv_workspace(const k3moe_shape &s) { return gemv_ws(s.T, s.H, s.I, s.E, s.k).total; }
 
+namespace {
+
+// Blocks of a persistent grid: resident blocks per SM (occupancy, cached per kernel) x SMs.
+template <int KIND, int R, int NT, int NJ, bool EXACT>
+int persistent_grid(int nsm) {
+  static int nb = 0;
+  if (nb == 0) {
+    int v = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, gemv_rows_kernel<KIND, R, NT, NJ, EXACT>, kGvWarps * 32,
+                                                      0) !=
+            cudaSuccess ||
+        v < 1)
+      v = 1;
+    nb = v;
+  }
+  return nsm * nb;
+}
+
+template <int KIND, int R, int NT, int NJ, bool EXACT>
+cudaError_t launch_rows_kernel(const RowsParams &P, int nsm, cudaStream_t st) {
+  return launch_pdl(gemv_rows_kernel<KIND, R, NT, NJ, EXACT>, dim3(persistent_grid<KIND, R, NT, NJ, EXACT>(nsm)),
+                    dim3(kGvWarps * 32), 0, st, P);
+}
+
+// One token.  Gate/up (2 rows): exact instances for K/32 = 32 * NJ with NJ in
+// {2, 4, 7}, else the guarded one holding 8 chunks per lane and row (several
+// segments past K = 8192).  Down (4 rows): 2 chunks per lane and row (exact for
+// K = 2048), more would not fit the registers.
+template <int KIND, int R>
+cudaError_t launch_rows_nt1(const RowsParams &P, int K, int nsm, cudaStream_t st) {
+  const int nch = K / 32;
+  if constexpr (KIND == 1) {
+    if (nch == 64) return launch_rows_kernel<KIND, R, 1, 2, true>(P, nsm, st);
+    return launch_rows_kernel<KIND, R, 1, 2, false>(P, nsm, st);
+  } else {
+    if (nch == 64) return launch_rows_kernel<KIND, R, 1, 2, true>(P, nsm, st);
+    if (nch == 128) return launch_rows_kernel<KIND, R, 1, 4, true>(P, nsm, st);
+    if (nch == 224) return launch_rows_kernel<KIND, R, 1, 7, true>(P, nsm, st);
+    return launch_rows_kernel<KIND, R, 1, 8, false>(P, nsm, st);
+  }
+}
+
+// gate/up -> h to f16 -> down.  P holds the gate/up activations (x16, xexp);
+// h16/hexp are the down activations.
+template <int NT>
+int launch_rows(RowsParams P, int nsm, cudaStream_t st, int A, uint4 *h16, int32_t *hexp) {
+  // chunks per lane and row held in registers: fewer with several tokens (more accumulators)
+  constexpr int kBgu = NT == 2 ? 4 : 2;
+  constexpr int kRdn = NT == 4 ? 2 : kDnRows;  // W2 rows per down item (fewer accumulators with 4 tokens)
+  cudaError_t e;
+  if constexpr (NT == 1) e = launch_rows_nt1<0, 2>(P, P.H, nsm, st);
+  else e = launch_rows_kernel<0, 2, NT, kBgu, false>(P, nsm, st);
+  if (e != cudaSuccess) return -1;
+  if (launch_pdl(gemv_h16_kernel, dim3(A), dim3(256), 0, st, static_cast<const uint16_t *>(P.hrow),
+                 static_cast<const int32_t *>(P.hmax), P.I, h16, hexp) != cudaSuccess)
+    return -1;
+  P.aexp = hexp;
+  P.act = h16;
+  if constexpr (NT == 1) e = launch_rows_nt1<1, kDnRows>(P, P.I, nsm, st);
+  else e = launch_rows_kernel<1, kRdn, NT, 2, false>(P, nsm, st);
+  return e == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace
+
 int launch_ffn_gemv(const k3moe_shape &s, const uint16_t *x, const k3moe_weights &w,
                     const int32_t *offsets, const int32_t *perm, float *Y, void *ws,
                     int32_t *status, cudaStream_t st) {
   if (s.T == 0) return 0;
   const GemvWs L = gemv_ws(s.T, s.H, s.I, s.E, s.k);
   char *base = static_cast<char *>(ws);
-  int32_t *active = reinterpret_cast<int32_t *>(base + L.active);
-  int32_t *nactive = reinterpret_cast<int32_t *>(base + L.nactive);
+  int4 *slots = reinterpret_cast<int4 *>(base + L.slots);
+  int32_t *meta = reinterpret_cast<int32_t *>(base + L.meta);
   int32_t *xexp = reinterpret_cast<int32_t *>(base + L.xexp);
   uint4 *x16 = reinterpret_cast<uint4 *>(base + L.x16);
   uint16_t *hrow = reinterpret_cast<uint16_t *>(base + L.hrow);
+  int32_t *hmax = reinterpret_cast<int32_t *>(base + L.hmax);
+  uint4 *h16 = reinterpret_cast<uint4 *>(base + L.h16);
+  int32_t *hexp = reinterpret_cast<int32_t *>(base + L.hexp);
   const int A = s.T * s.k;
-  int dev = 0, nsm = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-  if (launch_pdl(ffn_prep_kernel, dim3(1 + s.T), dim3(256), 0, st, w, x, s.T, s.H, s.E, A, offsets,
-                 active, nactive, xexp, x16, status) != cudaSuccess)
+  static int nsm = 0;
+  if (nsm == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    if (nsm < 1) nsm = 1;
+  }
+  if (launch_pdl(gemv_prep_kernel, dim3(1 + s.T), dim3(256), 0, st, w, x, s.T, s.H, s.E, A, offsets, slots, meta,
+                 xexp, x16, hmax, status) != cudaSuccess)
     return -1;
-  const int max_act = A < s.E ? A : s.E;
-  const int ntmax = s.T < kNT ? s.T : kNT;
-  // gate/up: kWarps row pairs per item
-  {
-    const int rows_per_item = kWarps;
-    const size_t smem = static_cast<size_t>(ntmax) * s.H * 2;
-    static bool attr_set = false;
-    if (!attr_set) {
-      cudaFuncSetAttribute(ffn_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 4 * 16384 * 2);
-      attr_set = true;
-    }
-    const long long items = static_cast<long long>(max_act) * ((s.I + rows_per_item - 1) / rows_per_item);
-    int nb = 1;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, ffn_gateup_kernel, kWarps * 32, smem);
-    const long long cap = static_cast<long long>(nsm) * (nb > 0 ? nb : 1);
-    const int grid = static_cast<int>(items < cap ? items : cap);
-    if (launch_pdl(ffn_gateup_kernel, dim3(grid), dim3(kWarps * 32), smem, st, w, s.T, s.H, s.I, s.k,
-                   s.E, A, offsets, perm, static_cast<const int32_t *>(active),
-                   static_cast<const int32_t *>(nactive), static_cast<const int32_t *>(xexp),
-                   static_cast<const uint4 *>(x16), hrow, rows_per_item, ntmax, status) != cudaSuccess)
-      return -1;
-  }
-  {
-    const int rows_per_item = kWarps * 4;
-    const size_t smem = static_cast<size_t>(ntmax) * s.I * 2;
-    static bool attr_set = false;
-    if (!attr_set) {
-      cudaFuncSetAttribute(ffn_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 4 * 16384 * 2);
-      attr_set = true;
-    }
-    const long long items = static_cast<long long>(max_act) * ((s.H + rows_per_item - 1) / rows_per_item);
-    int nb = 1;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, ffn_down_kernel, kWarps * 32, smem);
-    const long long cap = static_cast<long long>(nsm) * (nb > 0 ? nb : 1);
-    const int grid = static_cast<int>(items < cap ? items : cap);
-    if (launch_pdl(ffn_down_kernel, dim3(grid), dim3(kWarps * 32), smem, st, w, s.H, s.I, s.E, offsets,
-                   static_cast<const int32_t *>(active), static_cast<const int32_t *>(nactive),
-                   static_cast<const uint16_t *>(hrow), Y, rows_per_item, ntmax) != cudaSuccess)
-      return -1;
-  }
-  return 0;
+  RowsParams P;
+  P.w = w;
+  P.H = s.H;
+  P.I = s.I;
+  P.k = s.k;
+  P.A = A;
+  P.perm = perm;
+  P.slots = slots;
+  P.meta = meta;
+  P.aexp = xexp;
+  P.act = x16;
+  P.hrow = hrow;
+  P.hmax = hmax;
+  P.Y = Y;
+  P.status = status;
+  const int nt = s.T < kGvMaxNT ? s.T : kGvMaxNT;
+  if (nt == 1) return launch_rows<1>(P, nsm, st, A, h16, hexp);
+  if (nt == 2) return launch_rows<2>(P, nsm, st, A, h16, hexp);
+  return launch_rows<4>(P, nsm, st, A, h16, hexp);
 }
 
 }  // namespace k3moe
