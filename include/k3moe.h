@@ -93,16 +93,17 @@ typedef struct {
 
 /* Expert FFN modes.  All compute the same function (bf16 activations, exact
  * MXFP4 weights, fp32 accumulation); they differ in how weights are streamed. */
-#define K3MOE_FFN_AUTO 0   /* the library picks per call                              */
-#define K3MOE_FFN_GEMV 1   /* CUDA-core GEMV kernels, 128-bit register loads (any shape) */
+#define K3MOE_FFN_AUTO 0   /* the library picks per call: GEMM when A = T*k >= 4 * min(A, E)
+                              and the shape allows it, else GEMV                      */
+#define K3MOE_FFN_GEMV 1   /* CUDA-core GEMV kernels, 128-bit register loads (any shape);
+                              each routed expert's weights are read once per call     */
 #define K3MOE_FFN_STREAM 2 /* one persistent CUDA-core kernel fed by 1-D TMA bulk copies
                               into a shared-memory ring; needs H/32 and I/32 multiples of
                               16 and H, I <= 8192 (else K3MOE_ERR_UNSUPPORTED)          */
 #define K3MOE_FFN_GEMM 3   /* grouped GEMMs on the tcgen05 tensor cores (weights dequantised
                               exactly to bf16, fp32 accumulators in tensor memory) for
                               token chunks; needs H and 2I multiples of 128 and I a
-                              multiple of 64 (else K3MOE_ERR_UNSUPPORTED).  AUTO picks it
-                              when A = T*k >= 8 * min(A, E).                            */
+                              multiple of 64 (else K3MOE_ERR_UNSUPPORTED).              */
 
 /* Workspace queries (bytes; 0 when the call needs none).  op is one of: */
 #define K3MOE_OP_BUCKET 1

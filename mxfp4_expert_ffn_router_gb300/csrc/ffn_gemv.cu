@@ -19,7 +19,7 @@
 //   gemv_rows<0> item = (active slot u, row pair i): for each token p of u,
 //                h[p][i] = bf16(silu(Wg_i x_p) * (Wu_i x_p)), max|h[p]| by atomicMax
 //   gemv_h16     h rows -> prescaled f16 (exponent from the row's max |h|)
-//   gemv_rows<1> item = (active slot u, 4 rows of W2; 2 with 4 tokens): Y[p][rows] = W2 rows . h[p]
+//   gemv_rows<1> item = (active slot u, 4 rows of W2): Y[p][rows] = W2 rows . h[p]
 //
 // Work is spread over warps, not blocks: warp w of the grid takes items w, w + W,
 // w + 2W, ... (W = warps in the grid).  An item is streamed in steps of B chunks
@@ -38,7 +38,6 @@ namespace k3moe {
 namespace {
 
 constexpr int kGvWarps = 8;   // warps per block
-constexpr int kGvMaxNT = 4;   // tokens per pass over an item's weights
 constexpr int kDnRows = 4;    // W2 rows per down item
 
 // Workspace layout (byte offsets, 256-aligned pieces).
@@ -236,7 +235,7 @@ __device__ __forceinline__ const uint8_t *ldg_ptr(const uint8_t *const *arr, int
 }
 
 // KIND 0 (gate/up): an item is one row pair (gate row i, up row I + i), K = H.
-// KIND 1 (down):    an item is R consecutive rows of W2 (4, or 2 with 4 tokens), K = I.
+// KIND 1 (down):    an item is R = 4 consecutive rows of W2, K = I.
 // A warp issues every 16-byte code load of its item's K segment (NJ chunks per
 // lane and row, one segment when K <= 32 * 32 * NJ) before it computes, and many
 // warps per SM keep loads in flight while others compute.  EXACT instances serve
@@ -437,24 +436,16 @@ cudaError_t launch_rows_nt1(const RowsParams &P, int K, int nsm, cudaStream_t st
 }
 
 // gate/up -> h to f16 -> down.  P holds the gate/up activations (x16, xexp);
-// h16/hexp are the down activations.
-template <int NT>
+// h16/hexp are the down activations.  Tokens are taken one at a time: an item's
+// weight codes stay in registers while the warp loops over the expert's tokens.
 int launch_rows(RowsParams P, int nsm, cudaStream_t st, int A, uint4 *h16, int32_t *hexp) {
-  // chunks per lane and row held in registers: fewer with several tokens (more accumulators)
-  constexpr int kBgu = NT == 2 ? 4 : 2;
-  constexpr int kRdn = NT == 4 ? 2 : kDnRows;  // W2 rows per down item (fewer accumulators with 4 tokens)
-  cudaError_t e;
-  if constexpr (NT == 1) e = launch_rows_nt1<0, 2>(P, P.H, nsm, st);
-  else e = launch_rows_kernel<0, 2, NT, kBgu, false>(P, nsm, st);
-  if (e != cudaSuccess) return -1;
+  if (launch_rows_nt1<0, 2>(P, P.H, nsm, st) != cudaSuccess) return -1;
   if (launch_pdl(gemv_h16_kernel, dim3(A), dim3(256), 0, st, static_cast<const uint16_t *>(P.hrow),
                  static_cast<const int32_t *>(P.hmax), P.I, h16, hexp) != cudaSuccess)
     return -1;
   P.aexp = hexp;
   P.act = h16;
-  if constexpr (NT == 1) e = launch_rows_nt1<1, kDnRows>(P, P.I, nsm, st);
-  else e = launch_rows_kernel<1, kRdn, NT, 2, false>(P, nsm, st);
-  return e == cudaSuccess ? 0 : -1;
+  return launch_rows_nt1<1, kDnRows>(P, P.I, nsm, st) == cudaSuccess ? 0 : -1;
 }
 
 }  // namespace
@@ -499,10 +490,7 @@ int launch_ffn_gemv(const k3moe_shape &s, const uint16_t *x, const k3moe_weights
   P.hmax = hmax;
   P.Y = Y;
   P.status = status;
-  const int nt = s.T < kGvMaxNT ? s.T : kGvMaxNT;
-  if (nt == 1) return launch_rows<1>(P, nsm, st, A, h16, hexp);
-  if (nt == 2) return launch_rows<2>(P, nsm, st, A, h16, hexp);
-  return launch_rows<4>(P, nsm, st, A, h16, hexp);
+  return launch_rows(P, nsm, st, A, h16, hexp);
 }
 
 }  // namespace k3moe

@@ -58,7 +58,7 @@ extern "C" int k3moe_expert_ffn_noalloc(k3moe_shape s, const uint16_t *x, const 
   if (static_cast<long long>(s.T) * s.k >= (1LL << 31)) return K3MOE_ERR_SHAPE;
   if (mode < K3MOE_FFN_AUTO || mode > K3MOE_FFN_STREAM) return K3MOE_ERR_ARG;
   int resolved = mode;
-  if (mode == K3MOE_FFN_AUTO) resolved = k3moe::ffn_stream_supported(s) ? K3MOE_FFN_STREAM : K3MOE_FFN_GEMV;
+  if (mode == K3MOE_FFN_AUTO) resolved = K3MOE_FFN_GEMV;
   if (resolved == K3MOE_FFN_STREAM && !k3moe::ffn_stream_supported(s)) return K3MOE_ERR_UNSUPPORTED;
   if (s.T == 0) return K3MOE_OK;
   if (!x || !w || !offsets || !perm || !Y) return K3MOE_ERR_ARG;
