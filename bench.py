@@ -265,6 +265,18 @@ def run_reference(a):
     print(json.dumps(line), flush=True)
 
 
+def ffn_kernel_label(s, mode):
+    """The kernels of one k3moe_expert_ffn call in the mode the library resolves."""
+    A = s.T * s.k
+    if mode == 0:
+        gemm_ok = (2 * s.I) % 128 == 0 and s.H % 128 == 0 and s.I % 64 == 0
+        mode = 3 if gemm_ok and A >= 4 * min(A, s.E) else 1
+    return {1: "k3moe_expert_ffn, GEMV mode (gemv_prep + gemv_rows gate/up + gemv_h16 + gemv_rows down)",
+            2: "k3moe_expert_ffn, STREAM mode (stream_prep + ffn_stream_kernel)",
+            3: "k3moe_expert_ffn, GEMM mode (gemm_prep + gemm_sched + rows_to_f16 + ffn_gemm_kernel gate/up "
+               "+ rows_to_f16 + ffn_gemm_kernel down)"}[mode]
+
+
 def workload_config(a, s):
     return {"workload": f"{a.config}: T={s.T} tokens, H={s.H}, I={s.I}, E={s.E}, top-{s.k}, "
                         f"MXFP4 experts resident",
@@ -358,7 +370,9 @@ def run_gpu(a):
     time.sleep(0.2)
     clk = clocks.stop()
     step_ms = np.array([e[0].elapsed_time(e[3]) for e in evs])
+    rb_ms = np.array([e[0].elapsed_time(e[1]) for e in evs])
     ffn_ms = np.array([e[1].elapsed_time(e[2]) for e in evs])
+    comb_ms = np.array([e[2].elapsed_time(e[3]) for e in evs])
     tot_ms = float(step_ms.sum())
     if ws > 1:
         t = torch.tensor([tot_ms], dtype=torch.float64, device=dev)
@@ -376,7 +390,7 @@ def run_gpu(a):
         peak, peak_src = float(peaks["hbm_gbs"]), "measured"
     else:
         peak, peak_src = 6800.0, "fallback"
-    roof = {"bound": "hbm", "kernel": "k3moe_expert_ffn (ffn_prep + ffn_gateup + ffn_down)",
+    roof = {"bound": "hbm", "kernel": ffn_kernel_label(s, a.mode),
             "achieved": achieved, "peak": peak, "peak_source": peak_src, "unit": "GB/s",
             "frac": achieved / peak, "traffic": recorded_traffic(a.config),
             "bytes_per_call": float(ffn_bytes.mean()), "ffn_us_median": float(np.median(ffn_ms) * 1e3)}
@@ -428,6 +442,9 @@ def run_gpu(a):
                 "gpu_launches": launches_per_step * a.steps,
                 "step_us": {"median": float(np.median(step_ms) * 1e3), "min": float(step_ms.min() * 1e3),
                             "max": float(step_ms.max() * 1e3)},
+                "phase_us_median": {"route_bucket": float(np.median(rb_ms) * 1e3),
+                                    "expert_ffn": float(np.median(ffn_ms) * 1e3),
+                                    "combine": float(np.median(comb_ms) * 1e3)},
                 "wall_s_timed_region": t_wall}
         print(json.dumps(line), flush=True)
     if ws > 1:

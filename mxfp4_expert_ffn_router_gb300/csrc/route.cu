@@ -1,119 +1,182 @@
-// route.cu -- router top-k selection and softmax weights (one warp per token).
+// route.cu -- router top-k selection and softmax weights (one block per token).
 //
 // Follows the kimi-k3-in-c CHANGELOG walkthrough, "[0.1.0] Added": each MoE
 // layer routes a token to 16 of 896 experts; the score is the softmax of the
 // router logits renormalised over the selected experts, selection is on the raw
 // fp32 logits (exact comparisons), ties go to the lower expert index.
+//
+// Per token: each logit becomes an order-preserving unsigned key (-0 and +0 the
+// same key).  A 32-step bitwise search finds tau, the largest key with at least
+// k keys >= tau (the k-th largest key); every key > tau is selected, and keys
+// equal to tau are selected in index order until k are taken.  The k picks are
+// ordered by (key descending, index ascending) and their weights are
+// exp(l - m) / sum exp(l - m) over the picks, in double.
 #include "k3moe_dev.cuh"
 #include "k3moe_launch.h"
 
 namespace k3moe {
 
-// PER = logits held per lane (E <= 32 * PER).  Lane l holds experts l + 32 i.
+namespace {
+
+// Order-preserving key of an fp32 value (larger value -> larger key; -0 -> +0).
+// Keys of finite and infinite values are >= 0x007FFFFF (the key of -inf), so 0
+// marks a padding slot that is never selected.
+__device__ __forceinline__ uint32_t sort_key(float v) {
+  uint32_t u = __float_as_uint(v);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Sum of one int per thread over the block (all threads get it).  `buf` holds 32
+// ints; consecutive calls must alternate buffers (the second barrier of a call
+// is the next call's first).
+__device__ __forceinline__ int block_sum(int v, int *buf) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
+  v = __reduce_add_sync(0xFFFFFFFFu, v);
+  if (lane == 0) buf[warp] = v;
+  __syncthreads();
+  return __reduce_add_sync(0xFFFFFFFFu, lane < nwarp ? buf[lane] : 0);
+}
+
+}  // namespace
+
+// PER = logits per thread (E <= PER * blockDim.x); element e = i * blockDim.x + tid.
 template <int PER>
-__global__ void __launch_bounds__(128) route_kernel(const float *__restrict__ logits, int T, int E,
-                                                    int k, int32_t *__restrict__ idx,
-                                                    float *__restrict__ w, int32_t *status) {
+__global__ void __launch_bounds__(1024) route_kernel(const float *__restrict__ logits, int T, int E, int k,
+                                                     int32_t *__restrict__ idx, float *__restrict__ w,
+                                                     int32_t *status) {
   pdl_wait();
   pdl_trigger();
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 4 + (threadIdx.x >> 5);
+  __shared__ int sbuf[2][32];
+  __shared__ int s_n;
+  __shared__ uint32_t s_key[32];
+  __shared__ int s_e[32];
+  __shared__ float s_v[32];
+  __shared__ float s_sorted[32];
+  const int t = blockIdx.x;
   if (t >= T) return;
+  const int tid = threadIdx.x, nth = blockDim.x, lane = tid & 31;
   const float *row = logits + static_cast<size_t>(t) * E;
-  float v[PER];
+  int32_t *it = idx + static_cast<size_t>(t) * k;
+  float *wt = w + static_cast<size_t>(t) * k;
+  uint32_t key[PER];
+  float val[PER];
   bool nan_here = false;
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
-    const int e = lane + 32 * i;
-    v[i] = (e < E) ? __ldg(row + e) : __uint_as_float(0x7FC00000u);  // NaN = not selectable
-    if (e < E && v[i] != v[i]) nan_here = true;
-  }
-  int32_t *it = idx + static_cast<size_t>(t) * k;
-  float *wt = w + static_cast<size_t>(t) * k;
-  if (__any_sync(0xFFFFFFFFu, nan_here)) {
-    if (lane < k) {
-      it[lane] = lane;
-      wt[lane] = 1.0f / static_cast<float>(k);
+    const int e = i * nth + tid;
+    val[i] = 0.f;
+    key[i] = 0u;
+    if (e < E) {
+      val[i] = __ldg(row + e);
+      if (val[i] != val[i]) nan_here = true;
+      key[i] = sort_key(val[i]);
     }
-    if (lane == 0) set_status(status, K3MOE_DEV_NONFINITE);
+  }
+  if (tid == 0) s_n = 0;
+  if (__syncthreads_or(nan_here)) {
+    if (tid < k) {
+      it[tid] = tid;
+      wt[tid] = 1.0f / static_cast<float>(k);
+    }
+    if (tid == 0) set_status(status, K3MOE_DEV_NONFINITE);
     return;
   }
-  // k rounds of a warp-wide arg-max over (value desc, index asc).
-  float my_v = 0.f;
-  int my_e = 0;
-  for (int j = 0; j < k; ++j) {
-    float bv = 0.f;
-    int be = 0x7FFFFFFF;  // "none"
+  // tau = the k-th largest key: the largest value with count(key >= tau) >= k
+  uint32_t tau = 0u;
+  int par = 0;
+  for (int b = 31; b >= 0; --b) {
+    const uint32_t cand = tau | (1u << b);
+    int c = 0;
 #pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      // i ascending = expert index ascending, so a strict '>' keeps the lower index on ties
-      if (v[i] == v[i] && (be == 0x7FFFFFFF || v[i] > bv)) {
-        bv = v[i];
-        be = lane + 32 * i;
+    for (int i = 0; i < PER; ++i) c += key[i] >= cand;
+    if (block_sum(c, sbuf[par]) >= k) tau = cand;
+    par ^= 1;
+  }
+  int c_gt = 0;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) c_gt += key[i] > tau;
+  c_gt = block_sum(c_gt, sbuf[par]);
+  par ^= 1;
+  const int need = k - c_gt;  // ties at tau to take, lowest indices first
+  int ties_before = 0;        // ties in earlier rounds (lower indices)
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const bool tie = key[i] == tau && key[i] != 0u;
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, tie);
+    // exclusive prefix of the per-warp tie counts over the warps of this round
+    const int warp = tid >> 5, nwarp = nth >> 5;
+    int *buf = sbuf[par];
+    par ^= 1;
+    if (lane == 0) buf[warp] = __popc(m);
+    __syncthreads();
+    const int wc = lane < nwarp ? buf[lane] : 0;
+    int incl = wc;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    const int round_total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    const int warp_excl = __shfl_sync(0xFFFFFFFFu, incl - wc, warp);
+    const int rank = ties_before + warp_excl + __popc(m & ((1u << lane) - 1u));
+    const bool sel = key[i] > tau || (tie && rank < need);
+    if (sel) {
+      const int slot = atomicAdd(&s_n, 1);
+      if (slot < 32) {
+        s_key[slot] = key[i];
+        s_e[slot] = i * nth + tid;
+        s_v[slot] = val[i];
       }
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
-      const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, off);
-      if (oe != 0x7FFFFFFF && (be == 0x7FFFFFFF || ov > bv || (ov == bv && oe < be))) {
-        bv = ov;
-        be = oe;
-      }
-    }
-    if ((be & 31) == lane) {  // the owner retires the winner
-#pragma unroll
-      for (int i = 0; i < PER; ++i)
-        if (lane + 32 * i == be) v[i] = __uint_as_float(0x7FC00000u);
-    }
-    if (lane == j) {
-      my_v = bv;
-      my_e = be;
-    }
+    ties_before += round_total;
   }
-  // weights over the k picks; exp and the normalisation in double (exact argument)
-  const float m = __shfl_sync(0xFFFFFFFFu, my_v, 0);
-  const bool active = lane < k;
-  float wj;
-  if (m == -INFINITY) {
-    wj = 1.0f / static_cast<float>(k);
-  } else if (m == INFINITY) {
-    const int ninf = __popc(__ballot_sync(0xFFFFFFFFu, active && my_v == INFINITY));
-    wj = (my_v == INFINITY) ? 1.0f / static_cast<float>(ninf) : 0.0f;
-  } else {
-    const double ex = active ? exp(static_cast<double>(my_v) - static_cast<double>(m)) : 0.0;
-    double sum = ex;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
-    wj = static_cast<float>(ex / sum);
+  __syncthreads();
+  if (tid < k) {  // k picks in shared memory: order by (key desc, index asc)
+    const uint32_t mk = s_key[tid];
+    const int me = s_e[tid];
+    int r = 0;
+    for (int j = 0; j < k; ++j) r += (s_key[j] > mk) || (s_key[j] == mk && s_e[j] < me);
+    it[r] = me;
+    s_sorted[r] = s_v[tid];
   }
-  if (active) {
-    it[lane] = my_e;
-    wt[lane] = wj;
+  __syncthreads();
+  if (tid < 32) {  // weights over the k picks; exp and the normalisation in double
+    const bool active = lane < k;
+    const float my_v = active ? s_sorted[lane] : 0.f;
+    const float m = s_sorted[0];
+    float wj;
+    if (m == -INFINITY) {
+      wj = 1.0f / static_cast<float>(k);
+    } else if (m == INFINITY) {
+      const int ninf = __popc(__ballot_sync(0xFFFFFFFFu, active && my_v == INFINITY));
+      wj = (my_v == INFINITY) ? 1.0f / static_cast<float>(ninf) : 0.0f;
+    } else {
+      const double ex = active ? exp(static_cast<double>(my_v) - static_cast<double>(m)) : 0.0;
+      double sum = ex;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
+      wj = static_cast<float>(ex / sum);
+    }
+    if (active) wt[lane] = wj;
   }
 }
 
 int launch_route(const k3moe_shape &s, const float *logits, int32_t *idx, float *w,
                  int32_t *status, cudaStream_t st) {
   if (s.T == 0) return 0;
-  const dim3 grid((s.T + 3) / 4), block(128);
-  const int per = (s.E + 31) / 32;
+  const int nth = s.E >= 1024 ? 1024 : ((s.E + 31) / 32) * 32;
+  const int per = (s.E + nth - 1) / nth;  // <= 4 for E <= 4096
+  const dim3 grid(s.T), block(nth);
   cudaError_t err;
-#define K3_ROUTE_CASE(P)                                                                        \
-  if (per <= P)                                                                                 \
-    err = launch_pdl(route_kernel<P>, grid, block, 0, st, logits, s.T, s.E, s.k, idx, w, status); \
+  if (per == 1)
+    err = launch_pdl(route_kernel<1>, grid, block, 0, st, logits, s.T, s.E, s.k, idx, w, status);
+  else if (per == 2)
+    err = launch_pdl(route_kernel<2>, grid, block, 0, st, logits, s.T, s.E, s.k, idx, w, status);
+  else if (per <= 4)
+    err = launch_pdl(route_kernel<4>, grid, block, 0, st, logits, s.T, s.E, s.k, idx, w, status);
   else
-  K3_ROUTE_CASE(1)
-  K3_ROUTE_CASE(2)
-  K3_ROUTE_CASE(4)
-  K3_ROUTE_CASE(8)
-  K3_ROUTE_CASE(16)
-  K3_ROUTE_CASE(28)
-  K3_ROUTE_CASE(32)
-  K3_ROUTE_CASE(64)
-  K3_ROUTE_CASE(128)
-  return -1;
-#undef K3_ROUTE_CASE
+    return -1;
   return err == cudaSuccess ? 0 : -1;
 }
 
