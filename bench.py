@@ -8,7 +8,9 @@ A step is one whole MoE layer over one batch of synthetic input (the default
 workload: 1 token, H=7168, I=2048, 896 experts, top-16, all 21 GB of MXFP4
 weights resident in HBM).  Steps rotate over --sets input sets (different
 tokens, so different experts) and a 256 MiB buffer is written between timed
-steps to flush L2.  Prints one JSON line (rank 0).  With N>1 (torchrun) each
+steps to flush L2 unless every step already reads more than twice the L2 in
+expert weights (then the rotating inputs keep L2 cold; --l2-flush forces the
+write).  Prints one JSON line (rank 0).  With N>1 (torchrun) each
 rank runs an independent replica on its own GPU (no collectives on the data
 path); value = tokens of all ranks / the slowest rank's time.
 
@@ -33,6 +35,7 @@ import gen  # noqa: E402
 
 METRIC = "MoE-layer tokens/s + achieved HBM GB/s (decode), FP4 TFLOPS (prefill)"
 L2_FLUSH_BYTES = 256 << 20
+L2_BYTES = 126 << 20  # GB300 L2
 
 
 def parse():
@@ -47,6 +50,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle sample budget")
+    p.add_argument("--l2-flush", action="store_true",
+                   help="write a 256 MiB buffer between timed steps even when the inputs exceed L2")
     p.add_argument("--experts", type=int, default=0,
                    help="override E (small cases for profiling; 0 = the workload's own)")
     return p.parse_args()
@@ -245,6 +250,7 @@ def run_reference(a):
         ffn = time.perf_counter() - t
         return rb / s.T + ffn, 1
 
+    a.l2_mode = l2_policy(a, s, sets)[1]
     for i in range(a.warmup):
         one_step(i)
     tot, toks = 0.0, 0
@@ -265,12 +271,35 @@ def run_reference(a):
     print(json.dumps(line), flush=True)
 
 
+def l2_policy(a, s, sets):
+    """L2 between timed steps.  The inputs rotate over the sets (different routed
+    experts); when every set reads more than twice the L2 in expert weights the
+    steps need no flush, else a 256 MiB buffer is written between them."""
+    min_step_bytes = min(len(np.unique(routed_experts(s, l))) for l, _ in sets) * expert_bytes(s)
+    do_flush = a.l2_flush or min_step_bytes < 2 * L2_BYTES
+    text = (f"{L2_FLUSH_BYTES >> 20} MiB buffer written between timed steps" if do_flush else
+            f"inputs larger than L2: each step reads >= {min_step_bytes / 1e6:.0f} MB of expert weights "
+            f"(L2 {L2_BYTES >> 20} MiB), no flush")
+    return do_flush, text
+
+
+def resolved_mode(s, mode):
+    """The expert FFN mode the library resolves AUTO (0) to for this shape."""
+    if mode != 0:
+        return mode
+    A = s.T * s.k
+    gemm_ok = (2 * s.I) % 128 == 0 and s.H % 128 == 0 and s.I % 64 == 0
+    return 3 if gemm_ok and A >= 4 * min(A, s.E) else 1
+
+
+def ffn_kernel_count(s, mode):
+    """Kernels one k3moe_expert_ffn call launches."""
+    return {1: 4, 2: 2, 3: 6}[resolved_mode(s, mode)]
+
+
 def ffn_kernel_label(s, mode):
     """The kernels of one k3moe_expert_ffn call in the mode the library resolves."""
-    A = s.T * s.k
-    if mode == 0:
-        gemm_ok = (2 * s.I) % 128 == 0 and s.H % 128 == 0 and s.I % 64 == 0
-        mode = 3 if gemm_ok and A >= 4 * min(A, s.E) else 1
+    mode = resolved_mode(s, mode)
     return {1: "k3moe_expert_ffn, GEMV mode (gemv_prep + gemv_rows gate/up + gemv_h16 + gemv_rows down)",
             2: "k3moe_expert_ffn, STREAM mode (stream_prep + ffn_stream_kernel)",
             3: "k3moe_expert_ffn, GEMM mode (gemm_prep + gemm_sched + rows_to_f16 + ffn_gemm_kernel gate/up "
@@ -281,8 +310,8 @@ def workload_config(a, s):
     return {"workload": f"{a.config}: T={s.T} tokens, H={s.H}, I={s.I}, E={s.E}, top-{s.k}, "
                         f"MXFP4 experts resident",
             "tokens": s.T, "hidden": s.H, "intermediate": s.I, "experts": s.E, "top_k": s.k,
-            "l2": f"{L2_FLUSH_BYTES >> 20} MiB buffer written between timed steps; inputs rotate over "
-                  f"{a.sets} sets", "parallelism": f"replicas x{a.gpus}"}
+            "l2": f"{getattr(a, 'l2_mode', 'L2 flushed between steps')}; inputs rotate over {a.sets} sets",
+            "parallelism": f"replicas x{a.gpus}"}
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -325,9 +354,10 @@ def run_gpu(a):
                       device=dev)
     Y = torch.empty((A, s.H), dtype=f32, device=dev)
     out = torch.empty((s.T, s.H), dtype=torch.bfloat16, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    do_flush, a.l2_mode = l2_policy(a, s, sets)
+    flush = torch.empty(L2_FLUSH_BYTES if do_flush else 1, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-    launches_per_step = 1 + (1 if A <= 4096 else 3) + 3 + 1
+    launches_per_step = 1 + (1 if A <= 4096 else 3) + ffn_kernel_count(s, a.mode) + 1
 
     def layer(i, ev=None):
         j = i % nsets
@@ -345,7 +375,8 @@ def run_gpu(a):
             ev[3].record(stream)
 
     for i in range(a.warmup):
-        flush.fill_(i & 0xFF)
+        if do_flush:
+            flush.fill_(i & 0xFF)
         layer(i)
     torch.cuda.synchronize()
     if int(st.item()) != 0:
@@ -360,7 +391,8 @@ def run_gpu(a):
     clocks.mark("t0")
     t_wall = time.perf_counter()
     for i in range(a.steps):
-        flush.fill_((i + 1) & 0xFF)
+        if do_flush:
+            flush.fill_((i + 1) & 0xFF)
         layer(a.warmup + i, evs[i])
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
@@ -408,7 +440,8 @@ def run_gpu(a):
         tot = 0.0
         for i in range(n_e2e + 3):
             j = i % nsets
-            flush.fill_(i & 0xFF)
+            if do_flush:
+                flush.fill_(i & 0xFF)
             ev0.record(stream)
             lg_dev.copy_(lg_h[j], non_blocking=True)
             x_dev.copy_(x_h[j], non_blocking=True)
