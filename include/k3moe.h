@@ -104,6 +104,10 @@ typedef struct {
                               exactly to bf16, fp32 accumulators in tensor memory) for
                               token chunks; needs H and 2I multiples of 128 and I a
                               multiple of 64 (else K3MOE_ERR_UNSUPPORTED).              */
+#define K3MOE_FFN_W4A4 4   /* the GEMM mode with MXFP4 activations: x and h are quantised to
+                              MXFP4 per 32-block (k3moe_quantize_mxfp4's rule) before the
+                              products, which are then exact; same shape rules as GEMM.
+                              Never chosen by AUTO.                                     */
 
 /* Workspace queries (bytes; 0 when the call needs none).  op is one of: */
 #define K3MOE_OP_BUCKET 1
@@ -171,6 +175,22 @@ int k3moe_expert_ffn(k3moe_shape s, const uint16_t *x, const k3moe_weights *w,
 int k3moe_expert_ffn_noalloc(k3moe_shape s, const uint16_t *x, const k3moe_weights *w,
                              const int32_t *offsets, const int32_t *perm, float *Y, int mode,
                              int32_t *dev_status, k3moe_stream_t stream);
+
+/* MXFP4 quantisation of bf16 activations (the W4A4 mode's input step; OCP
+ * Microscaling Formats v1.0, conversion to MXFP4).  Per block of 32 consecutive
+ * values: shared exponent e = floor(log2 amax) - 2 clamped to [-127, 127] (an
+ * all-zero block: e = -127), stored as the E8M0 byte e + 127; each element's code
+ * is |v| / 2^e rounded to the nearest E2M1 value (ties to the even code),
+ * saturating at 6, with the sign bit set iff v < 0 (NaN elements give code 0;
+ * results for blocks holding an infinity are unspecified).
+ *   n      : number of values, a multiple of 32 (rows whose length is a multiple of
+ *            32 may be passed as one run)
+ *   x      : bf16 [n], 16-byte aligned
+ *   codes  : uint8 [n/2], 16-byte aligned; byte i holds values 2i (low nibble), 2i+1
+ *   scales : uint8 [n/32]
+ * Errors: n < 0 or not a multiple of 32 -> K3MOE_ERR_SHAPE; NULL -> ERR_ARG;
+ * misaligned x/codes -> ERR_ALIGN; n == 0 launches nothing. */
+int k3moe_quantize_mxfp4(int64_t n, const uint16_t *x, uint8_t *codes, uint8_t *scales, k3moe_stream_t stream);
 
 /* Combine: out_f32[t] = sum_{j=0..k-1} w[t][j] * Y[inv[t*k+j]], accumulated in
  * fp32 in increasing j; out[t] = bf16_rne(out_f32[t]).

@@ -24,7 +24,7 @@ K3MOE_ERR_WORKSPACE, K3MOE_ERR_ARCH, K3MOE_ERR_LAUNCH, K3MOE_ERR_UNSUPPORTED = -
 K3MOE_ERR_NOALLOC_LIMIT = -8
 K3MOE_NOALLOC_SCRATCH_BYTES = 8 << 20
 K3MOE_DEV_NONFINITE, K3MOE_DEV_BOUNDS, K3MOE_DEV_TIMEOUT = 1, 2, 4
-K3MOE_FFN_AUTO, K3MOE_FFN_GEMV, K3MOE_FFN_STREAM, K3MOE_FFN_GEMM = 0, 1, 2, 3
+K3MOE_FFN_AUTO, K3MOE_FFN_GEMV, K3MOE_FFN_STREAM, K3MOE_FFN_GEMM, K3MOE_FFN_W4A4 = 0, 1, 2, 3, 4
 K3MOE_OP_BUCKET, K3MOE_OP_EXPERT_FFN = 1, 2
 
 
@@ -77,6 +77,8 @@ def lib():
             L.k3moe_expert_ffn_noalloc.restype = i32
             L.k3moe_expert_ffn_noalloc.argtypes = [Shape, vp, ctypes.POINTER(_WeightsC), vp, vp, vp, i32,
                                                    vp, vp]
+            L.k3moe_quantize_mxfp4.restype = i32
+            L.k3moe_quantize_mxfp4.argtypes = [ctypes.c_int64, vp, vp, vp, vp]
             L.k3moe_combine.restype = i32
             L.k3moe_combine.argtypes = [Shape, vp, vp, vp, vp, vp, vp]
             L.k3moe_status_string.restype = ctypes.c_char_p
@@ -190,6 +192,15 @@ def k3moe_expert_ffn_noalloc(shape, x, weights: Weights, offsets, perm, Y, mode=
                                         mode, _ptr(dev_status, torch.int32, "dev_status"),
                                         _stream(stream))
     _check("k3moe_expert_ffn_noalloc", rc)
+
+
+def k3moe_quantize_mxfp4(x, codes, scales, stream=None):
+    """MXFP4 quantisation of bf16 values x [n] (n a multiple of 32) into codes
+    uint8 [n/2] (low nibble = even element) and E8M0 scales uint8 [n/32]."""
+    n = x.numel() if isinstance(x, torch.Tensor) else 0
+    rc = lib().k3moe_quantize_mxfp4(n, _ptr(x, _BF16, "x"), _ptr(codes, torch.uint8, "codes"),
+                                    _ptr(scales, torch.uint8, "scales"), _stream(stream))
+    _check("k3moe_quantize_mxfp4", rc)
 
 
 def k3moe_combine(shape, Y, w, inv, out, out_f32=None, stream=None):

@@ -46,6 +46,7 @@
 
 #include "k3moe_dev.cuh"
 #include "k3moe_launch.h"
+#include "mx_quant.cuh"
 
 namespace k3moe {
 
@@ -339,9 +340,38 @@ __global__ void __launch_bounds__(128)
   asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
 }
 
+// The 8 values of row `s` at columns c .. c+7 (c a multiple of 8; ok = c < K) as
+// fp32.  With A4 they are first quantised to MXFP4 and dequantised (exactly):
+// the 4 lanes sharing a 32-block (lanes 4j..4j+3 hold its 4 pieces of 8) take
+// its largest magnitude with shuffles.  Every lane of the warp must call it.
+template <bool A4>
+__device__ __forceinline__ void load8_act(const uint16_t *s, int c, bool ok, float (&v)[8]) {
+  uint4 u = make_uint4(0, 0, 0, 0);
+  if (ok) u = *reinterpret_cast<const uint4 *>(s + c);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    v[2 * m] = __uint_as_float(w[m] << 16);
+    v[2 * m + 1] = __uint_as_float(w[m] & 0xFFFF0000u);
+  }
+  if (A4) {
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+    const int e = mx_shared_exp(amax);
+    const float x = mx_pow2(e), inv_x = mx_pow2(-e);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = mx_value(mx_code(v[i], inv_x), x);
+  }
+}
+
 // Row p of `dst` (f16) = row of `src` (bf16, K values) times 2^-e, e chosen per
 // row so the largest magnitude lands in [2^14, 2^15): exact for bf16 inputs.
-// Gate/up: src row = x[perm[p] / k]; down: src row = h[p].
+// Gate/up: src row = x[perm[p] / k]; down: src row = h[p].  With A4 (the W4A4
+// mode) the row is first quantised to MXFP4 and dequantised, per 32-block.
+template <bool A4>
 __global__ void __launch_bounds__(256)
     gemm_rows_to_f16_kernel(const uint16_t *__restrict__ src, const int32_t *__restrict__ perm, int k, int A,
                             int K, uint16_t *__restrict__ dst, int32_t *__restrict__ exps, int32_t *status) {
@@ -363,12 +393,12 @@ __global__ void __launch_bounds__(256)
   const uint16_t *s = src + static_cast<size_t>(row) * K;
   __shared__ float red[8];
   float mx = 0.f;
-  for (int c = threadIdx.x * 8; c < K; c += 256 * 8) {
-    const uint4 v = *reinterpret_cast<const uint4 *>(s + c);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  for (int c0 = 0; c0 < K; c0 += 256 * 8) {  // trip count uniform across the block
+    const int c = c0 + threadIdx.x * 8;
+    float v[8];
+    load8_act<A4>(s, c, c < K, v);
 #pragma unroll
-    for (int m = 0; m < 4; ++m)
-      mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[m] << 16)), fabsf(__uint_as_float(w[m] & 0xFFFF0000u))));
+    for (int i = 0; i < 8; ++i) mx = fmaxf(mx, fabsf(v[i]));
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
@@ -379,16 +409,17 @@ __global__ void __launch_bounds__(256)
   const int e = prescale_exp16(mx);
   if (threadIdx.x == 0) exps[p] = e;
   const float sc = mul_pow2(1.0f, -e);
-  for (int c = threadIdx.x * 8; c < K; c += 256 * 8) {
-    const uint4 v = *reinterpret_cast<const uint4 *>(s + c);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  for (int c0 = 0; c0 < K; c0 += 256 * 8) {
+    const int c = c0 + threadIdx.x * 8;
+    float v[8];
+    load8_act<A4>(s, c, c < K, v);
     uint32_t o[4];
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-      const __half2 h = __floats2half2_rn(__uint_as_float(w[m] << 16) * sc, __uint_as_float(w[m] & 0xFFFF0000u) * sc);
+      const __half2 h = __floats2half2_rn(v[2 * m] * sc, v[2 * m + 1] * sc);
       o[m] = *reinterpret_cast<const uint32_t *>(&h);
     }
-    *reinterpret_cast<uint4 *>(d + c) = make_uint4(o[0], o[1], o[2], o[3]);
+    if (c < K) *reinterpret_cast<uint4 *>(d + c) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -739,7 +770,7 @@ bool ffn_gemm_supported(const k3moe_shape &s) {
 }
 
 int launch_ffn_gemm(const k3moe_shape &s, const uint16_t *x, const k3moe_weights &w, const int32_t *offsets,
-                    const int32_t *perm, float *Y, void *ws, int32_t *status, cudaStream_t st) {
+                    const int32_t *perm, float *Y, void *ws, int32_t *status, cudaStream_t st, bool a4) {
   if (s.T == 0) return 0;
   const GemmWs L = gemm_ws(s.T, s.H, s.I, s.E, s.k);
   char *base = static_cast<char *>(ws);
@@ -774,7 +805,8 @@ int launch_ffn_gemm(const k3moe_shape &s, const uint16_t *x, const k3moe_weights
                  static_cast<const int32_t *>(pgu), static_cast<const int32_t *>(pdn), mt_gu, mt_dn, tab_gu, tab_dn,
                  maps) != cudaSuccess)
     return -1;
-  if (launch_pdl(gemm_rows_to_f16_kernel, dim3(A), dim3(256), 0, st, x, perm, s.k, A, s.H, xg, xexp, status) !=
+  auto rows_to_f16 = a4 ? gemm_rows_to_f16_kernel<true> : gemm_rows_to_f16_kernel<false>;
+  if (launch_pdl(rows_to_f16, dim3(A), dim3(256), 0, st, x, perm, s.k, A, s.H, xg, xexp, status) !=
       cudaSuccess)
     return -1;
   static bool attr = false;
@@ -799,7 +831,7 @@ int launch_ffn_gemm(const k3moe_shape &s, const uint16_t *x, const k3moe_weights
   if (launch_pdl(ffn_gemm_kernel, dim3(static_cast<unsigned>(ntile_max * mt_gu)), dim3(kThreadsG), kGemmSmem, st,
                  xmap, P) != cudaSuccess)
     return -1;
-  if (launch_pdl(gemm_rows_to_f16_kernel, dim3(A), dim3(256), 0, st, static_cast<const uint16_t *>(hrow),
+  if (launch_pdl(rows_to_f16, dim3(A), dim3(256), 0, st, static_cast<const uint16_t *>(hrow),
                  static_cast<const int32_t *>(nullptr), 1, A, s.I, h16, hexp, status) != cudaSuccess)
     return -1;
   P.kind = 1;

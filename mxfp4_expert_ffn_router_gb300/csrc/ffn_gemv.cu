@@ -391,6 +391,173 @@ __global__ void __launch_bounds__(kGvWarps * 32, 2) gemv_rows_kernel(RowsParams 
 }
 
 // ----------------------------------------------------------------------------
+// Exact shapes (K = 1024 * NJ), software-pipelined over half items: a lane's NJ
+// chunks per row are split into halves A (HA chunks) and B (NJ - HA).  While half
+// B of item i is computed, half A of the warp's next item is already loading,
+// and half B of the next item loads while the warp finishes item i; so every
+// warp keeps half an item in flight while it computes, with the registers of one
+// item.  Tokens are taken one at a time; with several tokens on an item the next
+// item's halves load during its last token.
+template <int R>
+struct ItemRows {
+  int4 sl;                    // slot record {expert, first position, tokens, present}
+  int rb;                     // row block of the item
+  const uint8_t *cr[R], *sr[R];  // the lane's first code chunk and scale byte of each row
+};
+
+template <int KIND, int R, int NJ>
+__device__ __forceinline__ void item_rows_at(const RowsParams &P, long long item, int per_slot, ItemRows<R> &it) {
+  const int lane = threadIdx.x & 31;
+  constexpr size_t cbytes = 512 * NJ, sbytes = 32 * NJ;  // K/2 and K/32 for K = 1024 * NJ
+  it.sl = __ldg(P.slots + static_cast<int>(item / per_slot));
+  it.rb = static_cast<int>(item % per_slot);
+  const uint8_t *cb = nullptr, *sb = nullptr;
+  if (it.sl.w) {
+    cb = ldg_ptr(KIND == 0 ? P.w.w13_codes : P.w.w2_codes, it.sl.x);
+    sb = ldg_ptr(KIND == 0 ? P.w.w13_scales : P.w.w2_scales, it.sl.x);
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    int row;
+    if (KIND == 0) row = r == 0 ? it.rb : P.I + it.rb;
+    else row = min(it.rb * R + r, P.H - 1);  // rows past H are computed (duplicates), not stored
+    it.cr[r] = cb + row * cbytes + 16 * lane;
+    it.sr[r] = sb + row * sbytes + lane;
+  }
+}
+
+// 16-byte code load / scale byte load kept in program order (issued ahead of use).
+__device__ __forceinline__ uint4 ldg_code_pf(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ldg_u8_pf(const void *p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u8 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+template <int R, int J0, int NH>
+__device__ __forceinline__ void load_half(const ItemRows<R> &it, uint4 (&cw)[R][NH], uint32_t (&sc)[R][NH]) {
+#pragma unroll
+  for (int j = 0; j < NH; ++j)
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      cw[r][j] = ldg_code_pf(it.cr[r] + 16 * 32 * (J0 + j));
+      sc[r][j] = ldg_u8_pf(it.sr[r] + 32 * (J0 + j));
+    }
+}
+
+// acc[r] += lane's share of row r . activation over chunks J0 .. J0 + NH - 1.
+template <int R, int J0, int NH, int NCH>
+__device__ __forceinline__ void compute_half(const uint4 (&cw)[R][NH], const uint32_t (&sc)[R][NH],
+                                             const uint4 *arow, float (&acc)[R]) {
+#pragma unroll
+  for (int j = 0; j < NH; ++j) {
+    float d0[R], d1[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) d0[r] = d1[r] = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 xv = __ldg(arow + q * NCH + 32 * (J0 + j));
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        uint32_t wh[4];
+        const uint32_t word = q == 0 ? cw[r][j].x : q == 1 ? cw[r][j].y : q == 2 ? cw[r][j].z : cw[r][j].w;
+        e2m1x8_to_f16x2(word, wh);
+        d0[r] = fma2_f16_f32(wh[0], xv.x, d0[r]);
+        d1[r] = fma2_f16_f32(wh[1], xv.y, d1[r]);
+        d0[r] = fma2_f16_f32(wh[2], xv.z, d0[r]);
+        d1[r] = fma2_f16_f32(wh[3], xv.w, d1[r]);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) acc[r] = fmaf(d0[r] + d1[r], e8m0_to_f32(sc[r][j]), acc[r]);
+  }
+}
+
+template <int KIND, int R, int NJ>
+__global__ void __launch_bounds__(kGvWarps * 32, 2) gemv_rows_pipe_kernel(RowsParams P) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int HA = (NJ + 1) / 2, HB = NJ - HA;
+  constexpr int NCH = 32 * NJ;  // chunks per row
+  const int lane = threadIdx.x & 31;
+  const int per_slot = KIND == 0 ? P.I : (P.H + R - 1) / R;
+  const long long nitems = static_cast<long long>(P.meta[0]) * per_slot;
+  const long long stride = static_cast<long long>(gridDim.x) * kGvWarps;
+  long long item = static_cast<long long>(blockIdx.x) * kGvWarps + (threadIdx.x >> 5);
+  if (item >= nitems) return;
+  ItemRows<R> cur;
+  item_rows_at<KIND, R, NJ>(P, item, per_slot, cur);
+  uint4 ca[R][HA], cb[R][HB > 0 ? HB : 1];
+  uint32_t sa[R][HA], sb[R][HB > 0 ? HB : 1];
+  if (cur.sl.w) {
+    load_half<R, 0, HA>(cur, ca, sa);
+    if (HB > 0) load_half<R, HA, HB>(cur, cb, sb);
+  }
+  for (;;) {
+    const long long nitem = item + stride;
+    const bool has_next = nitem < nitems;
+    ItemRows<R> nxt;
+    if (has_next) item_rows_at<KIND, R, NJ>(P, nitem, per_slot, nxt);
+    const bool pf = has_next && nxt.sl.w;
+    for (int t = 0; t < cur.sl.z; ++t) {
+      const int p = cur.sl.y + t;
+      const bool last = t == cur.sl.z - 1;
+      int row, ex;
+      if (KIND == 0) {
+        const int a = __ldg(P.perm + p);
+        const bool ok = a >= 0 && a < P.A;
+        if (!ok) set_status(P.status, K3MOE_DEV_BOUNDS);
+        row = ok ? a / P.k : 0;
+      } else {
+        row = p;
+      }
+      ex = __ldg(P.aexp + row);
+      const uint4 *arow = P.act + static_cast<size_t>(row) * (NCH * 4) + lane;
+      float acc[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) acc[r] = 0.f;
+      if (cur.sl.w) compute_half<R, 0, HA, NCH>(ca, sa, arow, acc);
+      if (last && pf) load_half<R, 0, HA>(nxt, ca, sa);  // half A of the next item flies now
+      if (HB > 0) {
+        if (cur.sl.w) compute_half<R, HA, HB, NCH>(cb, sb, arow, acc);
+        if (last && pf) load_half<R, HA, HB>(nxt, cb, sb);
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc[r] += __shfl_xor_sync(0xFFFFFFFFu, acc[r], off);
+      if (KIND == 0) {
+        if (lane == 0) {
+          float hv = 0.f;
+          if (cur.sl.w) {
+            const float gg = scale_pow2(acc[0], ex);
+            const float uu = scale_pow2(acc[R - 1], ex);
+            hv = (gg / (1.0f + expf(-gg))) * uu;
+          }
+          const uint16_t hb = f32_to_bf16_rne(hv);
+          P.hrow[static_cast<size_t>(p) * P.I + cur.rb] = hb;
+          atomicMax(P.hmax + p, static_cast<int>(__float_as_uint(fabsf(bf16_bits_to_f32(hb)))));
+        }
+      } else {
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+          if (lane == r && cur.rb * R + r < P.H)
+            P.Y[static_cast<size_t>(p) * P.H + cur.rb * R + r] = cur.sl.w ? scale_pow2(acc[r], ex) : 0.f;
+      }
+    }
+    if (!has_next) break;
+    item = nitem;
+    cur = nxt;
+  }
+}
+
+// ----------------------------------------------------------------------------
 size_t ffn_gemv_workspace(const k3moe_shape &s) { return gemv_ws(s.T, s.H, s.I, s.E, s.k).total; }
 
 namespace {
@@ -421,16 +588,34 @@ cudaError_t launch_rows_kernel(const RowsParams &P, int nsm, cudaStream_t st) {
 // {2, 4, 7}, else the guarded one holding 8 chunks per lane and row (several
 // segments past K = 8192).  Down (4 rows): 2 chunks per lane and row (exact for
 // K = 2048), more would not fit the registers.
+template <int KIND, int R, int NJ>
+cudaError_t launch_rows_pipe(const RowsParams &P, int nsm, cudaStream_t st) {
+  static int nb = 0;
+  if (nb == 0) {
+    int v = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, gemv_rows_pipe_kernel<KIND, R, NJ>, kGvWarps * 32, 0) !=
+            cudaSuccess ||
+        v < 1)
+      v = 1;
+    nb = v;
+  }
+  return launch_pdl(gemv_rows_pipe_kernel<KIND, R, NJ>, dim3(nsm * nb), dim3(kGvWarps * 32), 0, st, P);
+}
+
+// Gate/up (2 rows): pipelined exact instances for K/32 = 32 * NJ with NJ in
+// {2, 4, 7}, else the guarded kernel holding 8 chunks per lane and row (several
+// segments past K = 8192).  Down (4 rows): the pipelined exact instance for
+// K = 2048, else the guarded kernel with 2 chunks per lane and row.
 template <int KIND, int R>
 cudaError_t launch_rows_nt1(const RowsParams &P, int K, int nsm, cudaStream_t st) {
   const int nch = K / 32;
   if constexpr (KIND == 1) {
-    if (nch == 64) return launch_rows_kernel<KIND, R, 1, 2, true>(P, nsm, st);
+    if (nch == 64) return launch_rows_pipe<KIND, R, 2>(P, nsm, st);
     return launch_rows_kernel<KIND, R, 1, 2, false>(P, nsm, st);
   } else {
-    if (nch == 64) return launch_rows_kernel<KIND, R, 1, 2, true>(P, nsm, st);
-    if (nch == 128) return launch_rows_kernel<KIND, R, 1, 4, true>(P, nsm, st);
-    if (nch == 224) return launch_rows_kernel<KIND, R, 1, 7, true>(P, nsm, st);
+    if (nch == 64) return launch_rows_pipe<KIND, R, 2>(P, nsm, st);
+    if (nch == 128) return launch_rows_pipe<KIND, R, 4>(P, nsm, st);
+    if (nch == 224) return launch_rows_pipe<KIND, R, 7>(P, nsm, st);
     return launch_rows_kernel<KIND, R, 1, 8, false>(P, nsm, st);
   }
 }

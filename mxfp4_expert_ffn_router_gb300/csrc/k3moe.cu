@@ -70,6 +70,7 @@ static int resolve_ffn_mode(const k3moe_shape &s, int mode) {
     case K3MOE_FFN_GEMV: return K3MOE_FFN_GEMV;
     case K3MOE_FFN_STREAM: return k3moe::ffn_stream_supported(s) ? K3MOE_FFN_STREAM : -1;
     case K3MOE_FFN_GEMM: return k3moe::ffn_gemm_supported(s) ? K3MOE_FFN_GEMM : -1;
+    case K3MOE_FFN_W4A4: return k3moe::ffn_gemm_supported(s) ? K3MOE_FFN_W4A4 : -1;
     default: return -1;
   }
 }
@@ -77,7 +78,7 @@ static int resolve_ffn_mode(const k3moe_shape &s, int mode) {
 static size_t ffn_workspace(const k3moe_shape &s, int resolved) {
   if (resolved == K3MOE_FFN_STREAM) return k3moe::ffn_stream_workspace(s);
   if (resolved == K3MOE_FFN_GEMV) return k3moe::ffn_gemv_workspace(s);
-  if (resolved == K3MOE_FFN_GEMM) return k3moe::ffn_gemm_workspace(s);
+  if (resolved == K3MOE_FFN_GEMM || resolved == K3MOE_FFN_W4A4) return k3moe::ffn_gemm_workspace(s);
   return 0;
 }
 
@@ -117,7 +118,7 @@ int k3moe_expert_ffn(k3moe_shape s, const uint16_t *x, const k3moe_weights *w, c
                      int32_t *dev_status, k3moe_stream_t stream) {
   int rc = check_shape(s);
   if (rc) return rc;
-  if (mode < K3MOE_FFN_AUTO || mode > K3MOE_FFN_GEMM) return K3MOE_ERR_ARG;
+  if (mode < K3MOE_FFN_AUTO || mode > K3MOE_FFN_W4A4) return K3MOE_ERR_ARG;
   const int resolved = resolve_ffn_mode(s, mode);
   if (resolved < 0) return K3MOE_ERR_UNSUPPORTED;
   if (s.T == 0) return K3MOE_OK;
@@ -130,9 +131,21 @@ int k3moe_expert_ffn(k3moe_shape s, const uint16_t *x, const k3moe_weights *w, c
   const cudaStream_t st = reinterpret_cast<k3moe_stream>(stream);
   if (resolved == K3MOE_FFN_STREAM)
     return launched(k3moe::launch_ffn_stream(s, x, *w, offsets, perm, Y, ws, dev_status, st));
-  if (resolved == K3MOE_FFN_GEMM)
-    return launched(k3moe::launch_ffn_gemm(s, x, *w, offsets, perm, Y, ws, dev_status, st));
+  if (resolved == K3MOE_FFN_GEMM || resolved == K3MOE_FFN_W4A4)
+    return launched(k3moe::launch_ffn_gemm(s, x, *w, offsets, perm, Y, ws, dev_status, st,
+                                           resolved == K3MOE_FFN_W4A4));
   return launched(k3moe::launch_ffn_gemv(s, x, *w, offsets, perm, Y, ws, dev_status, st));
+}
+
+int k3moe_quantize_mxfp4(int64_t n, const uint16_t *x, uint8_t *codes, uint8_t *scales, k3moe_stream_t stream) {
+  if (n < 0 || n % 32) return K3MOE_ERR_SHAPE;
+  if (n == 0) return K3MOE_OK;
+  if (!x || !codes || !scales) return K3MOE_ERR_ARG;
+  if (!aligned16(x) || !aligned16(codes)) return K3MOE_ERR_ALIGN;
+  int rc;
+  if ((rc = check_arch())) return rc;
+  return launched(k3moe::launch_quantize_mxfp4(static_cast<long long>(n), x, codes, scales,
+                                               reinterpret_cast<k3moe_stream>(stream)));
 }
 
 int k3moe_combine(k3moe_shape s, const float *Y, const float *w, const int32_t *inv, uint16_t *out,

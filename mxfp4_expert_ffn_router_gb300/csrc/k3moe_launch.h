@@ -43,7 +43,8 @@ int launch_ffn_stream(const k3moe_shape &s, const uint16_t *x, const k3moe_weigh
 size_t ffn_gemm_workspace(const k3moe_shape &s);
 bool ffn_gemm_supported(const k3moe_shape &s);
 int launch_ffn_gemm(const k3moe_shape &s, const uint16_t *x, const k3moe_weights &w, const int32_t *offsets,
-                    const int32_t *perm, float *Y, void *ws, int32_t *status, cudaStream_t st);
+                    const int32_t *perm, float *Y, void *ws, int32_t *status, cudaStream_t st, bool a4);
+int launch_quantize_mxfp4(long long n, const uint16_t *x, uint8_t *codes, uint8_t *scales, cudaStream_t st);
 int launch_combine(const k3moe_shape &s, const float *Y, const float *w, const int32_t *inv,
                    uint16_t *out, float *out_f32, cudaStream_t st);
 

@@ -116,3 +116,23 @@ def test_binding_refuses_cpu_tensors(L):
     with pytest.raises(ValueError):
         k3.k3moe_route(s, torch.zeros(4, 8), torch.zeros(4, 2, dtype=torch.int32),
                        torch.zeros(4, 2))
+
+
+def test_quantize_host_validation(L):
+    d = ctypes.c_void_p(256)
+    assert L.k3moe_quantize_mxfp4(ctypes.c_int64(0), None, None, None, None) == k3.K3MOE_OK
+    assert L.k3moe_quantize_mxfp4(ctypes.c_int64(48), d, d, d, None) == k3.K3MOE_ERR_SHAPE
+    assert L.k3moe_quantize_mxfp4(ctypes.c_int64(-32), d, d, d, None) == k3.K3MOE_ERR_SHAPE
+    assert L.k3moe_quantize_mxfp4(ctypes.c_int64(64), None, d, d, None) == k3.K3MOE_ERR_ARG
+    assert L.k3moe_quantize_mxfp4(ctypes.c_int64(64), d, d, None, None) == k3.K3MOE_ERR_ARG
+    assert L.k3moe_quantize_mxfp4(ctypes.c_int64(64), ctypes.c_void_p(258), d, d, None) == k3.K3MOE_ERR_ALIGN
+    assert L.k3moe_quantize_mxfp4(ctypes.c_int64(64), d, ctypes.c_void_p(264), d, None) == k3.K3MOE_ERR_ALIGN
+
+
+def test_w4a4_mode_is_a_valid_mode(L):
+    s = _shape(T=8, H=256, I=128, E=4, k=2)
+    assert L.k3moe_workspace_bytes(s, k3.K3MOE_OP_EXPERT_FFN, k3.K3MOE_FFN_W4A4) == \
+        L.k3moe_workspace_bytes(s, k3.K3MOE_OP_EXPERT_FFN, k3.K3MOE_FFN_GEMM)
+    d = ctypes.c_void_p(256)
+    wz = k3._WeightsC(256, 256, 256, 256)
+    assert L.k3moe_expert_ffn(s, d, ctypes.byref(wz), d, d, d, 5, d, 1 << 30, None, None) == k3.K3MOE_ERR_ARG
