@@ -220,7 +220,7 @@ __device__ __forceinline__ bool decode_tile(const int32_t *pref, const int32_t *
 }
 
 struct GemmWs {
-  size_t active, meta, sp0, scnt, pref_gu, pref_dn, maps, tab_gu, tab_dn, xg, xexp, hrow, h16, hexp, total;
+  size_t active, meta, sp0, scnt, pref_gu, pref_dn, maps, tab_gu, tab_dn, xg, xexp, hrow, h16, hexp, xsc, hsc, total;
 };
 __host__ __device__ inline size_t g256(size_t v) { return (v + 255) & ~size_t(255); }
 __host__ __device__ inline GemmWs gemm_ws(int T, int H, int I, int E, int k) {
@@ -243,6 +243,8 @@ __host__ __device__ inline GemmWs gemm_ws(int T, int H, int I, int E, int k) {
   w.hrow = o;    o = g256(o + sizeof(uint16_t) * A * I);  // h, bf16 (the rounding point)
   w.h16 = o;     o = g256(o + sizeof(uint16_t) * A * I);  // h prescaled to f16
   w.hexp = o;    o = g256(o + sizeof(int32_t) * (A ? A : 1));
+  w.xsc = o;     o = g256(o + 2 * A * (static_cast<size_t>(H) / 32));  // block scales of the x pieces (two per 32-block)
+  w.hsc = o;     o = g256(o + 2 * A * (static_cast<size_t>(I) / 32));  // block scales of the h pieces
   w.total = o;
   return w;
 }
@@ -300,8 +302,9 @@ __global__ void __launch_bounds__(32)
 // Tensor maps of the active experts' weight codes: maps[u] (w13) and
 // maps[E + u] (w2) for active slot u, each the host-encoded template with its
 // global address replaced by the expert's code pointer.  Experts whose code
-// pointers are NULL or not 16-byte aligned keep the template's address; the
-// GEMM treats them as absent and never loads through their map.
+// pointers are NULL or not aligned to align_mask + 1 bytes (16, or 32 for the
+// gapped 4-bit maps) keep the template's address; the GEMM treats them as absent
+// and never loads through their map.
 //
 // The same launch writes the tile tables of both GEMMs: entry t of a table is
 // {active slot, expert, first bucket position, (tokens << 16) | row tile} of
@@ -318,7 +321,8 @@ __global__ void __launch_bounds__(128)
                       k3moe_weights w, const int32_t *__restrict__ active, const int32_t *__restrict__ meta, int E,
                       const int32_t *__restrict__ slot_p0, const int32_t *__restrict__ slot_cnt,
                       const int32_t *__restrict__ pref_gu, const int32_t *__restrict__ pref_dn, int mt_gu, int mt_dn,
-                      int4 *__restrict__ tab_gu, int4 *__restrict__ tab_dn, uint8_t *__restrict__ maps) {
+                      int4 *__restrict__ tab_gu, int4 *__restrict__ tab_dn, uint8_t *__restrict__ maps,
+                      unsigned align_mask) {
   pdl_wait();
   pdl_trigger();
   const int na = meta[0];
@@ -334,7 +338,7 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
   for (int i = 0; i < kMapBytes / 16; ++i) d4[i] = tmpl[i];
   const uint8_t *codes = which ? w.w2_codes[e] : w.w13_codes[e];
-  if (codes && (reinterpret_cast<uintptr_t>(codes) & 15u) == 0)
+  if (codes && (reinterpret_cast<uintptr_t>(codes) & align_mask) == 0)
     asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;" ::"l"(dst), "l"(codes)
                  : "memory");
   asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
@@ -709,6 +713,449 @@ __global__ void __launch_bounds__(kThreadsG, 1)
   }
 }
 
+
+// ============================================================================
+// Block-scaled grouped GEMM: tcgen05.mma with the E8M0 block scales of both
+// operands in tensor memory, so the weight codes go from TMA to the tensor core
+// as they are stored (e2m1, two per byte, low nibble = even column).
+//  * W4A16 (kind::mxf8f6f4, scale_vec::1X, K = 32 per MMA): each bf16 activation
+//    is split into two e4m3 pieces hi + lo with one E8M0 scale per 32-block and
+//    piece (a pre-pass); hi keeps the top 4 significant bits of each value and lo
+//    the rest (a bf16 value has 8), so the pair is exact for every value within
+//    2^11 of its block's largest (smaller values keep at least the hi piece).
+//    This kind reads 4-bit operands as 16 values per 16-byte unit (8 bytes of
+//    codes, 8 bytes of gap): the weight maps use the TMA type that lays packed
+//    4-bit rows out that way (16U4_ALIGN16B), one box = 128 K values x 64 rows.
+//  * W4A4 (kind::mxf4, scale_vec::2X, K = 64 per MMA): activations are the MXFP4
+//    codes and scales of the quantiser rule, both operands dense (two per byte);
+//    products are then exact.
+// Tensor-memory layout of the scale factors (M = 128): the scale bytes of tile
+// row r (or token column n) sit in lane r % 32 of every lane quadrant, column
+// base + r / 32; a 32-bit cell holds the scales of 4 consecutive K blocks and the
+// instruction descriptor's scale-factor id picks the byte.
+// Warps: 0-3 write the scale factors of every stage (tcgen05.st) and run the
+// epilogue; 4 issues the TMA loads (weight codes through the expert's tensor map,
+// activation pieces); 5 owns tensor memory and issues the MMAs.  One ring of
+// stages, each holding the weight codes and the activation pieces of one K range.
+namespace {
+
+constexpr int kBsSfWarps = 4;
+constexpr int kBsTmaWarp = 4;
+constexpr int kBsMmaWarp = 5;
+constexpr int kBsThreads = 6 * 32;
+constexpr int kBsAtomB = kTileN * 128;   // one 128-row x 128-byte swizzled tile (16 KiB)
+constexpr int kBsColSf = kTileN;         // tensor-memory columns: accumulator [0, 128), then 16 per stage
+
+template <bool A4>
+struct BsCfg {
+  static constexpr int KS = A4 ? 256 : 128;      // K per stage (one 128-byte row of codes per operand piece)
+  static constexpr int PIECES = A4 ? 1 : 2;      // activation pieces
+  static constexpr int MMA_K = A4 ? 64 : 32;
+  static constexpr int STEPS = KS / MMA_K;       // MMA K steps per stage and piece (4)
+  static constexpr int STAGES = A4 ? 3 : 2;
+  static constexpr int STAGE_B = (1 + PIECES) * kBsAtomB;  // weight tile + activation pieces
+  // transaction bytes of the weight tile: the gapped 4-bit layout fills 16 KiB of
+  // shared memory from 8 KiB of packed codes and the barrier counts the latter
+  static constexpr int WTX = A4 ? kBsAtomB : kBsAtomB / 2;
+  static constexpr int SMEM = STAGES * STAGE_B;
+  static constexpr int DYN_SMEM = 1024 + (SMEM > kEpiBytes ? SMEM : kEpiBytes);
+};
+static_assert(kBsColSf + 16 * BsCfg<true>::STAGES <= kTmemCols, "tensor-memory budget (W4A4)");
+static_assert(kBsColSf + 16 * BsCfg<false>::STAGES <= kTmemCols, "tensor-memory budget (W4A16)");
+
+// Instruction descriptor of the block-scaled kinds: B scale-factor id [4,6), A
+// format [7,10), B format [10,13), N/8 [17,23), E8M0 scales (bit 23), M/16
+// [24,29), A scale-factor id [29,31).  Formats: E2M1 = 5 and E4M3 = 0 for
+// kind::mxf8f6f4, E2M1 = 1 for kind::mxf4.
+template <bool A4>
+__device__ __forceinline__ uint32_t idesc_bs(int M, int N, int sfa_id, int sfb_id) {
+  const uint32_t af = A4 ? 1u : 5u, bf = A4 ? 1u : 0u;
+  return (static_cast<uint32_t>(sfb_id) << 4) | (af << 7) | (bf << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) | (static_cast<uint32_t>(sfa_id) << 29);
+}
+
+template <bool A4>
+__device__ __forceinline__ void tc_mma_bs(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t tmem_sfa, uint32_t tmem_sfb, uint32_t accumulate) {
+  if (A4)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(tmem_sfa), "r"(tmem_sfb), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(tmem_sfa), "r"(tmem_sfb), "r"(accumulate)
+        : "memory");
+}
+
+// 32 lanes x 32 bit, 4 consecutive columns per thread, registers -> tensor memory.
+__device__ __forceinline__ void tc_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+// 4 bytes of a byte array as a little-endian word (aligned or not).
+__device__ __forceinline__ uint32_t ld_u32_any(const uint8_t *p) {
+  if ((reinterpret_cast<uintptr_t>(p) & 3u) == 0) return *reinterpret_cast<const uint32_t *>(p);
+  return static_cast<uint32_t>(p[0]) | (static_cast<uint32_t>(p[1]) << 8) | (static_cast<uint32_t>(p[2]) << 16) |
+         (static_cast<uint32_t>(p[3]) << 24);
+}
+
+// Bounded wait that also gives up as soon as another role has given up (`abort`
+// in shared memory); a timeout raises the flag.  Returns true when the phase completed.
+__device__ __forceinline__ bool mb_wait_or_abort(uint64_t *b, uint32_t parity, volatile int *abort) {
+  for (long long i = 0; i < kSpinG; ++i) {
+    if (mb_try(b, parity)) return true;
+    if (*abort) return false;
+    if (i > 32) __nanosleep(20);
+  }
+  *abort = 1;
+  return false;
+}
+
+}  // namespace
+
+struct BsParams {
+  k3moe_weights w;
+  int H, I, A, E;
+  const int32_t *meta;
+  const int4 *tab;         // tile table of this GEMM
+  const uint8_t *maps;     // weight-code tensor maps per active slot (w13 at u, w2 at E + u)
+  const uint8_t *bscale;   // activation block scales: piece q of bucket row p at q*A*(K/32) + p*(K/32)
+  uint16_t *hrow;          // [A][I] bf16 (gate/up output)
+  float *Y;                // [A][H]
+  int kind;                // 0 gate/up, 1 down
+  int32_t *status;
+};
+
+template <bool A4>
+__global__ void __launch_bounds__(kBsThreads, 1)
+    ffn_gemm_bs_kernel(const __grid_constant__ CUtensorMap amap, BsParams P) {
+  using C = BsCfg<A4>;
+  extern __shared__ __align__(1024) uint8_t bsm_raw[];
+  uint8_t *bsm = bsm_raw + ((1024u - (su32(bsm_raw) & 1023u)) & 1023u);
+  __shared__ uint64_t full[C::STAGES], empty[C::STAGES], acc_bar;
+  __shared__ uint32_t tmem_holder;
+  __shared__ int s_abort;
+  volatile int *abort = &s_abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_wait();
+  pdl_trigger();
+  const int kind = P.kind;
+  if (static_cast<int>(blockIdx.x) >= P.meta[1 + kind]) return;
+  GemmTile g;
+  {
+    const int4 te = P.tab[blockIdx.x];
+    g.u = te.x;
+    g.e = te.y;
+    g.p0 = te.z;
+    g.n = te.w >> 16;
+    g.m0 = (te.w & 0xFFFF) * kTileM;
+  }
+  const int K = kind == 0 ? P.H : P.I;
+  const int nst = K / C::KS;  // stages (K is a multiple of 256)
+  const int Npad = (g.n + 15) & ~15;
+  const uint8_t *c13 = P.w.w13_codes[g.e], *s13 = P.w.w13_scales[g.e];
+  const uint8_t *c2 = P.w.w2_codes[g.e], *s2 = P.w.w2_scales[g.e];
+  const uintptr_t al = reinterpret_cast<uintptr_t>(c13) | reinterpret_cast<uintptr_t>(c2);
+  // the gapped 4-bit maps (W4A16) want 32-byte bases, the dense ones 16
+  const bool present = c13 && s13 && c2 && s2 && (al & (A4 ? 15u : 31u)) == 0;
+  const uint8_t *wscales = kind == 0 ? s13 : s2;
+  if (tid == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mb_init(&full[s], 1 + kBsSfWarps);  // TMA bytes + one arrival per scale-factor warp
+      mb_init(&empty[s], 1);
+    }
+    mb_init(&acc_bar, 1);
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (!present && c13 && s13 && c2 && s2 && blockIdx.x == 0) set_status(P.status, K3MOE_DEV_BOUNDS);
+  }
+  if (warp == kBsMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&tmem_holder)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_holder;
+  bool timeout = false;
+
+  if (warp < kBsSfWarps) {
+    // ---------------------------------------------------- scale factors
+    // lane l of every warp writes tile rows / token columns l, l+32, l+64, l+96
+    // into its own lane quadrant (the same data in all four); columns of stage s:
+    // SFA at base + 16 s (+4 for blocks 4-7 with W4A4), SFB at base + 16 s + 8
+    // (+4 for the lo piece with W4A16, for blocks 4-7 with W4A4)
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+    const int sbytes = K / 32;
+    const uint8_t *srow[4];
+    int tokrow[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int r = lane + 32 * c;
+      srow[c] = present ? wscales + static_cast<size_t>(tile_wrow(kind, g.m0, r, P.I)) * sbytes : nullptr;
+      tokrow[c] = r < g.n ? g.p0 + r : -1;
+    }
+    for (int a = 0; a < nst; ++a) {
+      const int s = a % C::STAGES;
+      if (!__all_sync(0xFFFFFFFFu, mb_wait_or_abort(&empty[s], (static_cast<uint32_t>(a / C::STAGES) & 1u) ^ 1u,
+                                                    abort))) {
+        timeout = true;
+        break;
+      }
+      const int nb = C::KS / 32;  // scale bytes per row and stage (4 or 8)
+      uint32_t va[2][4], vb[2][4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        va[0][c] = srow[c] ? ld_u32_any(srow[c] + nb * a) : 0u;
+        va[1][c] = (A4 && srow[c]) ? ld_u32_any(srow[c] + nb * a + 4) : 0u;
+        const int p = tokrow[c];
+#pragma unroll
+        for (int gq = 0; gq < 2; ++gq) {
+          const size_t off = A4 ? static_cast<size_t>(p) * sbytes + nb * a + 4 * gq
+                                : static_cast<size_t>(gq) * P.A * sbytes + static_cast<size_t>(p) * sbytes + nb * a;
+          vb[gq][c] = p >= 0 ? *reinterpret_cast<const uint32_t *>(P.bscale + off) : 0u;
+        }
+      }
+      tc_st4(lane_addr + kBsColSf + 16 * s, va[0][0], va[0][1], va[0][2], va[0][3]);
+      if (A4) tc_st4(lane_addr + kBsColSf + 16 * s + 4, va[1][0], va[1][1], va[1][2], va[1][3]);
+      tc_st4(lane_addr + kBsColSf + 16 * s + 8, vb[0][0], vb[0][1], vb[0][2], vb[0][3]);
+      tc_st4(lane_addr + kBsColSf + 16 * s + 12, vb[1][0], vb[1][1], vb[1][2], vb[1][3]);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mb_arrive(&full[s]);
+    }
+  } else if (warp == kBsTmaWarp) {
+    // ---------------------------------------------------- TMA
+    if (lane == 0) {
+      const CUtensorMap *wmap =
+          reinterpret_cast<const CUtensorMap *>(P.maps + static_cast<size_t>(kind * P.E + g.u) * kMapBytes);
+      if (present) asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(wmap) : "memory");
+      const int y0 = tile_wrow(kind, g.m0, 0, P.I), y1 = tile_wrow(kind, g.m0, kWBoxRows, P.I);
+      for (int a = 0; a < nst; ++a) {
+        const int s = a % C::STAGES;
+        if (!mb_wait_or_abort(&empty[s], (static_cast<uint32_t>(a / C::STAGES) & 1u) ^ 1u, abort)) {
+          timeout = true;
+          break;
+        }
+        uint8_t *st = bsm + s * C::STAGE_B;
+        mb_arrive_tx(&full[s], static_cast<uint32_t>((present ? 1 : 0) * C::WTX + C::PIECES * kBsAtomB));
+        if (present) {  // weight codes: K offset in 4-bit values (W4A16 map) or in bytes (W4A4 map)
+          const int wx = A4 ? a * 128 : a * C::KS;
+          tma_load_2d(st, wmap, wx, y0, &full[s]);
+          tma_load_2d(st + kBsAtomB / 2, wmap, wx, y1, &full[s]);
+        }
+#pragma unroll
+        for (int q = 0; q < C::PIECES; ++q)
+          tma_load_2d(st + (1 + q) * kBsAtomB, &amap, a * 128, q * P.A + g.p0, &full[s]);
+      }
+    }
+  } else {
+    // ---------------------------------------------------- MMA issue
+    if (lane == 0) {
+      for (int a = 0; a < nst; ++a) {
+        const int s = a % C::STAGES;
+        if (!mb_wait_or_abort(&full[s], static_cast<uint32_t>(a / C::STAGES) & 1u, abort)) {
+          timeout = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t wa = su32(bsm + s * C::STAGE_B);
+        const uint32_t sf = tmem + kBsColSf + 16 * s;
+#pragma unroll
+        for (int q = 0; q < C::PIECES; ++q)
+#pragma unroll
+          for (int j = 0; j < C::STEPS; ++j) {
+            // both operands advance 32 bytes per step (W4A16: 32 values of the
+            // gapped 4-bit layout / 32 e4m3; W4A4: 64 dense 4-bit values)
+            uint32_t sfa, sfb;
+            int sfa_id, sfb_id;
+            if (A4) {
+              sfa = sf + 4 * (j >> 1);
+              sfb = sf + 8 + 4 * (j >> 1);
+              sfa_id = sfb_id = 2 * (j & 1);
+            } else {
+              sfa = sf;
+              sfb = sf + 8 + 4 * q;
+              sfa_id = sfb_id = j;
+            }
+            tc_mma_bs<A4>(tmem, smem_desc_sw128(wa + 32 * j), smem_desc_sw128(wa + (1 + q) * kBsAtomB + 32 * j),
+                          idesc_bs<A4>(kTileM, Npad, sfa_id, sfb_id), sfa, sfb, (a > 0 || q > 0 || j > 0) ? 1u : 0u);
+          }
+        tc_commit(&empty[s]);
+      }
+      tc_commit(&acc_bar);  // also after an abort: completes when every MMA issued so far has finished
+    }
+  }
+
+  // ---- epilogue (scale-factor warps): lane quadrant = warp, all Npad columns
+  if (warp < kBsSfWarps) {
+    if (!mb_wait(&acc_bar, 0)) {
+      timeout = true;
+      *abort = 1;
+    }
+    tc_fence_after();
+    float *stage = reinterpret_cast<float *>(bsm);  // [kTileN][kTileM + 1]
+    const int row = 32 * warp + lane;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+    for (int c0 = 0; c0 < Npad; c0 += 16) {
+      float v[16];
+      tc_ld16(lane_addr + c0, v);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) stage[(c0 + j) * (kTileM + 1) + row] = v[j];
+    }
+    tc_fence_before();
+    asm volatile("bar.sync 1, %0;" ::"r"(kBsSfWarps * 32) : "memory");
+    if (kind == 0) {
+      // h[p0 + n][m0/2 + i] = bf16(silu(g) * u), g = tile row i, u = tile row 64 + i
+      const int ncols = kTileM / 2;
+      for (int idx = tid; idx < g.n * ncols; idx += kBsSfWarps * 32) {
+        const int n = idx / ncols, i = idx % ncols;
+        float hv = 0.f;
+        if (present) {
+          const float gg = stage[n * (kTileM + 1) + i];
+          const float uu = stage[n * (kTileM + 1) + ncols + i];
+          hv = (gg / (1.0f + expf(-gg))) * uu;
+        }
+        P.hrow[static_cast<size_t>(g.p0 + n) * P.I + (g.m0 >> 1) + i] = f32_to_bf16_rne(hv);
+      }
+    } else {
+      for (int idx = tid; idx < g.n * kTileM; idx += kBsSfWarps * 32) {
+        const int n = idx / kTileM, r = idx % kTileM;
+        P.Y[static_cast<size_t>(g.p0 + n) * P.H + g.m0 + r] = present ? stage[n * (kTileM + 1) + r] : 0.f;
+      }
+    }
+  }
+  if (timeout) set_status(P.status, K3MOE_DEV_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  if (*abort) {
+    // a role gave up: copies it issued may still be landing in shared memory (and
+    // their barrier may never complete), so wait a bounded 2 ms before leaving
+    for (int i = 0; i < 2000; ++i) __nanosleep(1000);
+    __syncthreads();
+  }
+  if (warp == kBsMmaWarp) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+// Activation pieces for the block-scaled GEMM, one block of 256 threads per bucket
+// row p (source row x[perm[p] / k] for gate/up, h[p] for down; 4 lanes per
+// 32-block, 8 values each).  W4A16: e4m3 pieces hi (rows [0, A)) and lo (rows
+// [A, 2A)) of `pieces` [2A][K] with scales [2][A][K/32]: per block, e_hi =
+// floor(log2 amax) - 7 (so amax / 2^e_hi is in [128, 256), inside e4m3), hi =
+// e4m3(v / 2^e_hi), r = v - hi * 2^e_hi (exact), e_lo from max |r| the same way,
+// lo = e4m3(r / 2^e_lo).  W4A4: MXFP4 codes [A][K/2] and scales [A][K/32] by the
+// quantiser rule.
+template <bool A4>
+__global__ void __launch_bounds__(256)
+    gemm_rows_to_pieces_kernel(const uint16_t *__restrict__ src, const int32_t *__restrict__ perm, int k, int A,
+                               int K, uint8_t *__restrict__ pieces, uint8_t *__restrict__ scales,
+                               int32_t *status) {
+  pdl_wait();
+  pdl_trigger();
+  const int p = blockIdx.x;
+  int row = p;
+  if (perm) {
+    const int a = perm[p];
+    row = (a >= 0 && a < A) ? a / k : -1;
+    if (row < 0) set_status(status, K3MOE_DEV_BOUNDS);
+  }
+  const uint16_t *s = row >= 0 ? src + static_cast<size_t>(row) * K : nullptr;
+  const int sbytes = K / 32;
+  for (int c0 = 0; c0 < K; c0 += 256 * 8) {  // trip count uniform across the block
+    const int c = c0 + threadIdx.x * 8;
+    const bool ok = c < K;
+    float v[8];
+    uint4 u = make_uint4(0, 0, 0, 0);
+    if (ok && s) u = *reinterpret_cast<const uint4 *>(s + c);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      v[2 * m] = __uint_as_float(w[m] << 16);
+      v[2 * m + 1] = __uint_as_float(w[m] & 0xFFFF0000u);
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+    if (A4) {
+      const int e = mx_shared_exp(amax);
+      const float inv_x = mx_pow2(-e);
+      uint32_t code = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) code |= mx_code(v[i], inv_x) << (4 * i);
+      if (ok) {
+        *reinterpret_cast<uint32_t *>(pieces + static_cast<size_t>(p) * (K / 2) + c / 2) = code;
+        if ((threadIdx.x & 3) == 0) scales[static_cast<size_t>(p) * sbytes + c / 32] = static_cast<uint8_t>(e + 127);
+      }
+    } else {
+      // hi piece
+      int ehi = -127;
+      if (amax > 0.f && amax != INFINITY) {
+        int ex;
+        frexpf(amax, &ex);  // floor(log2 amax) = ex - 1
+        ehi = max(-127, min(127, ex - 8));
+      }
+      const float inv_hi = mx_pow2(-ehi), x_hi = mx_pow2(ehi);
+      uint32_t hw[2], lw[2];
+      float r[8];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        uint16_t pk;
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pk) : "f"(v[2 * m + 1] * inv_hi), "f"(v[2 * m] * inv_hi));
+        uint32_t hh;
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hh) : "h"(pk));
+        const __half2 h2 = *reinterpret_cast<const __half2 *>(&hh);
+        r[2 * m] = v[2 * m] - __low2float(h2) * x_hi;
+        r[2 * m + 1] = v[2 * m + 1] - __high2float(h2) * x_hi;
+        if (m & 1) hw[m >> 1] |= static_cast<uint32_t>(pk) << 16;
+        else hw[m >> 1] = pk;
+      }
+      float rmax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) rmax = fmaxf(rmax, fabsf(r[i]));
+      rmax = fmaxf(rmax, __shfl_xor_sync(0xFFFFFFFFu, rmax, 1));
+      rmax = fmaxf(rmax, __shfl_xor_sync(0xFFFFFFFFu, rmax, 2));
+      int elo = -127;
+      if (rmax > 0.f && rmax != INFINITY) {
+        int ex;
+        frexpf(rmax, &ex);
+        elo = max(-127, min(127, ex - 8));
+      }
+      const float inv_lo = mx_pow2(-elo);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        uint16_t pk;
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pk) : "f"(r[2 * m + 1] * inv_lo), "f"(r[2 * m] * inv_lo));
+        if (m & 1) lw[m >> 1] |= static_cast<uint32_t>(pk) << 16;
+        else lw[m >> 1] = pk;
+      }
+      if (ok) {
+        *reinterpret_cast<uint2 *>(pieces + static_cast<size_t>(p) * K + c) = make_uint2(hw[0], hw[1]);
+        *reinterpret_cast<uint2 *>(pieces + static_cast<size_t>(A + p) * K + c) = make_uint2(lw[0], lw[1]);
+        if ((threadIdx.x & 3) == 0) {
+          scales[static_cast<size_t>(p) * sbytes + c / 32] = static_cast<uint8_t>(ehi + 127);
+          scales[static_cast<size_t>(A + p) * sbytes + c / 32] = static_cast<uint8_t>(elo + 127);
+        }
+      }
+    }
+  }
+}
+
 // ----------------------------------------------------------------------------
 namespace {
 
@@ -760,6 +1207,74 @@ bool make_code_map(CUtensorMap *m, void *base, int rows, int kbytes) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D map over the weight codes of one expert as 4-bit values (rows x K) laid out
+// in shared memory with 8-byte gaps after every 8 bytes of codes (the layout
+// kind::mxf8f6f4 reads 4-bit operands in): box = 128 values (128 bytes in shared
+// memory) x 64 rows, 128B swizzle.  Bases and row strides must be 32-byte aligned.
+bool make_code_map_gapped(CUtensorMap *m, void *base, int rows, int K) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) / 2};
+  const cuuint32_t box[2] = {128, kWBoxRows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D map over activation bytes (rows x row_bytes): box = 128 bytes x 128 rows,
+// 128B swizzle; rows past the end read as zero.
+bool make_byte_map(CUtensorMap *m, void *base, int rows, int row_bytes) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+  const cuuint32_t box[2] = {128, kTileN};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The block-scaled GEMM (both projections): pieces pre-pass -> gate/up -> pieces
+// of h -> down.
+template <bool A4>
+int launch_gemm_bs(const k3moe_shape &s, const uint16_t *x, const int32_t *perm, int A, long long ntile_max,
+                   int mt_gu, int mt_dn, BsParams P, const int4 *tab_dn, uint8_t *xp, uint8_t *xsc, uint8_t *hp,
+                   uint8_t *hsc, int32_t *status, cudaStream_t st) {
+  using C = BsCfg<A4>;
+  CUtensorMap xmap, hmap;
+  const int prow = A4 ? A : 2 * A;  // rows of the activation byte arrays (pieces stacked)
+  if (!make_byte_map(&xmap, xp, prow, A4 ? s.H / 2 : s.H) || !make_byte_map(&hmap, hp, prow, A4 ? s.I / 2 : s.I))
+    return -1;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(ffn_gemm_bs_kernel<A4>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::DYN_SMEM) !=
+        cudaSuccess)
+      return -1;
+    attr = true;
+  }
+  if (launch_pdl(gemm_rows_to_pieces_kernel<A4>, dim3(A), dim3(256), 0, st, x, perm, s.k, A, s.H, xp, xsc,
+                 status) != cudaSuccess)
+    return -1;
+  P.kind = 0;
+  P.bscale = xsc;
+  if (launch_pdl(ffn_gemm_bs_kernel<A4>, dim3(static_cast<unsigned>(ntile_max * mt_gu)), dim3(kBsThreads),
+                 C::DYN_SMEM, st, xmap, P) != cudaSuccess)
+    return -1;
+  if (launch_pdl(gemm_rows_to_pieces_kernel<A4>, dim3(A), dim3(256), 0, st, static_cast<const uint16_t *>(P.hrow),
+                 static_cast<const int32_t *>(nullptr), 1, A, s.I, hp, hsc, status) != cudaSuccess)
+    return -1;
+  P.kind = 1;
+  P.tab = tab_dn;
+  P.bscale = hsc;
+  if (launch_pdl(ffn_gemm_bs_kernel<A4>, dim3(static_cast<unsigned>(ntile_max * mt_dn)), dim3(kBsThreads),
+                 C::DYN_SMEM, st, hmap, P) != cudaSuccess)
+    return -1;
+  return 0;
+}
+
 }  // namespace
 
 size_t ffn_gemm_workspace(const k3moe_shape &s) { return gemm_ws(s.T, s.H, s.I, s.E, s.k).total; }
@@ -799,12 +1314,31 @@ int launch_ffn_gemm(const k3moe_shape &s, const uint16_t *x, const k3moe_weights
   // upper bound of the token tiles: sum_e ceil(n_e / 128) <= A / 128 + min(A, E)
   const long long ntile_max = A / kTileN + (A < s.E ? A : s.E);
   const long long sched_threads = std::max<long long>(2LL * s.E, ntile_max * std::max(mt_gu, mt_dn));
+  const bool bs = s.H % kWK == 0 && s.I % kWK == 0;  // the block-scaled tensor-core path
+  if (bs && !a4) {  // W4A16 on kind::mxf8f6f4 reads the weight codes through gapped 4-bit maps
+    if (!make_code_map_gapped(&t13, maps, 2 * s.I, s.H) || !make_code_map_gapped(&t2, maps, s.H, s.I)) return -1;
+  }
   if (launch_pdl(gemm_sched_kernel, dim3(static_cast<unsigned>((sched_threads + 127) / 128)), dim3(128), 0, st, t13,
                  t2, w, static_cast<const int32_t *>(active), static_cast<const int32_t *>(meta), s.E,
                  static_cast<const int32_t *>(sp0), static_cast<const int32_t *>(scnt),
                  static_cast<const int32_t *>(pgu), static_cast<const int32_t *>(pdn), mt_gu, mt_dn, tab_gu, tab_dn,
-                 maps) != cudaSuccess)
+                 maps, (bs && !a4) ? 31u : 15u) != cudaSuccess)
     return -1;
+  if (bs) {
+    BsParams B;
+    B.w = w;
+    B.H = s.H; B.I = s.I; B.A = A; B.E = s.E;
+    B.meta = meta;
+    B.tab = tab_gu;
+    B.maps = maps;
+    B.hrow = hrow;
+    B.Y = Y;
+    B.status = status;
+    uint8_t *xp = reinterpret_cast<uint8_t *>(xg), *hp = reinterpret_cast<uint8_t *>(h16);
+    uint8_t *xsc = reinterpret_cast<uint8_t *>(base + L.xsc), *hsc = reinterpret_cast<uint8_t *>(base + L.hsc);
+    return a4 ? launch_gemm_bs<true>(s, x, perm, A, ntile_max, mt_gu, mt_dn, B, tab_dn, xp, xsc, hp, hsc, status, st)
+              : launch_gemm_bs<false>(s, x, perm, A, ntile_max, mt_gu, mt_dn, B, tab_dn, xp, xsc, hp, hsc, status, st);
+  }
   auto rows_to_f16 = a4 ? gemm_rows_to_f16_kernel<true> : gemm_rows_to_f16_kernel<false>;
   if (launch_pdl(rows_to_f16, dim3(A), dim3(256), 0, st, x, perm, s.k, A, s.H, xg, xexp, status) !=
       cudaSuccess)
