@@ -45,7 +45,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--config", default="decode", choices=sorted(gen.CONFIGS))
     p.add_argument("--impl", default="k3moe", choices=["k3moe", "reference"])
-    p.add_argument("--mode", type=int, default=0, help="expert FFN mode (0 auto, 1 gemv)")
+    p.add_argument("--mode", type=int, default=0, help="expert FFN mode (0 auto, 1 gemv, 2 stream, 3 gemm, 4 w4a4)")
     p.add_argument("--sets", type=int, default=64, help="rotating input sets")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -54,6 +54,8 @@ def parse():
                    help="write a 256 MiB buffer between timed steps even when the inputs exceed L2")
     p.add_argument("--experts", type=int, default=0,
                    help="override E (small cases for profiling; 0 = the workload's own)")
+    p.add_argument("--tokens", type=int, default=0,
+                   help="override T (small cases for profiling; 0 = the workload's own)")
     return p.parse_args()
 
 
@@ -211,6 +213,8 @@ def workload_shape(a):
     s = gen.CONFIGS[a.config]
     if a.experts:
         s = gen.Shape(s.T, s.H, s.I, a.experts, min(s.k, a.experts))
+    if a.tokens:
+        s = gen.Shape(a.tokens, s.H, s.I, s.E, s.k)
     return s
 
 
@@ -294,7 +298,7 @@ def resolved_mode(s, mode):
 
 def ffn_kernel_count(s, mode):
     """Kernels one k3moe_expert_ffn call launches."""
-    return {1: 4, 2: 2, 3: 6}[resolved_mode(s, mode)]
+    return {1: 4, 2: 2, 3: 6, 4: 6}[resolved_mode(s, mode)]
 
 
 def ffn_kernel_label(s, mode):
@@ -302,8 +306,32 @@ def ffn_kernel_label(s, mode):
     mode = resolved_mode(s, mode)
     return {1: "k3moe_expert_ffn, GEMV mode (gemv_prep + gemv_rows gate/up + gemv_h16 + gemv_rows down)",
             2: "k3moe_expert_ffn, STREAM mode (stream_prep + ffn_stream_kernel)",
-            3: "k3moe_expert_ffn, GEMM mode (gemm_prep + gemm_sched + rows_to_f16 + ffn_gemm_kernel gate/up "
-               "+ rows_to_f16 + ffn_gemm_kernel down)"}[mode]
+            3: "k3moe_expert_ffn, GEMM mode (gemm_prep + gemm_sched + rows_to_pieces + ffn_gemm_bs_kernel "
+               "gate/up + rows_to_pieces + ffn_gemm_bs_kernel down; kind::mxf8f6f4, e2m1 x e4m3 hi/lo)",
+            4: "k3moe_expert_ffn, W4A4 mode (gemm_prep + gemm_sched + rows_to_pieces + ffn_gemm_bs_kernel "
+               "gate/up + rows_to_pieces + ffn_gemm_bs_kernel down; kind::mxf4)"}[mode]
+
+
+def tensor_figures(s, mode, ffn_s):
+    """Tensor-pipe view of a GEMM-mode expert FFN: useful FLOPs (2 A (2I H + H I)),
+    FLOPs the MMAs execute (W4A16 runs every product twice, for the hi and lo
+    activation pieces), and the dense peak of the MMA kind: the measured bf16 peak
+    times the nominal ratio (fp8/fp6/fp4 operands 2x, kind::mxf4 6x)."""
+    mode = resolved_mode(s, mode)
+    if mode not in (3, 4):
+        return None
+    A = s.T * s.k
+    useful = 2.0 * A * 3 * s.H * s.I
+    executed = useful * (2 if mode == 3 else 1)
+    peaks = measured_peaks()
+    bf16 = float(peaks["bf16_tflops"]) if peaks and "bf16_tflops" in peaks else 1900.0
+    ratio = 2.0 if mode == 3 else 6.0
+    peak = bf16 * ratio
+    tf = executed / ffn_s / 1e12
+    return {"kind": "mxf8f6f4 (e2m1 x e4m3, 2 pieces)" if mode == 3 else "mxf4 (e2m1 x e2m1)",
+            "useful_tflops": useful / ffn_s / 1e12, "executed_tflops": tf, "peak_tflops": peak,
+            "peak_source": ("measured bf16 x %g" % ratio) if peaks else ("fallback bf16 x %g" % ratio),
+            "frac": tf / peak, "fp4_dense_frac": useful / ffn_s / 1e12 / (bf16 * 6.0)}
 
 
 def workload_config(a, s):
@@ -425,7 +453,8 @@ def run_gpu(a):
     roof = {"bound": "hbm", "kernel": ffn_kernel_label(s, a.mode),
             "achieved": achieved, "peak": peak, "peak_source": peak_src, "unit": "GB/s",
             "frac": achieved / peak, "traffic": recorded_traffic(a.config),
-            "bytes_per_call": float(ffn_bytes.mean()), "ffn_us_median": float(np.median(ffn_ms) * 1e3)}
+            "bytes_per_call": float(ffn_bytes.mean()), "ffn_us_median": float(np.median(ffn_ms) * 1e3),
+            "tensor": tensor_figures(s, a.mode, float(np.median(ffn_ms)) / 1e3)}
 
     # ------------------------------------------------------------- end to end (host buffers)
     e2e = None

@@ -104,6 +104,15 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(su32(bar))
       : "memory");
 }
+// 2-D TMA prefetch of one box into L2 (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
 __device__ __forceinline__ bool mb_wait(uint64_t *b, uint32_t parity) {
   for (long long i = 0; i < kSpinG; ++i) {
     if (mb_try(b, parity)) return true;
@@ -745,6 +754,7 @@ constexpr int kBsMmaWarp = 5;
 constexpr int kBsThreads = 6 * 32;
 constexpr int kBsAtomB = kTileN * 128;   // one 128-row x 128-byte swizzled tile (16 KiB)
 constexpr int kBsColSf = kTileN;         // tensor-memory columns: accumulator [0, 128), then 16 per stage
+constexpr int kBsAhead = 8;              // weight-code stages prefetched into L2 ahead of the ring
 
 template <bool A4>
 struct BsCfg {
@@ -759,9 +769,15 @@ struct BsCfg {
   static constexpr int WTX = A4 ? kBsAtomB : kBsAtomB / 2;
   static constexpr int SMEM = STAGES * STAGE_B;
   static constexpr int DYN_SMEM = 1024 + (SMEM > kEpiBytes ? SMEM : kEpiBytes);
+  // Scale factors travel in chunks of 16 bytes per row (512 K values): CH stages.
+  // A chunk takes 16 tensor-memory columns per operand (weights, then each
+  // activation piece): 4 words of 4 block scales x 4 row groups of 32.
+  static constexpr int CH = 512 / KS;
+  static constexpr int SF_CHUNK_COLS = 16 * (1 + PIECES);
 };
-static_assert(kBsColSf + 16 * BsCfg<true>::STAGES <= kTmemCols, "tensor-memory budget (W4A4)");
-static_assert(kBsColSf + 16 * BsCfg<false>::STAGES <= kTmemCols, "tensor-memory budget (W4A16)");
+// two chunk slots of scale factors after the accumulator
+static_assert(kBsColSf + 2 * BsCfg<true>::SF_CHUNK_COLS <= kTmemCols, "tensor-memory budget (W4A4)");
+static_assert(kBsColSf + 2 * BsCfg<false>::SF_CHUNK_COLS <= kTmemCols, "tensor-memory budget (W4A16)");
 
 // Instruction descriptor of the block-scaled kinds: B scale-factor id [4,6), A
 // format [7,10), B format [10,13), N/8 [17,23), E8M0 scales (bit 23), M/16
@@ -793,19 +809,44 @@ __device__ __forceinline__ void tc_mma_bs(uint32_t tmem_d, uint64_t adesc, uint6
         : "memory");
 }
 
-// 32 lanes x 32 bit, 4 consecutive columns per thread, registers -> tensor memory.
-__device__ __forceinline__ void tc_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
+// 32 lanes x 32 bit, 16 consecutive columns per thread, registers -> tensor
+// memory (no wait: the caller waits once for several stores).
+__device__ __forceinline__ void tc_st16_nw(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
 }
 
-// 4 bytes of a byte array as a little-endian word (aligned or not).
-__device__ __forceinline__ uint32_t ld_u32_any(const uint8_t *p) {
-  if ((reinterpret_cast<uintptr_t>(p) & 3u) == 0) return *reinterpret_cast<const uint32_t *>(p);
-  return static_cast<uint32_t>(p[0]) | (static_cast<uint32_t>(p[1]) << 8) | (static_cast<uint32_t>(p[2]) << 16) |
-         (static_cast<uint32_t>(p[3]) << 24);
+// `valid` (16 or 8) bytes of a byte array as four little-endian words, zero
+// beyond `valid`; any alignment (the out-of-line path takes what is not one
+// aligned 16-byte load).
+__device__ __noinline__ uint4 ld_sf16_slow(const uint8_t *p, int valid) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  if ((a & 7u) == 0) {
+    const uint2 lo = *reinterpret_cast<const uint2 *>(p);
+    const uint2 hi = valid == 16 ? *reinterpret_cast<const uint2 *>(p + 8) : make_uint2(0u, 0u);
+    return make_uint4(lo.x, lo.y, hi.x, hi.y);
+  }
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    if (i < valid) w[i >> 2] |= static_cast<uint32_t>(p[i]) << (8 * (i & 3));
+  return make_uint4(w[0], w[1], w[2], w[3]);
 }
+__device__ __forceinline__ uint4 ld_sf16(const uint8_t *p, int valid) {
+  if (valid == 16 && (reinterpret_cast<uintptr_t>(p) & 15u) == 0) return *reinterpret_cast<const uint4 *>(p);
+  return ld_sf16_slow(p, valid);
+}
+
+// One chunk of scale words for the 128 rows / token columns a lane covers
+// (lane + 32 c): weights, then the activation pieces.
+struct SfChunk {
+  uint4 w[4];
+  uint4 b[2][4];
+};
 
 // Bounded wait that also gives up as soon as another role has given up (`abort`
 // in shared memory); a timeout raises the flag.  Returns true when the phase completed.
@@ -835,12 +876,12 @@ struct BsParams {
 };
 
 template <bool A4>
-__global__ void __launch_bounds__(kBsThreads, 1)
+__global__ void __launch_bounds__(kBsThreads, 2)
     ffn_gemm_bs_kernel(const __grid_constant__ CUtensorMap amap, BsParams P) {
   using C = BsCfg<A4>;
   extern __shared__ __align__(1024) uint8_t bsm_raw[];
   uint8_t *bsm = bsm_raw + ((1024u - (su32(bsm_raw) & 1023u)) & 1023u);
-  __shared__ uint64_t full[C::STAGES], empty[C::STAGES], acc_bar;
+  __shared__ uint64_t full[C::STAGES], empty[C::STAGES], sf_full[2], sf_empty[2], acc_bar;
   __shared__ uint32_t tmem_holder;
   __shared__ int s_abort;
   volatile int *abort = &s_abort;
@@ -869,8 +910,12 @@ __global__ void __launch_bounds__(kBsThreads, 1)
   const uint8_t *wscales = kind == 0 ? s13 : s2;
   if (tid == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mb_init(&full[s], 1 + kBsSfWarps);  // TMA bytes + one arrival per scale-factor warp
+      mb_init(&full[s], 1);  // TMA bytes
       mb_init(&empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mb_init(&sf_full[s], kBsSfWarps);  // one arrival per scale-factor warp
+      mb_init(&sf_empty[s], 1);
     }
     mb_init(&acc_bar, 1);
     s_abort = 0;
@@ -891,12 +936,14 @@ __global__ void __launch_bounds__(kBsThreads, 1)
 
   if (warp < kBsSfWarps) {
     // ---------------------------------------------------- scale factors
-    // lane l of every warp writes tile rows / token columns l, l+32, l+64, l+96
-    // into its own lane quadrant (the same data in all four); columns of stage s:
-    // SFA at base + 16 s (+4 for blocks 4-7 with W4A4), SFB at base + 16 s + 8
-    // (+4 for the lo piece with W4A16, for blocks 4-7 with W4A4)
+    // Lane l of every warp writes rows / token columns l, l+32, l+64, l+96 into
+    // its own lane quadrant (the same data in all four).  Chunk ch (stages
+    // [CH ch, CH ch + CH)) goes to slot ch & 1: weights at columns +0..15, piece
+    // q at +16 (q+1); column 4 w + c holds scale word w of row group c.  Loads run
+    // two chunks ahead of the stores in two register sets.
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * warp) << 16);
     const int sbytes = K / 32;
+    const int nch = (nst + C::CH - 1) / C::CH;
     const uint8_t *srow[4];
     int tokrow[4];
 #pragma unroll
@@ -904,37 +951,66 @@ __global__ void __launch_bounds__(kBsThreads, 1)
       const int r = lane + 32 * c;
       srow[c] = present ? wscales + static_cast<size_t>(tile_wrow(kind, g.m0, r, P.I)) * sbytes : nullptr;
       tokrow[c] = r < g.n ? g.p0 + r : -1;
-    }
-    for (int a = 0; a < nst; ++a) {
-      const int s = a % C::STAGES;
-      if (!__all_sync(0xFFFFFFFFu, mb_wait_or_abort(&empty[s], (static_cast<uint32_t>(a / C::STAGES) & 1u) ^ 1u,
-                                                    abort))) {
-        timeout = true;
-        break;
+      if (srow[c]) {  // the tile's weight-scale rows are read once, 16 bytes per chunk: pull them into L2 now
+        for (int off = 0; off < sbytes; off += 128) prefetch_l2(srow[c] + off);
+        prefetch_l2(srow[c] + sbytes - 1);
       }
-      const int nb = C::KS / 32;  // scale bytes per row and stage (4 or 8)
-      uint32_t va[2][4], vb[2][4];
+    }
+    auto load_chunk = [&](int ch, SfChunk &R) {
+      const int off = 16 * ch;
+      const int valid = sbytes - off < 16 ? sbytes - off : 16;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        va[0][c] = srow[c] ? ld_u32_any(srow[c] + nb * a) : 0u;
-        va[1][c] = (A4 && srow[c]) ? ld_u32_any(srow[c] + nb * a + 4) : 0u;
+        R.w[c] = srow[c] ? ld_sf16(srow[c] + off, valid) : make_uint4(0u, 0u, 0u, 0u);
         const int p = tokrow[c];
 #pragma unroll
-        for (int gq = 0; gq < 2; ++gq) {
-          const size_t off = A4 ? static_cast<size_t>(p) * sbytes + nb * a + 4 * gq
-                                : static_cast<size_t>(gq) * P.A * sbytes + static_cast<size_t>(p) * sbytes + nb * a;
-          vb[gq][c] = p >= 0 ? *reinterpret_cast<const uint32_t *>(P.bscale + off) : 0u;
-        }
+        for (int q = 0; q < C::PIECES; ++q)
+          R.b[q][c] = p >= 0 ? ld_sf16(P.bscale + (static_cast<size_t>(q) * P.A + p) * sbytes + off, valid)
+                             : make_uint4(0u, 0u, 0u, 0u);
       }
-      tc_st4(lane_addr + kBsColSf + 16 * s, va[0][0], va[0][1], va[0][2], va[0][3]);
-      if (A4) tc_st4(lane_addr + kBsColSf + 16 * s + 4, va[1][0], va[1][1], va[1][2], va[1][3]);
-      tc_st4(lane_addr + kBsColSf + 16 * s + 8, vb[0][0], vb[0][1], vb[0][2], vb[0][3]);
-      tc_st4(lane_addr + kBsColSf + 16 * s + 12, vb[1][0], vb[1][1], vb[1][2], vb[1][3]);
+    };
+    auto words = [](const uint4 (&v)[4], uint32_t (&o)[16]) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        o[c] = v[c].x;
+        o[4 + c] = v[c].y;
+        o[8 + c] = v[c].z;
+        o[12 + c] = v[c].w;
+      }
+    };
+    auto store_chunk = [&](int ch, const SfChunk &R) -> bool {
+      const int slot = ch & 1;
+      if (!__all_sync(0xFFFFFFFFu,
+                      mb_wait_or_abort(&sf_empty[slot], (static_cast<uint32_t>(ch >> 1) & 1u) ^ 1u, abort)))
+        return false;
+      const uint32_t base = lane_addr + kBsColSf + slot * C::SF_CHUNK_COLS;
+      uint32_t o[16];
+      words(R.w, o);
+      tc_st16_nw(base, o);
+#pragma unroll
+      for (int q = 0; q < C::PIECES; ++q) {
+        words(R.b[q], o);
+        tc_st16_nw(base + 16 * (1 + q), o);
+      }
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mb_arrive(&full[s]);
+      if (lane == 0) mb_arrive(&sf_full[slot]);
+      return true;
+    };
+    SfChunk R0, R1;
+    load_chunk(0, R0);
+    if (nch > 1) load_chunk(1, R1);
+    bool ok = true;
+    for (int ch = 0; ch < nch && ok; ch += 2) {
+      ok = store_chunk(ch, R0);
+      if (ok && ch + 2 < nch) load_chunk(ch + 2, R0);
+      if (ok && ch + 1 < nch) {
+        ok = store_chunk(ch + 1, R1);
+        if (ok && ch + 3 < nch) load_chunk(ch + 3, R1);
+      }
     }
+    if (!ok) timeout = true;
   } else if (warp == kBsTmaWarp) {
     // ---------------------------------------------------- TMA
     if (lane == 0) {
@@ -942,6 +1018,13 @@ __global__ void __launch_bounds__(kBsThreads, 1)
           reinterpret_cast<const CUtensorMap *>(P.maps + static_cast<size_t>(kind * P.E + g.u) * kMapBytes);
       if (present) asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(wmap) : "memory");
       const int y0 = tile_wrow(kind, g.m0, 0, P.I), y1 = tile_wrow(kind, g.m0, kWBoxRows, P.I);
+      // K offset of stage a in the weight map: 4-bit values (W4A16 map) or bytes (W4A4 map)
+      auto wx_of = [](int a) { return A4 ? a * 128 : a * C::KS; };
+      if (present)
+        for (int a = 0; a < kBsAhead && a < nst; ++a) {
+          tma_prefetch_2d(wmap, wx_of(a), y0);
+          tma_prefetch_2d(wmap, wx_of(a), y1);
+        }
       for (int a = 0; a < nst; ++a) {
         const int s = a % C::STAGES;
         if (!mb_wait_or_abort(&empty[s], (static_cast<uint32_t>(a / C::STAGES) & 1u) ^ 1u, abort)) {
@@ -950,10 +1033,13 @@ __global__ void __launch_bounds__(kBsThreads, 1)
         }
         uint8_t *st = bsm + s * C::STAGE_B;
         mb_arrive_tx(&full[s], static_cast<uint32_t>((present ? 1 : 0) * C::WTX + C::PIECES * kBsAtomB));
-        if (present) {  // weight codes: K offset in 4-bit values (W4A16 map) or in bytes (W4A4 map)
-          const int wx = A4 ? a * 128 : a * C::KS;
-          tma_load_2d(st, wmap, wx, y0, &full[s]);
-          tma_load_2d(st + kBsAtomB / 2, wmap, wx, y1, &full[s]);
+        if (present) {
+          tma_load_2d(st, wmap, wx_of(a), y0, &full[s]);
+          tma_load_2d(st + kBsAtomB / 2, wmap, wx_of(a), y1, &full[s]);
+          if (a + kBsAhead < nst) {
+            tma_prefetch_2d(wmap, wx_of(a + kBsAhead), y0);
+            tma_prefetch_2d(wmap, wx_of(a + kBsAhead), y1);
+          }
         }
 #pragma unroll
         for (int q = 0; q < C::PIECES; ++q)
@@ -965,34 +1051,35 @@ __global__ void __launch_bounds__(kBsThreads, 1)
     if (lane == 0) {
       for (int a = 0; a < nst; ++a) {
         const int s = a % C::STAGES;
+        const int ch = a / C::CH, t = a % C::CH, slot = ch & 1;
+        if (t == 0 && !mb_wait_or_abort(&sf_full[slot], static_cast<uint32_t>(ch >> 1) & 1u, abort)) {
+          timeout = true;
+          break;
+        }
         if (!mb_wait_or_abort(&full[s], static_cast<uint32_t>(a / C::STAGES) & 1u, abort)) {
           timeout = true;
           break;
         }
         tc_fence_after();
         const uint32_t wa = su32(bsm + s * C::STAGE_B);
-        const uint32_t sf = tmem + kBsColSf + 16 * s;
+        const uint32_t sf = tmem + kBsColSf + slot * C::SF_CHUNK_COLS;
 #pragma unroll
         for (int q = 0; q < C::PIECES; ++q)
 #pragma unroll
           for (int j = 0; j < C::STEPS; ++j) {
             // both operands advance 32 bytes per step (W4A16: 32 values of the
-            // gapped 4-bit layout / 32 e4m3; W4A4: 64 dense 4-bit values)
-            uint32_t sfa, sfb;
-            int sfa_id, sfb_id;
-            if (A4) {
-              sfa = sf + 4 * (j >> 1);
-              sfb = sf + 8 + 4 * (j >> 1);
-              sfa_id = sfb_id = 2 * (j & 1);
-            } else {
-              sfa = sf;
-              sfb = sf + 8 + 4 * q;
-              sfa_id = sfb_id = j;
-            }
+            // gapped 4-bit layout / 32 e4m3; W4A4: 64 dense 4-bit values); the
+            // step's 32-value blocks start at K offset KS t + MMA_K j within the
+            // chunk: scale word (KS t + MMA_K j) / 128, byte ((KS t + MMA_K j) / 32) % 4
+            const int kofs = C::KS * t + C::MMA_K * j;
+            const uint32_t word = static_cast<uint32_t>(kofs >> 7);
+            const int id = (kofs >> 5) & 3;
             tc_mma_bs<A4>(tmem, smem_desc_sw128(wa + 32 * j), smem_desc_sw128(wa + (1 + q) * kBsAtomB + 32 * j),
-                          idesc_bs<A4>(kTileM, Npad, sfa_id, sfb_id), sfa, sfb, (a > 0 || q > 0 || j > 0) ? 1u : 0u);
+                          idesc_bs<A4>(kTileM, Npad, id, id), sf + 4 * word, sf + 16 * (1 + q) + 4 * word,
+                          (a > 0 || q > 0 || j > 0) ? 1u : 0u);
           }
         tc_commit(&empty[s]);
+        if (t == C::CH - 1 || a == nst - 1) tc_commit(&sf_empty[slot]);
       }
       tc_commit(&acc_bar);  // also after an abort: completes when every MMA issued so far has finished
     }
