@@ -306,32 +306,31 @@ def ffn_kernel_label(s, mode):
     mode = resolved_mode(s, mode)
     return {1: "k3moe_expert_ffn, GEMV mode (gemv_prep + gemv_rows gate/up + gemv_h16 + gemv_rows down)",
             2: "k3moe_expert_ffn, STREAM mode (stream_prep + ffn_stream_kernel)",
-            3: "k3moe_expert_ffn, GEMM mode (gemm_prep + gemm_sched + rows_to_pieces + ffn_gemm_bs_kernel "
-               "gate/up + rows_to_pieces + ffn_gemm_bs_kernel down; kind::mxf8f6f4, e2m1 x e4m3 hi/lo)",
-            4: "k3moe_expert_ffn, W4A4 mode (gemm_prep + gemm_sched + rows_to_pieces + ffn_gemm_bs_kernel "
-               "gate/up + rows_to_pieces + ffn_gemm_bs_kernel down; kind::mxf4)"}[mode]
+            3: "k3moe_expert_ffn, GEMM mode (gemm_prep + gemm_sched + rows_to_f16 + ffn_gemm_kernel gate/up "
+               "+ rows_to_f16 + ffn_gemm_kernel down; kind::f16 after in-kernel e2m1 dequantisation)",
+            4: "k3moe_expert_ffn, W4A4 mode (gemm_prep + gemm_sched + rows_to_mxfp4 + ffn_gemm_mxf4_kernel "
+               "gate/up + rows_to_mxfp4 + ffn_gemm_mxf4_kernel down; kind::mxf4)"}[mode]
 
 
 def tensor_figures(s, mode, ffn_s):
-    """Tensor-pipe view of a GEMM-mode expert FFN: useful FLOPs (2 A (2I H + H I)),
-    FLOPs the MMAs execute (W4A16 runs every product twice, for the hi and lo
-    activation pieces), and the dense peak of the MMA kind: the measured bf16 peak
-    times the nominal ratio (fp8/fp6/fp4 operands 2x, kind::mxf4 6x)."""
+    """Tensor-pipe view of a GEMM-mode expert FFN: FLOPs 2 A (2I H + H I) per call
+    and the dense peak of the MMA kind the mode runs: the measured bf16 peak for
+    kind::f16 (GEMM mode), times the nominal fp4/bf16 ratio 6 for kind::mxf4
+    (W4A4 mode)."""
     mode = resolved_mode(s, mode)
     if mode not in (3, 4):
         return None
     A = s.T * s.k
-    useful = 2.0 * A * 3 * s.H * s.I
-    executed = useful * (2 if mode == 3 else 1)
+    flops = 2.0 * A * 3 * s.H * s.I
     peaks = measured_peaks()
     bf16 = float(peaks["bf16_tflops"]) if peaks and "bf16_tflops" in peaks else 1900.0
-    ratio = 2.0 if mode == 3 else 6.0
-    peak = bf16 * ratio
-    tf = executed / ffn_s / 1e12
-    return {"kind": "mxf8f6f4 (e2m1 x e4m3, 2 pieces)" if mode == 3 else "mxf4 (e2m1 x e2m1)",
-            "useful_tflops": useful / ffn_s / 1e12, "executed_tflops": tf, "peak_tflops": peak,
-            "peak_source": ("measured bf16 x %g" % ratio) if peaks else ("fallback bf16 x %g" % ratio),
-            "frac": tf / peak, "fp4_dense_frac": useful / ffn_s / 1e12 / (bf16 * 6.0)}
+    ratio = 1.0 if mode == 3 else 6.0
+    tf = flops / ffn_s / 1e12
+    src = "measured" if peaks else "fallback"
+    return {"kind": "f16 (bf16 x bf16 after dequantisation)" if mode == 3 else "mxf4 (e2m1 x e2m1)",
+            "tflops": tf, "peak_tflops": bf16 * ratio,
+            "peak_source": f"{src} bf16" + ("" if mode == 3 else " x 6 (nominal fp4/bf16)"),
+            "frac": tf / (bf16 * ratio), "fp4_dense_frac": tf / (bf16 * 6.0)}
 
 
 def workload_config(a, s):

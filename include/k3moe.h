@@ -107,6 +107,10 @@ typedef struct {
 #define K3MOE_FFN_W4A4 4   /* the GEMM mode with MXFP4 activations: x and h are quantised to
                               MXFP4 per 32-block (k3moe_quantize_mxfp4's rule) before the
                               products, which are then exact; same shape rules as GEMM.
+                              With H and I multiples of 256 the products run on the
+                              block-scaled FP4 tensor core (tcgen05 kind::mxf4: codes
+                              and E8M0 scales of both operands as stored), else on the
+                              GEMM mode's kernel after exact dequantisation.
                               Never chosen by AUTO.                                     */
 
 /* Workspace queries (bytes; 0 when the call needs none).  op is one of: */

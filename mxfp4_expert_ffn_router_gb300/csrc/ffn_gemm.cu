@@ -252,8 +252,8 @@ __host__ __device__ inline GemmWs gemm_ws(int T, int H, int I, int E, int k) {
   w.hrow = o;    o = g256(o + sizeof(uint16_t) * A * I);  // h, bf16 (the rounding point)
   w.h16 = o;     o = g256(o + sizeof(uint16_t) * A * I);  // h prescaled to f16
   w.hexp = o;    o = g256(o + sizeof(int32_t) * (A ? A : 1));
-  w.xsc = o;     o = g256(o + 2 * A * (static_cast<size_t>(H) / 32));  // block scales of the x pieces (two per 32-block)
-  w.hsc = o;     o = g256(o + 2 * A * (static_cast<size_t>(I) / 32));  // block scales of the h pieces
+  w.xsc = o;     o = g256(o + A * (static_cast<size_t>(H) / 32));  // MXFP4 block scales of x (W4A4)
+  w.hsc = o;     o = g256(o + A * (static_cast<size_t>(I) / 32));  // MXFP4 block scales of h (W4A4)
   w.total = o;
   return w;
 }
@@ -311,9 +311,8 @@ __global__ void __launch_bounds__(32)
 // Tensor maps of the active experts' weight codes: maps[u] (w13) and
 // maps[E + u] (w2) for active slot u, each the host-encoded template with its
 // global address replaced by the expert's code pointer.  Experts whose code
-// pointers are NULL or not aligned to align_mask + 1 bytes (16, or 32 for the
-// gapped 4-bit maps) keep the template's address; the GEMM treats them as absent
-// and never loads through their map.
+// pointers are NULL or not 16-byte aligned keep the template's address; the
+// GEMMs treat them as absent and never load through their map.
 //
 // The same launch writes the tile tables of both GEMMs: entry t of a table is
 // {active slot, expert, first bucket position, (tokens << 16) | row tile} of
@@ -330,8 +329,7 @@ __global__ void __launch_bounds__(128)
                       k3moe_weights w, const int32_t *__restrict__ active, const int32_t *__restrict__ meta, int E,
                       const int32_t *__restrict__ slot_p0, const int32_t *__restrict__ slot_cnt,
                       const int32_t *__restrict__ pref_gu, const int32_t *__restrict__ pref_dn, int mt_gu, int mt_dn,
-                      int4 *__restrict__ tab_gu, int4 *__restrict__ tab_dn, uint8_t *__restrict__ maps,
-                      unsigned align_mask) {
+                      int4 *__restrict__ tab_gu, int4 *__restrict__ tab_dn, uint8_t *__restrict__ maps) {
   pdl_wait();
   pdl_trigger();
   const int na = meta[0];
@@ -347,7 +345,7 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
   for (int i = 0; i < kMapBytes / 16; ++i) d4[i] = tmpl[i];
   const uint8_t *codes = which ? w.w2_codes[e] : w.w13_codes[e];
-  if (codes && (reinterpret_cast<uintptr_t>(codes) & align_mask) == 0)
+  if (codes && (reinterpret_cast<uintptr_t>(codes) & 15u) == 0)
     asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;" ::"l"(dst), "l"(codes)
                  : "memory");
   asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
@@ -724,89 +722,57 @@ __global__ void __launch_bounds__(kThreadsG, 1)
 
 
 // ============================================================================
-// Block-scaled grouped GEMM: tcgen05.mma with the E8M0 block scales of both
-// operands in tensor memory, so the weight codes go from TMA to the tensor core
-// as they are stored (e2m1, two per byte, low nibble = even column).
-//  * W4A16 (kind::mxf8f6f4, scale_vec::1X, K = 32 per MMA): each bf16 activation
-//    is split into two e4m3 pieces hi + lo with one E8M0 scale per 32-block and
-//    piece (a pre-pass); hi keeps the top 4 significant bits of each value and lo
-//    the rest (a bf16 value has 8), so the pair is exact for every value within
-//    2^11 of its block's largest (smaller values keep at least the hi piece).
-//    This kind reads 4-bit operands as 16 values per 16-byte unit (8 bytes of
-//    codes, 8 bytes of gap): the weight maps use the TMA type that lays packed
-//    4-bit rows out that way (16U4_ALIGN16B), one box = 128 K values x 64 rows.
-//  * W4A4 (kind::mxf4, scale_vec::2X, K = 64 per MMA): activations are the MXFP4
-//    codes and scales of the quantiser rule, both operands dense (two per byte);
-//    products are then exact.
+// W4A4 grouped GEMM on the block-scaled tensor core: tcgen05.mma kind::mxf4
+// (scale_vec::2X, K = 64 per MMA) with the E8M0 block scales of both operands in
+// tensor memory.  The weight codes go from TMA to the tensor core as they are
+// stored (e2m1, two per byte, low nibble = even column) and the activations are
+// the MXFP4 codes and scales of the quantiser rule (a pre-pass), so every product
+// is exact and only the fp32 accumulation rounds.
 // Tensor-memory layout of the scale factors (M = 128): the scale bytes of tile
 // row r (or token column n) sit in lane r % 32 of every lane quadrant, column
 // base + r / 32; a 32-bit cell holds the scales of 4 consecutive K blocks and the
-// instruction descriptor's scale-factor id picks the byte.
-// Warps: 0-3 write the scale factors of every stage (tcgen05.st) and run the
-// epilogue; 4 issues the TMA loads (weight codes through the expert's tensor map,
-// activation pieces); 5 owns tensor memory and issues the MMAs.  One ring of
-// stages, each holding the weight codes and the activation pieces of one K range.
+// instruction descriptor's scale-factor id picks the byte pair of a K-64 step.
+// Warps: 0-3 write the scale factors (tcgen05.st) and run the epilogue; 4 issues
+// the TMA loads (weight codes through the expert's tensor map, activation codes);
+// 5 owns tensor memory and issues the MMAs.  One ring of stages of 256 K values.
 namespace {
 
-constexpr int kBsSfWarps = 4;
-constexpr int kBsTmaWarp = 4;
-constexpr int kBsMmaWarp = 5;
-constexpr int kBsThreads = 6 * 32;
-constexpr int kBsAtomB = kTileN * 128;   // one 128-row x 128-byte swizzled tile (16 KiB)
-constexpr int kBsColSf = kTileN;         // tensor-memory columns: accumulator [0, 128), then 16 per stage
-constexpr int kBsAhead = 8;              // weight-code stages prefetched into L2 ahead of the ring
+constexpr int kMxSfWarps = 4;
+constexpr int kMxTmaWarp = 4;
+constexpr int kMxMmaWarp = 5;
+constexpr int kMxThreads = 6 * 32;
+constexpr int kMxAtomB = kTileN * 128;  // one 128-row x 128-byte swizzled tile (16 KiB)
+constexpr int kMxColSf = kTileN;        // tensor-memory columns: accumulator [0, 128), then the scale slots
+constexpr int kMxAhead = 8;             // weight-code stages prefetched into L2 ahead of the ring
+constexpr int kMxKS = 256;              // K values per stage: one 128-byte row of codes per operand
+constexpr int kMxSteps = kMxKS / 64;    // MMAs per stage
+constexpr int kMxStages = 3;
+constexpr int kMxStageB = 2 * kMxAtomB;  // weight tile + activation tile
+constexpr int kMxSmem = kMxStages * kMxStageB;
+constexpr int kMxDynSmem = 1024 + (kMxSmem > kEpiBytes ? kMxSmem : kEpiBytes);
+// Scale factors travel in chunks of 16 bytes per row (512 K values, 2 stages).  A
+// chunk takes 16 tensor-memory columns per operand: 4 words of 4 block scales x
+// 4 row groups of 32.  Two chunk slots follow the accumulator.
+constexpr int kMxCh = 512 / kMxKS;
+constexpr int kMxSfChunkCols = 32;
+static_assert(kMxColSf + 2 * kMxSfChunkCols <= kTmemCols, "tensor-memory budget");
 
-template <bool A4>
-struct BsCfg {
-  static constexpr int KS = A4 ? 256 : 128;      // K per stage (one 128-byte row of codes per operand piece)
-  static constexpr int PIECES = A4 ? 1 : 2;      // activation pieces
-  static constexpr int MMA_K = A4 ? 64 : 32;
-  static constexpr int STEPS = KS / MMA_K;       // MMA K steps per stage and piece (4)
-  static constexpr int STAGES = A4 ? 3 : 2;
-  static constexpr int STAGE_B = (1 + PIECES) * kBsAtomB;  // weight tile + activation pieces
-  // transaction bytes of the weight tile: the gapped 4-bit layout fills 16 KiB of
-  // shared memory from 8 KiB of packed codes and the barrier counts the latter
-  static constexpr int WTX = A4 ? kBsAtomB : kBsAtomB / 2;
-  static constexpr int SMEM = STAGES * STAGE_B;
-  static constexpr int DYN_SMEM = 1024 + (SMEM > kEpiBytes ? SMEM : kEpiBytes);
-  // Scale factors travel in chunks of 16 bytes per row (512 K values): CH stages.
-  // A chunk takes 16 tensor-memory columns per operand (weights, then each
-  // activation piece): 4 words of 4 block scales x 4 row groups of 32.
-  static constexpr int CH = 512 / KS;
-  static constexpr int SF_CHUNK_COLS = 16 * (1 + PIECES);
-};
-// two chunk slots of scale factors after the accumulator
-static_assert(kBsColSf + 2 * BsCfg<true>::SF_CHUNK_COLS <= kTmemCols, "tensor-memory budget (W4A4)");
-static_assert(kBsColSf + 2 * BsCfg<false>::SF_CHUNK_COLS <= kTmemCols, "tensor-memory budget (W4A16)");
-
-// Instruction descriptor of the block-scaled kinds: B scale-factor id [4,6), A
-// format [7,10), B format [10,13), N/8 [17,23), E8M0 scales (bit 23), M/16
-// [24,29), A scale-factor id [29,31).  Formats: E2M1 = 5 and E4M3 = 0 for
-// kind::mxf8f6f4, E2M1 = 1 for kind::mxf4.
-template <bool A4>
-__device__ __forceinline__ uint32_t idesc_bs(int M, int N, int sfa_id, int sfb_id) {
-  const uint32_t af = A4 ? 1u : 5u, bf = A4 ? 1u : 0u;
-  return (static_cast<uint32_t>(sfb_id) << 4) | (af << 7) | (bf << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
-         (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) | (static_cast<uint32_t>(sfa_id) << 29);
+// Instruction descriptor of kind::mxf4: B scale-factor id [4,6), A and B formats
+// [7,10) and [10,13) (E2M1 = 1), N/8 [17,23), E8M0 scales (bit 23), M/16 [24,29),
+// A scale-factor id [29,31).
+__device__ __forceinline__ uint32_t idesc_mxf4(int M, int N, int sf_id) {
+  return (static_cast<uint32_t>(sf_id) << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) | (static_cast<uint32_t>(sf_id) << 29);
 }
 
-template <bool A4>
-__device__ __forceinline__ void tc_mma_bs(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                          uint32_t tmem_sfa, uint32_t tmem_sfb, uint32_t accumulate) {
-  if (A4)
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
-            tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(tmem_sfa), "r"(tmem_sfb), "r"(accumulate)
-        : "memory");
-  else
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
-            tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(tmem_sfa), "r"(tmem_sfb), "r"(accumulate)
-        : "memory");
+__device__ __forceinline__ void tc_mma_mxf4(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t tmem_sfa, uint32_t tmem_sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(tmem_sfa), "r"(tmem_sfb), "r"(accumulate)
+      : "memory");
 }
 
 // 32 lanes x 32 bit, 16 consecutive columns per thread, registers -> tensor
@@ -842,10 +808,10 @@ __device__ __forceinline__ uint4 ld_sf16(const uint8_t *p, int valid) {
 }
 
 // One chunk of scale words for the 128 rows / token columns a lane covers
-// (lane + 32 c): weights, then the activation pieces.
+// (lane + 32 c): weights, then activations.
 struct SfChunk {
   uint4 w[4];
-  uint4 b[2][4];
+  uint4 b[4];
 };
 
 // Bounded wait that also gives up as soon as another role has given up (`abort`
@@ -862,26 +828,24 @@ __device__ __forceinline__ bool mb_wait_or_abort(uint64_t *b, uint32_t parity, v
 
 }  // namespace
 
-struct BsParams {
+struct Mx4Params {
   k3moe_weights w;
   int H, I, A, E;
   const int32_t *meta;
   const int4 *tab;         // tile table of this GEMM
   const uint8_t *maps;     // weight-code tensor maps per active slot (w13 at u, w2 at E + u)
-  const uint8_t *bscale;   // activation block scales: piece q of bucket row p at q*A*(K/32) + p*(K/32)
+  const uint8_t *ascale;   // activation block scales [A][K/32]
   uint16_t *hrow;          // [A][I] bf16 (gate/up output)
   float *Y;                // [A][H]
   int kind;                // 0 gate/up, 1 down
   int32_t *status;
 };
 
-template <bool A4>
-__global__ void __launch_bounds__(kBsThreads, 2)
-    ffn_gemm_bs_kernel(const __grid_constant__ CUtensorMap amap, BsParams P) {
-  using C = BsCfg<A4>;
-  extern __shared__ __align__(1024) uint8_t bsm_raw[];
-  uint8_t *bsm = bsm_raw + ((1024u - (su32(bsm_raw) & 1023u)) & 1023u);
-  __shared__ uint64_t full[C::STAGES], empty[C::STAGES], sf_full[2], sf_empty[2], acc_bar;
+__global__ void __launch_bounds__(kMxThreads, 2)
+    ffn_gemm_mxf4_kernel(const __grid_constant__ CUtensorMap amap, Mx4Params P) {
+  extern __shared__ __align__(1024) uint8_t msm_raw[];
+  uint8_t *msm = msm_raw + ((1024u - (su32(msm_raw) & 1023u)) & 1023u);
+  __shared__ uint64_t full[kMxStages], empty[kMxStages], sf_full[2], sf_empty[2], acc_bar;
   __shared__ uint32_t tmem_holder;
   __shared__ int s_abort;
   volatile int *abort = &s_abort;
@@ -900,21 +864,20 @@ __global__ void __launch_bounds__(kBsThreads, 2)
     g.m0 = (te.w & 0xFFFF) * kTileM;
   }
   const int K = kind == 0 ? P.H : P.I;
-  const int nst = K / C::KS;  // stages (K is a multiple of 256)
+  const int nst = K / kMxKS;  // stages (K is a multiple of 256)
   const int Npad = (g.n + 15) & ~15;
   const uint8_t *c13 = P.w.w13_codes[g.e], *s13 = P.w.w13_scales[g.e];
   const uint8_t *c2 = P.w.w2_codes[g.e], *s2 = P.w.w2_scales[g.e];
   const uintptr_t al = reinterpret_cast<uintptr_t>(c13) | reinterpret_cast<uintptr_t>(c2);
-  // the gapped 4-bit maps (W4A16) want 32-byte bases, the dense ones 16
-  const bool present = c13 && s13 && c2 && s2 && (al & (A4 ? 15u : 31u)) == 0;
+  const bool present = c13 && s13 && c2 && s2 && (al & 15u) == 0;
   const uint8_t *wscales = kind == 0 ? s13 : s2;
   if (tid == 0) {
-    for (int s = 0; s < C::STAGES; ++s) {
+    for (int s = 0; s < kMxStages; ++s) {
       mb_init(&full[s], 1);  // TMA bytes
       mb_init(&empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
-      mb_init(&sf_full[s], kBsSfWarps);  // one arrival per scale-factor warp
+      mb_init(&sf_full[s], kMxSfWarps);  // one arrival per scale-factor warp
       mb_init(&sf_empty[s], 1);
     }
     mb_init(&acc_bar, 1);
@@ -922,7 +885,7 @@ __global__ void __launch_bounds__(kBsThreads, 2)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     if (!present && c13 && s13 && c2 && s2 && blockIdx.x == 0) set_status(P.status, K3MOE_DEV_BOUNDS);
   }
-  if (warp == kBsMmaWarp) {
+  if (warp == kMxMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&tmem_holder)),
                  "r"(kTmemCols)
                  : "memory");
@@ -934,23 +897,23 @@ __global__ void __launch_bounds__(kBsThreads, 2)
   const uint32_t tmem = tmem_holder;
   bool timeout = false;
 
-  if (warp < kBsSfWarps) {
+  if (warp < kMxSfWarps) {
     // ---------------------------------------------------- scale factors
     // Lane l of every warp writes rows / token columns l, l+32, l+64, l+96 into
     // its own lane quadrant (the same data in all four).  Chunk ch (stages
-    // [CH ch, CH ch + CH)) goes to slot ch & 1: weights at columns +0..15, piece
-    // q at +16 (q+1); column 4 w + c holds scale word w of row group c.  Loads run
-    // two chunks ahead of the stores in two register sets.
+    // [2 ch, 2 ch + 2)) goes to slot ch & 1: weights at columns +0..15,
+    // activations at +16..31; column 4 w + c holds scale word w of row group c.
+    // Loads run two chunks ahead of the stores in two register sets.
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * warp) << 16);
     const int sbytes = K / 32;
-    const int nch = (nst + C::CH - 1) / C::CH;
+    const int nch = (nst + kMxCh - 1) / kMxCh;
     const uint8_t *srow[4];
-    int tokrow[4];
+    const uint8_t *arow[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const int r = lane + 32 * c;
       srow[c] = present ? wscales + static_cast<size_t>(tile_wrow(kind, g.m0, r, P.I)) * sbytes : nullptr;
-      tokrow[c] = r < g.n ? g.p0 + r : -1;
+      arow[c] = r < g.n ? P.ascale + static_cast<size_t>(g.p0 + r) * sbytes : nullptr;
       if (srow[c]) {  // the tile's weight-scale rows are read once, 16 bytes per chunk: pull them into L2 now
         for (int off = 0; off < sbytes; off += 128) prefetch_l2(srow[c] + off);
         prefetch_l2(srow[c] + sbytes - 1);
@@ -962,11 +925,7 @@ __global__ void __launch_bounds__(kBsThreads, 2)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         R.w[c] = srow[c] ? ld_sf16(srow[c] + off, valid) : make_uint4(0u, 0u, 0u, 0u);
-        const int p = tokrow[c];
-#pragma unroll
-        for (int q = 0; q < C::PIECES; ++q)
-          R.b[q][c] = p >= 0 ? ld_sf16(P.bscale + (static_cast<size_t>(q) * P.A + p) * sbytes + off, valid)
-                             : make_uint4(0u, 0u, 0u, 0u);
+        R.b[c] = arow[c] ? ld_sf16(arow[c] + off, valid) : make_uint4(0u, 0u, 0u, 0u);
       }
     };
     auto words = [](const uint4 (&v)[4], uint32_t (&o)[16]) {
@@ -983,15 +942,12 @@ __global__ void __launch_bounds__(kBsThreads, 2)
       if (!__all_sync(0xFFFFFFFFu,
                       mb_wait_or_abort(&sf_empty[slot], (static_cast<uint32_t>(ch >> 1) & 1u) ^ 1u, abort)))
         return false;
-      const uint32_t base = lane_addr + kBsColSf + slot * C::SF_CHUNK_COLS;
+      const uint32_t base = lane_addr + kMxColSf + slot * kMxSfChunkCols;
       uint32_t o[16];
       words(R.w, o);
       tc_st16_nw(base, o);
-#pragma unroll
-      for (int q = 0; q < C::PIECES; ++q) {
-        words(R.b[q], o);
-        tc_st16_nw(base + 16 * (1 + q), o);
-      }
+      words(R.b, o);
+      tc_st16_nw(base + 16, o);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
       __syncwarp();
@@ -1011,88 +967,79 @@ __global__ void __launch_bounds__(kBsThreads, 2)
       }
     }
     if (!ok) timeout = true;
-  } else if (warp == kBsTmaWarp) {
+  } else if (warp == kMxTmaWarp) {
     // ---------------------------------------------------- TMA
     if (lane == 0) {
       const CUtensorMap *wmap =
           reinterpret_cast<const CUtensorMap *>(P.maps + static_cast<size_t>(kind * P.E + g.u) * kMapBytes);
       if (present) asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(wmap) : "memory");
       const int y0 = tile_wrow(kind, g.m0, 0, P.I), y1 = tile_wrow(kind, g.m0, kWBoxRows, P.I);
-      // K offset of stage a in the weight map: 4-bit values (W4A16 map) or bytes (W4A4 map)
-      auto wx_of = [](int a) { return A4 ? a * 128 : a * C::KS; };
       if (present)
-        for (int a = 0; a < kBsAhead && a < nst; ++a) {
-          tma_prefetch_2d(wmap, wx_of(a), y0);
-          tma_prefetch_2d(wmap, wx_of(a), y1);
+        for (int a = 0; a < kMxAhead && a < nst; ++a) {
+          tma_prefetch_2d(wmap, a * 128, y0);
+          tma_prefetch_2d(wmap, a * 128, y1);
         }
       for (int a = 0; a < nst; ++a) {
-        const int s = a % C::STAGES;
-        if (!mb_wait_or_abort(&empty[s], (static_cast<uint32_t>(a / C::STAGES) & 1u) ^ 1u, abort)) {
+        const int s = a % kMxStages;
+        if (!mb_wait_or_abort(&empty[s], (static_cast<uint32_t>(a / kMxStages) & 1u) ^ 1u, abort)) {
           timeout = true;
           break;
         }
-        uint8_t *st = bsm + s * C::STAGE_B;
-        mb_arrive_tx(&full[s], static_cast<uint32_t>((present ? 1 : 0) * C::WTX + C::PIECES * kBsAtomB));
-        if (present) {
-          tma_load_2d(st, wmap, wx_of(a), y0, &full[s]);
-          tma_load_2d(st + kBsAtomB / 2, wmap, wx_of(a), y1, &full[s]);
-          if (a + kBsAhead < nst) {
-            tma_prefetch_2d(wmap, wx_of(a + kBsAhead), y0);
-            tma_prefetch_2d(wmap, wx_of(a + kBsAhead), y1);
+        uint8_t *st = msm + s * kMxStageB;
+        mb_arrive_tx(&full[s], static_cast<uint32_t>((present ? 2 : 1) * kMxAtomB));
+        if (present) {  // weight codes: K offset in bytes (128 per stage), two boxes of 64 rows
+          tma_load_2d(st, wmap, a * 128, y0, &full[s]);
+          tma_load_2d(st + kMxAtomB / 2, wmap, a * 128, y1, &full[s]);
+          if (a + kMxAhead < nst) {
+            tma_prefetch_2d(wmap, (a + kMxAhead) * 128, y0);
+            tma_prefetch_2d(wmap, (a + kMxAhead) * 128, y1);
           }
         }
-#pragma unroll
-        for (int q = 0; q < C::PIECES; ++q)
-          tma_load_2d(st + (1 + q) * kBsAtomB, &amap, a * 128, q * P.A + g.p0, &full[s]);
+        tma_load_2d(st + kMxAtomB, &amap, a * 128, g.p0, &full[s]);
       }
     }
   } else {
     // ---------------------------------------------------- MMA issue
     if (lane == 0) {
       for (int a = 0; a < nst; ++a) {
-        const int s = a % C::STAGES;
-        const int ch = a / C::CH, t = a % C::CH, slot = ch & 1;
+        const int s = a % kMxStages;
+        const int ch = a / kMxCh, t = a % kMxCh, slot = ch & 1;
         if (t == 0 && !mb_wait_or_abort(&sf_full[slot], static_cast<uint32_t>(ch >> 1) & 1u, abort)) {
           timeout = true;
           break;
         }
-        if (!mb_wait_or_abort(&full[s], static_cast<uint32_t>(a / C::STAGES) & 1u, abort)) {
+        if (!mb_wait_or_abort(&full[s], static_cast<uint32_t>(a / kMxStages) & 1u, abort)) {
           timeout = true;
           break;
         }
         tc_fence_after();
-        const uint32_t wa = su32(bsm + s * C::STAGE_B);
-        const uint32_t sf = tmem + kBsColSf + slot * C::SF_CHUNK_COLS;
+        const uint32_t wa = su32(msm + s * kMxStageB);
+        const uint32_t sf = tmem + kMxColSf + slot * kMxSfChunkCols;
 #pragma unroll
-        for (int q = 0; q < C::PIECES; ++q)
-#pragma unroll
-          for (int j = 0; j < C::STEPS; ++j) {
-            // both operands advance 32 bytes per step (W4A16: 32 values of the
-            // gapped 4-bit layout / 32 e4m3; W4A4: 64 dense 4-bit values); the
-            // step's 32-value blocks start at K offset KS t + MMA_K j within the
-            // chunk: scale word (KS t + MMA_K j) / 128, byte ((KS t + MMA_K j) / 32) % 4
-            const int kofs = C::KS * t + C::MMA_K * j;
-            const uint32_t word = static_cast<uint32_t>(kofs >> 7);
-            const int id = (kofs >> 5) & 3;
-            tc_mma_bs<A4>(tmem, smem_desc_sw128(wa + 32 * j), smem_desc_sw128(wa + (1 + q) * kBsAtomB + 32 * j),
-                          idesc_bs<A4>(kTileM, Npad, id, id), sf + 4 * word, sf + 16 * (1 + q) + 4 * word,
-                          (a > 0 || q > 0 || j > 0) ? 1u : 0u);
-          }
+        for (int j = 0; j < kMxSteps; ++j) {
+          // both operands advance 32 bytes (64 values) per step; the step's two
+          // 32-value blocks are blocks 8 t + 2 j, 8 t + 2 j + 1 of the chunk:
+          // scale word 2 t + j / 2, byte pair 2 (j % 2)
+          const uint32_t word = static_cast<uint32_t>(2 * t + (j >> 1));
+          tc_mma_mxf4(tmem, smem_desc_sw128(wa + 32 * j), smem_desc_sw128(wa + kMxAtomB + 32 * j),
+                      idesc_mxf4(kTileM, Npad, 2 * (j & 1)), sf + 4 * word, sf + 16 + 4 * word,
+                      (a > 0 || j > 0) ? 1u : 0u);
+        }
         tc_commit(&empty[s]);
-        if (t == C::CH - 1 || a == nst - 1) tc_commit(&sf_empty[slot]);
+        if (t == kMxCh - 1 || a == nst - 1) tc_commit(&sf_empty[slot]);
       }
       tc_commit(&acc_bar);  // also after an abort: completes when every MMA issued so far has finished
     }
   }
 
   // ---- epilogue (scale-factor warps): lane quadrant = warp, all Npad columns
-  if (warp < kBsSfWarps) {
+  if (warp < kMxSfWarps) {
     if (!mb_wait(&acc_bar, 0)) {
       timeout = true;
       *abort = 1;
     }
     tc_fence_after();
-    float *stage = reinterpret_cast<float *>(bsm);  // [kTileN][kTileM + 1]
+    float *stage = reinterpret_cast<float *>(msm);  // [kTileN][kTileM + 1]
     const int row = 32 * warp + lane;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * warp) << 16);
     for (int c0 = 0; c0 < Npad; c0 += 16) {
@@ -1102,11 +1049,11 @@ __global__ void __launch_bounds__(kBsThreads, 2)
       for (int j = 0; j < 16; ++j) stage[(c0 + j) * (kTileM + 1) + row] = v[j];
     }
     tc_fence_before();
-    asm volatile("bar.sync 1, %0;" ::"r"(kBsSfWarps * 32) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"r"(kMxSfWarps * 32) : "memory");
     if (kind == 0) {
       // h[p0 + n][m0/2 + i] = bf16(silu(g) * u), g = tile row i, u = tile row 64 + i
       const int ncols = kTileM / 2;
-      for (int idx = tid; idx < g.n * ncols; idx += kBsSfWarps * 32) {
+      for (int idx = tid; idx < g.n * ncols; idx += kMxSfWarps * 32) {
         const int n = idx / ncols, i = idx % ncols;
         float hv = 0.f;
         if (present) {
@@ -1117,7 +1064,7 @@ __global__ void __launch_bounds__(kBsThreads, 2)
         P.hrow[static_cast<size_t>(g.p0 + n) * P.I + (g.m0 >> 1) + i] = f32_to_bf16_rne(hv);
       }
     } else {
-      for (int idx = tid; idx < g.n * kTileM; idx += kBsSfWarps * 32) {
+      for (int idx = tid; idx < g.n * kTileM; idx += kMxSfWarps * 32) {
         const int n = idx / kTileM, r = idx % kTileM;
         P.Y[static_cast<size_t>(g.p0 + n) * P.H + g.m0 + r] = present ? stage[n * (kTileM + 1) + r] : 0.f;
       }
@@ -1132,25 +1079,19 @@ __global__ void __launch_bounds__(kBsThreads, 2)
     for (int i = 0; i < 2000; ++i) __nanosleep(1000);
     __syncthreads();
   }
-  if (warp == kBsMmaWarp) {
+  if (warp == kMxMmaWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
 }
 
-// Activation pieces for the block-scaled GEMM, one block of 256 threads per bucket
-// row p (source row x[perm[p] / k] for gate/up, h[p] for down; 4 lanes per
-// 32-block, 8 values each).  W4A16: e4m3 pieces hi (rows [0, A)) and lo (rows
-// [A, 2A)) of `pieces` [2A][K] with scales [2][A][K/32]: per block, e_hi =
-// floor(log2 amax) - 7 (so amax / 2^e_hi is in [128, 256), inside e4m3), hi =
-// e4m3(v / 2^e_hi), r = v - hi * 2^e_hi (exact), e_lo from max |r| the same way,
-// lo = e4m3(r / 2^e_lo).  W4A4: MXFP4 codes [A][K/2] and scales [A][K/32] by the
-// quantiser rule.
-template <bool A4>
+// MXFP4 activations for the W4A4 GEMM, one block of 256 threads per bucket row p
+// (source row x[perm[p] / k] for gate/up, h[p] for down; 4 lanes per 32-block, 8
+// values each): codes [A][K/2] (two per byte, low nibble = even column) and
+// scales [A][K/32] by the quantiser rule.
 __global__ void __launch_bounds__(256)
-    gemm_rows_to_pieces_kernel(const uint16_t *__restrict__ src, const int32_t *__restrict__ perm, int k, int A,
-                               int K, uint8_t *__restrict__ pieces, uint8_t *__restrict__ scales,
-                               int32_t *status) {
+    gemm_rows_to_mxfp4_kernel(const uint16_t *__restrict__ src, const int32_t *__restrict__ perm, int k, int A,
+                              int K, uint8_t *__restrict__ codes, uint8_t *__restrict__ scales, int32_t *status) {
   pdl_wait();
   pdl_trigger();
   const int p = blockIdx.x;
@@ -1179,66 +1120,14 @@ __global__ void __launch_bounds__(256)
     for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
     amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-    if (A4) {
-      const int e = mx_shared_exp(amax);
-      const float inv_x = mx_pow2(-e);
-      uint32_t code = 0;
+    const int e = mx_shared_exp(amax);
+    const float inv_x = mx_pow2(-e);
+    uint32_t code = 0;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) code |= mx_code(v[i], inv_x) << (4 * i);
-      if (ok) {
-        *reinterpret_cast<uint32_t *>(pieces + static_cast<size_t>(p) * (K / 2) + c / 2) = code;
-        if ((threadIdx.x & 3) == 0) scales[static_cast<size_t>(p) * sbytes + c / 32] = static_cast<uint8_t>(e + 127);
-      }
-    } else {
-      // hi piece
-      int ehi = -127;
-      if (amax > 0.f && amax != INFINITY) {
-        int ex;
-        frexpf(amax, &ex);  // floor(log2 amax) = ex - 1
-        ehi = max(-127, min(127, ex - 8));
-      }
-      const float inv_hi = mx_pow2(-ehi), x_hi = mx_pow2(ehi);
-      uint32_t hw[2], lw[2];
-      float r[8];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        uint16_t pk;
-        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pk) : "f"(v[2 * m + 1] * inv_hi), "f"(v[2 * m] * inv_hi));
-        uint32_t hh;
-        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hh) : "h"(pk));
-        const __half2 h2 = *reinterpret_cast<const __half2 *>(&hh);
-        r[2 * m] = v[2 * m] - __low2float(h2) * x_hi;
-        r[2 * m + 1] = v[2 * m + 1] - __high2float(h2) * x_hi;
-        if (m & 1) hw[m >> 1] |= static_cast<uint32_t>(pk) << 16;
-        else hw[m >> 1] = pk;
-      }
-      float rmax = 0.f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) rmax = fmaxf(rmax, fabsf(r[i]));
-      rmax = fmaxf(rmax, __shfl_xor_sync(0xFFFFFFFFu, rmax, 1));
-      rmax = fmaxf(rmax, __shfl_xor_sync(0xFFFFFFFFu, rmax, 2));
-      int elo = -127;
-      if (rmax > 0.f && rmax != INFINITY) {
-        int ex;
-        frexpf(rmax, &ex);
-        elo = max(-127, min(127, ex - 8));
-      }
-      const float inv_lo = mx_pow2(-elo);
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        uint16_t pk;
-        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pk) : "f"(r[2 * m + 1] * inv_lo), "f"(r[2 * m] * inv_lo));
-        if (m & 1) lw[m >> 1] |= static_cast<uint32_t>(pk) << 16;
-        else lw[m >> 1] = pk;
-      }
-      if (ok) {
-        *reinterpret_cast<uint2 *>(pieces + static_cast<size_t>(p) * K + c) = make_uint2(hw[0], hw[1]);
-        *reinterpret_cast<uint2 *>(pieces + static_cast<size_t>(A + p) * K + c) = make_uint2(lw[0], lw[1]);
-        if ((threadIdx.x & 3) == 0) {
-          scales[static_cast<size_t>(p) * sbytes + c / 32] = static_cast<uint8_t>(ehi + 127);
-          scales[static_cast<size_t>(A + p) * sbytes + c / 32] = static_cast<uint8_t>(elo + 127);
-        }
-      }
+    for (int i = 0; i < 8; ++i) code |= mx_code(v[i], inv_x) << (4 * i);
+    if (ok) {
+      *reinterpret_cast<uint32_t *>(codes + static_cast<size_t>(p) * (K / 2) + c / 2) = code;
+      if ((threadIdx.x & 3) == 0) scales[static_cast<size_t>(p) * sbytes + c / 32] = static_cast<uint8_t>(e + 127);
     }
   }
 }
@@ -1294,22 +1183,6 @@ bool make_code_map(CUtensorMap *m, void *base, int rows, int kbytes) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D map over the weight codes of one expert as 4-bit values (rows x K) laid out
-// in shared memory with 8-byte gaps after every 8 bytes of codes (the layout
-// kind::mxf8f6f4 reads 4-bit operands in): box = 128 values (128 bytes in shared
-// memory) x 64 rows, 128B swizzle.  Bases and row strides must be 32-byte aligned.
-bool make_code_map_gapped(CUtensorMap *m, void *base, int rows, int K) {
-  EncodeTiledFn fn = encode_tiled();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) / 2};
-  const cuuint32_t box[2] = {128, kWBoxRows};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, base, dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // 2-D map over activation bytes (rows x row_bytes): box = 128 bytes x 128 rows,
 // 128B swizzle; rows past the end read as zero.
 bool make_byte_map(CUtensorMap *m, void *base, int rows, int row_bytes) {
@@ -1324,40 +1197,36 @@ bool make_byte_map(CUtensorMap *m, void *base, int rows, int row_bytes) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The block-scaled GEMM (both projections): pieces pre-pass -> gate/up -> pieces
-// of h -> down.
-template <bool A4>
-int launch_gemm_bs(const k3moe_shape &s, const uint16_t *x, const int32_t *perm, int A, long long ntile_max,
-                   int mt_gu, int mt_dn, BsParams P, const int4 *tab_dn, uint8_t *xp, uint8_t *xsc, uint8_t *hp,
-                   uint8_t *hsc, int32_t *status, cudaStream_t st) {
-  using C = BsCfg<A4>;
+// The W4A4 GEMM (both projections): MXFP4 activations of x -> gate/up -> MXFP4
+// activations of h -> down.
+int launch_gemm_mxf4(const k3moe_shape &s, const uint16_t *x, const int32_t *perm, int A, long long ntile_max,
+                     int mt_gu, int mt_dn, Mx4Params P, const int4 *tab_dn, uint8_t *xq, uint8_t *xsc, uint8_t *hq,
+                     uint8_t *hsc, int32_t *status, cudaStream_t st) {
   CUtensorMap xmap, hmap;
-  const int prow = A4 ? A : 2 * A;  // rows of the activation byte arrays (pieces stacked)
-  if (!make_byte_map(&xmap, xp, prow, A4 ? s.H / 2 : s.H) || !make_byte_map(&hmap, hp, prow, A4 ? s.I / 2 : s.I))
-    return -1;
+  if (!make_byte_map(&xmap, xq, A, s.H / 2) || !make_byte_map(&hmap, hq, A, s.I / 2)) return -1;
   static bool attr = false;
   if (!attr) {
-    if (cudaFuncSetAttribute(ffn_gemm_bs_kernel<A4>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::DYN_SMEM) !=
+    if (cudaFuncSetAttribute(ffn_gemm_mxf4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxDynSmem) !=
         cudaSuccess)
       return -1;
     attr = true;
   }
-  if (launch_pdl(gemm_rows_to_pieces_kernel<A4>, dim3(A), dim3(256), 0, st, x, perm, s.k, A, s.H, xp, xsc,
-                 status) != cudaSuccess)
+  if (launch_pdl(gemm_rows_to_mxfp4_kernel, dim3(A), dim3(256), 0, st, x, perm, s.k, A, s.H, xq, xsc, status) !=
+      cudaSuccess)
     return -1;
   P.kind = 0;
-  P.bscale = xsc;
-  if (launch_pdl(ffn_gemm_bs_kernel<A4>, dim3(static_cast<unsigned>(ntile_max * mt_gu)), dim3(kBsThreads),
-                 C::DYN_SMEM, st, xmap, P) != cudaSuccess)
+  P.ascale = xsc;
+  if (launch_pdl(ffn_gemm_mxf4_kernel, dim3(static_cast<unsigned>(ntile_max * mt_gu)), dim3(kMxThreads), kMxDynSmem,
+                 st, xmap, P) != cudaSuccess)
     return -1;
-  if (launch_pdl(gemm_rows_to_pieces_kernel<A4>, dim3(A), dim3(256), 0, st, static_cast<const uint16_t *>(P.hrow),
-                 static_cast<const int32_t *>(nullptr), 1, A, s.I, hp, hsc, status) != cudaSuccess)
+  if (launch_pdl(gemm_rows_to_mxfp4_kernel, dim3(A), dim3(256), 0, st, static_cast<const uint16_t *>(P.hrow),
+                 static_cast<const int32_t *>(nullptr), 1, A, s.I, hq, hsc, status) != cudaSuccess)
     return -1;
   P.kind = 1;
   P.tab = tab_dn;
-  P.bscale = hsc;
-  if (launch_pdl(ffn_gemm_bs_kernel<A4>, dim3(static_cast<unsigned>(ntile_max * mt_dn)), dim3(kBsThreads),
-                 C::DYN_SMEM, st, hmap, P) != cudaSuccess)
+  P.ascale = hsc;
+  if (launch_pdl(ffn_gemm_mxf4_kernel, dim3(static_cast<unsigned>(ntile_max * mt_dn)), dim3(kMxThreads), kMxDynSmem,
+                 st, hmap, P) != cudaSuccess)
     return -1;
   return 0;
 }
@@ -1401,18 +1270,14 @@ int launch_ffn_gemm(const k3moe_shape &s, const uint16_t *x, const k3moe_weights
   // upper bound of the token tiles: sum_e ceil(n_e / 128) <= A / 128 + min(A, E)
   const long long ntile_max = A / kTileN + (A < s.E ? A : s.E);
   const long long sched_threads = std::max<long long>(2LL * s.E, ntile_max * std::max(mt_gu, mt_dn));
-  const bool bs = s.H % kWK == 0 && s.I % kWK == 0;  // the block-scaled tensor-core path
-  if (bs && !a4) {  // W4A16 on kind::mxf8f6f4 reads the weight codes through gapped 4-bit maps
-    if (!make_code_map_gapped(&t13, maps, 2 * s.I, s.H) || !make_code_map_gapped(&t2, maps, s.H, s.I)) return -1;
-  }
   if (launch_pdl(gemm_sched_kernel, dim3(static_cast<unsigned>((sched_threads + 127) / 128)), dim3(128), 0, st, t13,
                  t2, w, static_cast<const int32_t *>(active), static_cast<const int32_t *>(meta), s.E,
                  static_cast<const int32_t *>(sp0), static_cast<const int32_t *>(scnt),
                  static_cast<const int32_t *>(pgu), static_cast<const int32_t *>(pdn), mt_gu, mt_dn, tab_gu, tab_dn,
-                 maps, (bs && !a4) ? 31u : 15u) != cudaSuccess)
+                 maps) != cudaSuccess)
     return -1;
-  if (bs) {
-    BsParams B;
+  if (a4 && s.H % kMxKS == 0 && s.I % kMxKS == 0) {  // W4A4 on the block-scaled tensor core
+    Mx4Params B;
     B.w = w;
     B.H = s.H; B.I = s.I; B.A = A; B.E = s.E;
     B.meta = meta;
@@ -1421,10 +1286,9 @@ int launch_ffn_gemm(const k3moe_shape &s, const uint16_t *x, const k3moe_weights
     B.hrow = hrow;
     B.Y = Y;
     B.status = status;
-    uint8_t *xp = reinterpret_cast<uint8_t *>(xg), *hp = reinterpret_cast<uint8_t *>(h16);
+    uint8_t *xq = reinterpret_cast<uint8_t *>(xg), *hq = reinterpret_cast<uint8_t *>(h16);
     uint8_t *xsc = reinterpret_cast<uint8_t *>(base + L.xsc), *hsc = reinterpret_cast<uint8_t *>(base + L.hsc);
-    return a4 ? launch_gemm_bs<true>(s, x, perm, A, ntile_max, mt_gu, mt_dn, B, tab_dn, xp, xsc, hp, hsc, status, st)
-              : launch_gemm_bs<false>(s, x, perm, A, ntile_max, mt_gu, mt_dn, B, tab_dn, xp, xsc, hp, hsc, status, st);
+    return launch_gemm_mxf4(s, x, perm, A, ntile_max, mt_gu, mt_dn, B, tab_dn, xq, xsc, hq, hsc, status, st);
   }
   auto rows_to_f16 = a4 ? gemm_rows_to_f16_kernel<true> : gemm_rows_to_f16_kernel<false>;
   if (launch_pdl(rows_to_f16, dim3(A), dim3(256), 0, st, x, perm, s.k, A, s.H, xg, xexp, status) !=
