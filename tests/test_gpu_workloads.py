@@ -83,11 +83,14 @@ def test_decode_i1536():
     _full("decode_i1536", dx, gen.CONFIGS["decode_i1536"])
 
 
-@pytest.mark.parametrize("name", ["prefill", "skewed"])
-def test_prefill_sampled(experts_2048, name):
+@pytest.mark.parametrize("name,mode", [("prefill", k3.K3MOE_FFN_AUTO), ("skewed", k3.K3MOE_FFN_AUTO),
+                                       ("prefill", k3.K3MOE_FFN_W4A4), ("skewed", k3.K3MOE_FFN_W4A4)])
+def test_prefill_sampled(experts_2048, name, mode):
+    """W4A4 runs the persistent block-scaled GEMM at about 94 (gate/up) and 165
+    (down) tiles per CTA here; its sample is checked against the oracle's A4 path."""
     s = gen.CONFIGS[name]
     lg, xd, logits, xbits = device_inputs(name, s)
-    r = host(run_layer(s, lg, xd, _weights(experts_2048)))
+    r = host(run_layer(s, lg, xd, _weights(experts_2048), bufs=alloc_layer(s, mode=mode), mode=mode))
     assert r["status"][0] == 0
     idx, w, counts, offsets, perm, inv = _route_bucket_exact(s, logits, r)
     np.testing.assert_array_equal(r["out"], bf16_rne_bits_of(r["out_f32"]))
@@ -99,6 +102,7 @@ def test_prefill_sampled(experts_2048, name):
     sample |= set(int(t) for t in rng.integers(0, s.T, 3))
     sample = sorted(sample)
     W = _host_experts(s, np.unique(idx[sample]))
-    ref = np.stack([oracle.moe_token(s, xbits[t], idx[t], w[t], W) for t in sample])
+    a4 = mode == k3.K3MOE_FFN_W4A4
+    ref = np.stack([oracle.moe_token(s, xbits[t], idx[t], w[t], W, a4=a4) for t in sample])
     got = r["out_f32"][sample]
     assert max_rel_err(got, ref) <= TOL, max_rel_err(got, ref)
