@@ -293,7 +293,7 @@ def resolved_mode(s, mode):
         return mode
     A = s.T * s.k
     gemm_ok = (2 * s.I) % 128 == 0 and s.H % 128 == 0 and s.I % 64 == 0
-    return 3 if gemm_ok and A >= 4 * min(A, s.E) else 1
+    return 3 if gemm_ok and 2 * A >= 3 * min(A, s.E) else 1
 
 
 def ffn_kernel_count(s, mode):
