@@ -402,29 +402,27 @@ template <int R>
 struct ItemRows {
   int4 sl;                    // slot record {expert, first position, tokens, present}
   int rb;                     // row block of the item
-  const uint8_t *cb, *sb;     // the lane's first code chunk and scale byte in row 0 of the expert
-  int lim;                    // KIND 0: I (the up row of row pair i is I + i); KIND 1: H - 1 (last row)
+  const uint8_t *cr[R], *sr[R];  // the lane's first code chunk and scale byte of each row
 };
-
-// Row r of an item: gate/up (gate row i, up row I + i), down (R consecutive rows,
-// those past H computed as duplicates of row H - 1 and not stored).
-template <int KIND, int R>
-__device__ __forceinline__ int item_row(const ItemRows<R> &it, int r) {
-  if (KIND == 0) return r == 0 ? it.rb : it.lim + it.rb;
-  return min(it.rb * R + r, it.lim);
-}
 
 template <int KIND, int R, int NJ>
 __device__ __forceinline__ void item_rows_at(const RowsParams &P, long long item, int per_slot, ItemRows<R> &it) {
   const int lane = threadIdx.x & 31;
+  constexpr size_t cbytes = 512 * NJ, sbytes = 32 * NJ;  // K/2 and K/32 for K = 1024 * NJ
   it.sl = __ldg(P.slots + static_cast<int>(item / per_slot));
   it.rb = static_cast<int>(item % per_slot);
-  it.lim = KIND == 0 ? P.I : P.H - 1;
-  it.cb = nullptr;
-  it.sb = nullptr;
+  const uint8_t *cb = nullptr, *sb = nullptr;
   if (it.sl.w) {
-    it.cb = ldg_ptr(KIND == 0 ? P.w.w13_codes : P.w.w2_codes, it.sl.x) + 16 * lane;
-    it.sb = ldg_ptr(KIND == 0 ? P.w.w13_scales : P.w.w2_scales, it.sl.x) + lane;
+    cb = ldg_ptr(KIND == 0 ? P.w.w13_codes : P.w.w2_codes, it.sl.x);
+    sb = ldg_ptr(KIND == 0 ? P.w.w13_scales : P.w.w2_scales, it.sl.x);
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    int row;
+    if (KIND == 0) row = r == 0 ? it.rb : P.I + it.rb;
+    else row = min(it.rb * R + r, P.H - 1);  // rows past H are computed (duplicates), not stored
+    it.cr[r] = cb + row * cbytes + 16 * lane;
+    it.sr[r] = sb + row * sbytes + lane;
   }
 }
 
@@ -442,16 +440,14 @@ __device__ __forceinline__ uint32_t ldg_u8_pf(const void *p) {
   return v;
 }
 
-template <int KIND, int R, int NJ, int J0, int NH>
+template <int R, int J0, int NH>
 __device__ __forceinline__ void load_half(const ItemRows<R> &it, uint4 (&cw)[R][NH], uint32_t (&sc)[R][NH]) {
-  constexpr size_t cbytes = 512 * NJ, sbytes = 32 * NJ;  // K/2 and K/32 for K = 1024 * NJ
 #pragma unroll
   for (int j = 0; j < NH; ++j)
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      const size_t row = static_cast<size_t>(item_row<KIND, R>(it, r));
-      cw[r][j] = ldg_code_pf(it.cb + row * cbytes + 16 * 32 * (J0 + j));
-      sc[r][j] = ldg_u8_pf(it.sb + row * sbytes + 32 * (J0 + j));
+      cw[r][j] = ldg_code_pf(it.cr[r] + 16 * 32 * (J0 + j));
+      sc[r][j] = ldg_u8_pf(it.sr[r] + 32 * (J0 + j));
     }
 }
 
@@ -500,8 +496,8 @@ __global__ void __launch_bounds__(kGvWarps * 32, 2) gemv_rows_pipe_kernel(RowsPa
   uint4 ca[R][HA], cb[R][HB > 0 ? HB : 1];
   uint32_t sa[R][HA], sb[R][HB > 0 ? HB : 1];
   if (cur.sl.w) {
-    load_half<KIND, R, NJ, 0, HA>(cur, ca, sa);
-    if (HB > 0) load_half<KIND, R, NJ, HA, HB>(cur, cb, sb);
+    load_half<R, 0, HA>(cur, ca, sa);
+    if (HB > 0) load_half<R, HA, HB>(cur, cb, sb);
   }
   for (;;) {
     const long long nitem = item + stride;
@@ -527,10 +523,10 @@ __global__ void __launch_bounds__(kGvWarps * 32, 2) gemv_rows_pipe_kernel(RowsPa
 #pragma unroll
       for (int r = 0; r < R; ++r) acc[r] = 0.f;
       if (cur.sl.w) compute_half<R, 0, HA, NCH>(ca, sa, arow, acc);
-      if (last && pf) load_half<KIND, R, NJ, 0, HA>(nxt, ca, sa);  // half A of the next item flies now
+      if (last && pf) load_half<R, 0, HA>(nxt, ca, sa);  // half A of the next item flies now
       if (HB > 0) {
         if (cur.sl.w) compute_half<R, HA, HB, NCH>(cb, sb, arow, acc);
-        if (last && pf) load_half<KIND, R, NJ, HA, HB>(nxt, cb, sb);
+        if (last && pf) load_half<R, HA, HB>(nxt, cb, sb);
       }
 #pragma unroll
       for (int r = 0; r < R; ++r)
@@ -614,7 +610,7 @@ template <int KIND, int R>
 cudaError_t launch_rows_nt1(const RowsParams &P, int K, int nsm, cudaStream_t st) {
   const int nch = K / 32;
   if constexpr (KIND == 1) {
-    if (nch == 64) return launch_rows_pipe<KIND, 6, 2>(P, nsm, st);  // 6 rows: 1.5x the bytes in flight
+    if (nch == 64) return launch_rows_pipe<KIND, R, 2>(P, nsm, st);
     return launch_rows_kernel<KIND, R, 1, 2, false>(P, nsm, st);
   } else {
     if (nch == 64) return launch_rows_pipe<KIND, R, 2>(P, nsm, st);
