@@ -1,6 +1,7 @@
-"""C-ABI checks that need no GPU: the library builds and loads, exports every
-function that include/k3moe.h declares, and rejects bad arguments on the host
-before any launch."""
+"""C-ABI checks on the host: the library builds and loads, exports every
+function that include/k3moe.h declares, and rejects bad arguments before any
+launch (no GPU needed).  One GPU-marked test checks the AUTO mode's resolution,
+which needs the driver's tensor-map encoder that the GEMM modes depend on."""
 import ctypes
 import os
 import re
@@ -136,3 +137,29 @@ def test_w4a4_mode_is_a_valid_mode(L):
     d = ctypes.c_void_p(256)
     wz = k3._WeightsC(256, 256, 256, 256)
     assert L.k3moe_expert_ffn(s, d, ctypes.byref(wz), d, d, d, 5, d, 1 << 30, None, None) == k3.K3MOE_ERR_ARG
+
+
+def _bench_module():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("k3moe_bench", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("T,E,k,gemm", [
+    (1, 896, 16, False), (8, 896, 16, False), (64, 896, 16, False),   # < 1.5 assignments per possible expert
+    (96, 896, 16, True), (128, 896, 16, True), (300, 5, 1, True),     # >= 1.5: the tensor-core GEMM
+])
+def test_auto_mode_resolution(L, T, E, k, gemm):
+    """AUTO resolves to the GEMM exactly when 2 A >= 3 min(A, E) (the measured
+    crossover at H = 7168, I = 2048), seen through the workspace it asks for, and
+    bench.py's mirror of the rule (which labels and counts the kernels) agrees."""
+    import gen
+    s = gen.Shape(T, 7168, 2048, E, k)
+    ws = {m: L.k3moe_workspace_bytes(s, k3.K3MOE_OP_EXPERT_FFN, m)
+          for m in (k3.K3MOE_FFN_AUTO, k3.K3MOE_FFN_GEMV, k3.K3MOE_FFN_GEMM)}
+    assert ws[k3.K3MOE_FFN_GEMM] != ws[k3.K3MOE_FFN_GEMV]
+    assert ws[k3.K3MOE_FFN_AUTO] == ws[k3.K3MOE_FFN_GEMM if gemm else k3.K3MOE_FFN_GEMV]
+    assert _bench_module().resolved_mode(s, k3.K3MOE_FFN_AUTO) == (3 if gemm else 1)
