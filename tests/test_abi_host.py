@@ -158,7 +158,7 @@ def test_auto_mode_resolution(L, T, E, k, gemm):
     bench.py's mirror of the rule (which labels and counts the kernels) agrees."""
     import gen
     s = gen.Shape(T, 7168, 2048, E, k)
-    ws = {m: L.k3moe_workspace_bytes(s, k3.K3MOE_OP_EXPERT_FFN, m)
+    ws = {m: k3.k3moe_workspace_bytes(s, k3.K3MOE_OP_EXPERT_FFN, m)
           for m in (k3.K3MOE_FFN_AUTO, k3.K3MOE_FFN_GEMV, k3.K3MOE_FFN_GEMM)}
     assert ws[k3.K3MOE_FFN_GEMM] != ws[k3.K3MOE_FFN_GEMV]
     assert ws[k3.K3MOE_FFN_AUTO] == ws[k3.K3MOE_FFN_GEMM if gemm else k3.K3MOE_FFN_GEMV]
