@@ -54,7 +54,7 @@ typedef enum {
   K3MOE_ERR_WORKSPACE = -4,   /* workspace NULL or smaller than required         */
   K3MOE_ERR_ARCH = -5,        /* current device is not compute capability 10.3   */
   K3MOE_ERR_LAUNCH = -6,      /* a CUDA launch failed                            */
-  K3MOE_ERR_UNSUPPORTED = -7, /* valid request this build cannot serve           */
+  K3MOE_ERR_UNSUPPORTED = -7, /* valid request the chosen mode cannot serve      */
   K3MOE_ERR_NOALLOC_LIMIT = -8 /* problem needs more scratch than the fixed array of
                                   k3moe_expert_ffn_noalloc holds                  */
 } k3moe_status;

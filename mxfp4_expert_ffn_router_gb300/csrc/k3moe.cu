@@ -171,7 +171,7 @@ const char *k3moe_status_string(int code) {
     case K3MOE_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
     case K3MOE_ERR_ARCH: return "current device is not sm_103 (GB300)";
     case K3MOE_ERR_LAUNCH: return "CUDA launch failed";
-    case K3MOE_ERR_UNSUPPORTED: return "request not supported by this build";
+    case K3MOE_ERR_UNSUPPORTED: return "request not supported by the chosen mode";
     case K3MOE_ERR_NOALLOC_LIMIT: return "problem exceeds the fixed scratch of k3moe_expert_ffn_noalloc";
     default: return "unknown status";
   }
