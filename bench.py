@@ -65,6 +65,23 @@ def dist_env():
     return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def slowest_rank_ms(local_ms: float, ws: int, device) -> float:
+    """The longest of the ranks' timed regions (every rank calls it; a MAX
+    all_reduce of the timing only, no data crosses ranks)."""
+    if ws == 1:
+        return float(local_ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, slowest_ms: float, ws: int) -> float:
+    """Units all replicas processed per second of the slowest replica's time."""
+    return ws * units_per_rank / (slowest_ms / 1e3)
+
+
 def expert_bytes(s) -> int:
     """Packed MXFP4 bytes of one expert: 3 matrices x H*I x (1/2 code + 1/32 scale)."""
     return 3 * s.H * s.I * 17 // 32
@@ -444,12 +461,8 @@ def run_gpu(a):
     ffn_ms = np.array([e[1].elapsed_time(e[2]) for e in pevs])
     comb_ms = np.array([e[2].elapsed_time(e[3]) for e in pevs])
     pstep_ms = np.array([e[0].elapsed_time(e[3]) for e in pevs])
-    tot_ms = float(step_ms.sum())
-    if ws > 1:
-        t = torch.tensor([tot_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot_ms = float(t.item())
-    value = ws * s.T * a.steps / (tot_ms / 1e3)
+    tot_ms = slowest_rank_ms(float(step_ms.sum()), ws, dev)
+    value = whole_job_rate(s.T * a.steps, tot_ms, ws)
     # algorithmic bytes of the expert FFN per call: touched experts' codes+scales,
     # x read, h written and read (bf16), Y written (fp32)
     be = expert_bytes(s)
@@ -494,11 +507,7 @@ def run_gpu(a):
             ev1.synchronize()
             if i >= 3:
                 tot += ev0.elapsed_time(ev1)
-        e2e_val = s.T * n_e2e / (tot / 1e3)
-        if ws > 1:
-            t = torch.tensor([tot], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_val = ws * s.T * n_e2e / (float(t.item()) / 1e3)
+        e2e_val = whole_job_rate(s.T * n_e2e, slowest_rank_ms(tot, ws, dev), ws)
         e2e = {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": s.T * s.E * 4 + s.T * s.H * 2,
                "d2h_bytes_per_step": s.T * s.H * 2, "steps": n_e2e}
 
