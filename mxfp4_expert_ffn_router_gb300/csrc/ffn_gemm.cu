@@ -312,7 +312,9 @@ __global__ void __launch_bounds__(32)
 // maps[E + u] (w2) for active slot u, each the host-encoded template with its
 // global address replaced by the expert's code pointer.  Experts whose code
 // pointers are NULL or not 16-byte aligned keep the template's address; the
-// GEMMs treat them as absent and never load through their map.
+// GEMMs treat them as absent and never load through their map.  An expert whose
+// four pointers are all given but whose codes are misaligned is reported
+// (K3MOE_DEV_BOUNDS), once per map.
 //
 // The same launch writes the tile tables of both GEMMs: entry t of a table is
 // {active slot, expert, first bucket position, (tokens << 16) | row tile} of
@@ -329,7 +331,8 @@ __global__ void __launch_bounds__(128)
                       k3moe_weights w, const int32_t *__restrict__ active, const int32_t *__restrict__ meta, int E,
                       const int32_t *__restrict__ slot_p0, const int32_t *__restrict__ slot_cnt,
                       const int32_t *__restrict__ pref_gu, const int32_t *__restrict__ pref_dn, int mt_gu, int mt_dn,
-                      int4 *__restrict__ tab_gu, int4 *__restrict__ tab_dn, uint8_t *__restrict__ maps) {
+                      int4 *__restrict__ tab_gu, int4 *__restrict__ tab_dn, uint8_t *__restrict__ maps,
+                      int32_t *status) {
   pdl_wait();
   pdl_trigger();
   const int na = meta[0];
@@ -345,6 +348,9 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
   for (int i = 0; i < kMapBytes / 16; ++i) d4[i] = tmpl[i];
   const uint8_t *codes = which ? w.w2_codes[e] : w.w13_codes[e];
+  if (w.w13_codes[e] && w.w13_scales[e] && w.w2_codes[e] && w.w2_scales[e] &&
+      ((reinterpret_cast<uintptr_t>(w.w13_codes[e]) | reinterpret_cast<uintptr_t>(w.w2_codes[e])) & 15u) != 0)
+    set_status(status, K3MOE_DEV_BOUNDS);
   if (codes && (reinterpret_cast<uintptr_t>(codes) & 15u) == 0)
     asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;" ::"l"(dst), "l"(codes)
                  : "memory");
@@ -883,7 +889,6 @@ __global__ void __launch_bounds__(kMxThreads, 2)
     mb_init(&acc_bar, 1);
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    if (!present && c13 && s13 && c2 && s2 && blockIdx.x == 0) set_status(P.status, K3MOE_DEV_BOUNDS);
   }
   if (warp == kMxMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&tmem_holder)),
@@ -1274,7 +1279,7 @@ int launch_ffn_gemm(const k3moe_shape &s, const uint16_t *x, const k3moe_weights
                  t2, w, static_cast<const int32_t *>(active), static_cast<const int32_t *>(meta), s.E,
                  static_cast<const int32_t *>(sp0), static_cast<const int32_t *>(scnt),
                  static_cast<const int32_t *>(pgu), static_cast<const int32_t *>(pdn), mt_gu, mt_dn, tab_gu, tab_dn,
-                 maps) != cudaSuccess)
+                 maps, status) != cudaSuccess)
     return -1;
   if (a4 && s.H % kMxKS == 0 && s.I % kMxKS == 0) {  // W4A4 on the block-scaled tensor core
     Mx4Params B;

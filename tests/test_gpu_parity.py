@@ -296,3 +296,29 @@ def test_bad_expert_index_is_reported_not_read():
     r = host(b)
     assert r["status"][0] & k3.K3MOE_DEV_BOUNDS
     assert r["offsets"][-1] == 4 and r["inv"][2] == -1 and r["inv"][4] == -1
+
+
+@pytest.mark.parametrize("mode", [k3.K3MOE_FFN_GEMV, k3.K3MOE_FFN_STREAM, k3.K3MOE_FFN_GEMM, k3.K3MOE_FFN_W4A4])
+def test_misaligned_expert_is_reported_and_reads_as_absent(mode):
+    """An expert whose pointers are all given but whose gate/up codes are not
+    16-byte aligned: every mode checks the alignment before it reads through the
+    pointer, reports K3MOE_DEV_BOUNDS, and gives that expert zero rows; the other
+    experts are unaffected.  (The shifted pointer stays inside its allocation.)"""
+    s = gen.Shape(24, 512, 512, 6, 2)
+    logits = np.random.default_rng(11).standard_normal((24, 6)).astype(np.float32)
+    xbits = gen.normal_bf16_bits(4, gen.stream(gen.KIND_X), 24 * 512).reshape(24, 512)
+    experts = _experts_host(512, 512, 6)
+    idx, _, _ = oracle.route(s, logits)
+    bad = int(idx[0, 0])
+    Wd = _device_weights(experts)
+    ptrs = [p.clone() for p in Wd.ptrs]
+    ptrs[0][bad] += 1  # w13 codes of expert `bad`, one byte off
+    Wbad = k3.Weights(ptrs, keep=Wd.keep)
+    b = alloc_layer(s, mode=mode)
+    r = host(run_layer(s, torch.from_numpy(logits).cuda(), torch.from_numpy(xbits.view(np.int16)).cuda(),
+                       Wbad, bufs=b, mode=mode))
+    assert r["status"][0] & k3.K3MOE_DEV_BOUNDS
+    assert not (r["status"][0] & k3.K3MOE_DEV_TIMEOUT)
+    _full_check(s, logits, xbits, experts, r, a4=(mode == k3.K3MOE_FFN_W4A4), absent=(bad,))
+    lo, hi = r["offsets"][bad], r["offsets"][bad + 1]
+    assert hi > lo and not r["Y"][lo:hi].any()
