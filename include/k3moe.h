@@ -73,7 +73,10 @@ typedef struct {
 
 /* MXFP4 expert weights of one layer.  Each member is a DEVICE array of E device
  * pointers, one per expert.  Expert e is absent when any of its four pointers
- * is NULL: its assignments then produce zero rows (never an error).
+ * is NULL: its assignments then produce zero rows (never an error).  The host
+ * cannot see these pointers: an expert whose code arrays are not 16-byte aligned
+ * is also treated as absent (never read through), and the call sets
+ * K3MOE_DEV_BOUNDS in dev_status.
  *   w13_codes[e]  : uint8 [2I][H/2]  rows 0..I-1 are the gate projection, rows
  *                   I..2I-1 the up projection; byte c of a row holds column 2c in
  *                   its low nibble and column 2c+1 in its high nibble; each
