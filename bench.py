@@ -22,6 +22,7 @@ import glob
 import hashlib
 import json
 import os
+import platform
 import subprocess
 import sys
 import tempfile
@@ -80,6 +81,20 @@ def slowest_rank_ms(local_ms: float, ws: int, device) -> float:
 def whole_job_rate(units_per_rank: int, slowest_ms: float, ws: int) -> float:
     """Units all replicas processed per second of the slowest replica's time."""
     return ws * units_per_rank / (slowest_ms / 1e3)
+
+
+def host_cpu() -> dict:
+    """The host the oracle is timed on: logical CPUs and the CPU model."""
+    model = platform.machine()
+    try:
+        for line in open("/proc/cpuinfo"):
+            key = line.split(":")[0].strip().lower()
+            if key in ("model name", "hardware", "cpu model"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except OSError:
+        pass
+    return {"nproc": os.cpu_count(), "model": model, "oracle_threads": 1}
 
 
 def expert_bytes(s) -> int:
@@ -287,7 +302,7 @@ def run_reference(a):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": workload_config(a, s),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, "host": host_cpu()},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -514,7 +529,7 @@ def run_gpu(a):
     cpu = None
     if rank == 0 and not a.no_cpu_baseline:
         v, sample = oracle_sample(a.config, s, sets, a.cpu_seconds)
-        cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample}
+        cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample, "host": host_cpu()}
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": a.steps,
                 "warmup": a.warmup, "ms_per_step": tot_ms / a.steps, "higher_is_better": True,

@@ -83,3 +83,8 @@ def test_traffic_record_follows_the_sources(bench, tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.recorded_traffic("decode") is None
     assert bench.recorded_traffic("prefill") is None
+
+
+def test_host_cpu_is_described(bench):
+    h = bench.host_cpu()
+    assert h["nproc"] >= 1 and h["oracle_threads"] == 1 and isinstance(h["model"], str) and h["model"]
