@@ -165,20 +165,29 @@ int k3moe_expert_ffn(k3moe_shape s, const uint16_t *x, const k3moe_weights *w,
  * cannot call cudaMalloc around the layer: cudaMalloc/cudaFree may synchronise
  * the whole device and stall other streams, a host framework may own all device
  * memory through its own pool, or the code may run where CUDA allocation calls
- * are not allowed.  This entry point computes exactly what k3moe_expert_ffn does,
- * with the same arguments minus ws/ws_bytes; its scratch is a file-scope device
- * array of K3MOE_NOALLOC_SCRATCH_BYTES that every GPU loading the library keeps
- * until the process exits.  It calls no allocation routine.
- *  - Limit: problems whose scratch (k3moe_workspace_bytes(s, K3MOE_OP_EXPERT_FFN,
- *    mode)) exceeds K3MOE_NOALLOC_SCRATCH_BYTES return K3MOE_ERR_NOALLOC_LIMIT and
- *    launch nothing (decode-sized batches fit; large prefill chunks do not).
+ * are not allowed.  This entry point takes the arguments of k3moe_expert_ffn
+ * minus ws/ws_bytes; its scratch is a file-scope device array of
+ * K3MOE_NOALLOC_SCRATCH_BYTES that every GPU loading the library keeps until the
+ * process exits.  It calls no allocation routine.
+ *  - Modes: it serves the CUDA-core kernels only.  K3MOE_FFN_AUTO means
+ *    K3MOE_FFN_GEMV here (k3moe_expert_ffn's AUTO may pick the tensor-core GEMM
+ *    for the same shape, so the two entry points can then differ within the
+ *    parity tolerance, not bitwise); K3MOE_FFN_GEMV and K3MOE_FFN_STREAM compute
+ *    bitwise what k3moe_expert_ffn computes in the same mode.  K3MOE_FFN_GEMM and
+ *    K3MOE_FFN_W4A4 return K3MOE_ERR_UNSUPPORTED; other values K3MOE_ERR_ARG.
+ *  - Limit: a problem whose scratch, k3moe_workspace_bytes(s, K3MOE_OP_EXPERT_FFN,
+ *    K3MOE_FFN_GEMV) (STREAM: ..., K3MOE_FFN_STREAM), exceeds
+ *    K3MOE_NOALLOC_SCRATCH_BYTES returns K3MOE_ERR_NOALLOC_LIMIT and launches
+ *    nothing (decode-sized batches fit; large prefill chunks do not).
  *  - The first call on a device looks up the array's device address with that
  *    device current (one-time set-up); make that first call before any stream
- *    capture.
+ *    capture.  Calls after a cudaDeviceReset of that device are not supported.
  *  - Every call on a device uses the same array, which keeps the previous call's
  *    contents; each call re-initialises whatever it reads.  Calls whose kernels
  *    overlap on the GPU (different streams, no ordering between them) race on the
- *    array and give wrong results: order them on one stream or with events. */
+ *    array and give wrong results: order them on one stream or with events.
+ *  - A failed launch returns K3MOE_ERR_LAUNCH with its text in
+ *    k3moe_last_cuda_error(), as for the other entry points. */
 #define K3MOE_NOALLOC_SCRATCH_BYTES (8u << 20)
 int k3moe_expert_ffn_noalloc(k3moe_shape s, const uint16_t *x, const k3moe_weights *w,
                              const int32_t *offsets, const int32_t *perm, float *Y, int mode,

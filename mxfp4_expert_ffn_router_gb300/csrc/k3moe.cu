@@ -14,7 +14,13 @@ using k3moe_stream = cudaStream_t;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int check_shape(const k3moe_shape &s) {
+thread_local const char *t_last_cuda_error = "no error";
+
+}  // namespace
+
+namespace k3moe {
+
+int abi_check_shape(const k3moe_shape &s) {
   if (s.T < 0 || s.E < 1 || s.E > 4096 || s.k < 1 || s.k > 32 || s.k > s.E) return K3MOE_ERR_SHAPE;
   if (s.H < 32 || s.H > 16384 || s.H % 32 || s.I < 32 || s.I > 16384 || s.I % 32) return K3MOE_ERR_SHAPE;
   if (static_cast<long long>(s.T) * s.k >= (1LL << 31)) return K3MOE_ERR_SHAPE;
@@ -22,12 +28,15 @@ int check_shape(const k3moe_shape &s) {
 }
 
 // The kernels use sm_103a instructions: refuse any other device.
-int check_arch() {
+int abi_check_arch() {
   static std::mutex mu;
   static int cached[64];
   static bool init = false;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return K3MOE_ERR_ARCH;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();  // leave no error behind for the next call
+    return K3MOE_ERR_ARCH;
+  }
   std::lock_guard<std::mutex> g(mu);
   if (!init) {
     for (int i = 0; i < 64; ++i) cached[i] = 0;
@@ -42,16 +51,18 @@ int check_arch() {
   return cached[dev] == 1 ? K3MOE_OK : K3MOE_ERR_ARCH;
 }
 
-thread_local const char *t_last_cuda_error = "no error";
-
-int launched(int rc) {
+int abi_launched(int rc) {
   const cudaError_t e = cudaGetLastError();
   if (rc == 0 && e == cudaSuccess) return K3MOE_OK;
   t_last_cuda_error = cudaGetErrorString(e == cudaSuccess ? cudaErrorLaunchFailure : e);
   return K3MOE_ERR_LAUNCH;
 }
 
-}  // namespace
+}  // namespace k3moe
+
+using k3moe::abi_check_arch;
+using k3moe::abi_check_shape;
+using k3moe::abi_launched;
 
 extern "C" {
 
@@ -84,7 +95,7 @@ static size_t ffn_workspace(const k3moe_shape &s, int resolved) {
 }
 
 size_t k3moe_workspace_bytes(k3moe_shape s, int op, int mode) {
-  if (check_shape(s) != K3MOE_OK) return 0;
+  if (abi_check_shape(s) != K3MOE_OK) return 0;
   if (op == K3MOE_OP_BUCKET) return k3moe::bucket_workspace(s);
   if (op == K3MOE_OP_EXPERT_FFN) return ffn_workspace(s, resolve_ffn_mode(s, mode));
   return 0;
@@ -92,32 +103,32 @@ size_t k3moe_workspace_bytes(k3moe_shape s, int op, int mode) {
 
 int k3moe_route(k3moe_shape s, const float *logits, int32_t *idx, float *w, int32_t *dev_status,
                 k3moe_stream_t stream) {
-  int rc = check_shape(s);
+  int rc = abi_check_shape(s);
   if (rc) return rc;
   if (s.T == 0) return K3MOE_OK;
   if (!logits || !idx || !w) return K3MOE_ERR_ARG;
-  if ((rc = check_arch())) return rc;
-  return launched(k3moe::launch_route(s, logits, idx, w, dev_status, reinterpret_cast<k3moe_stream>(stream)));
+  if ((rc = abi_check_arch())) return rc;
+  return abi_launched(k3moe::launch_route(s, logits, idx, w, dev_status, reinterpret_cast<k3moe_stream>(stream)));
 }
 
 int k3moe_bucket(k3moe_shape s, const int32_t *idx, int32_t *counts, int32_t *offsets, int32_t *perm,
                  int32_t *inv, void *ws, size_t ws_bytes, int32_t *dev_status,
                  k3moe_stream_t stream) {
-  int rc = check_shape(s);
+  int rc = abi_check_shape(s);
   if (rc) return rc;
   if (!counts || !offsets) return K3MOE_ERR_ARG;
   if (s.T > 0 && (!idx || !perm || !inv)) return K3MOE_ERR_ARG;
   const size_t need = k3moe::bucket_workspace(s);
   if (need && (!ws || ws_bytes < need || !aligned16(ws))) return K3MOE_ERR_WORKSPACE;
-  if ((rc = check_arch())) return rc;
-  return launched(k3moe::launch_bucket(s, idx, counts, offsets, perm, inv, ws, dev_status,
+  if ((rc = abi_check_arch())) return rc;
+  return abi_launched(k3moe::launch_bucket(s, idx, counts, offsets, perm, inv, ws, dev_status,
                                        reinterpret_cast<k3moe_stream>(stream)));
 }
 
 int k3moe_expert_ffn(k3moe_shape s, const uint16_t *x, const k3moe_weights *w, const int32_t *offsets,
                      const int32_t *perm, float *Y, int mode, void *ws, size_t ws_bytes,
                      int32_t *dev_status, k3moe_stream_t stream) {
-  int rc = check_shape(s);
+  int rc = abi_check_shape(s);
   if (rc) return rc;
   if (mode < K3MOE_FFN_AUTO || mode > K3MOE_FFN_W4A4) return K3MOE_ERR_ARG;
   const int resolved = resolve_ffn_mode(s, mode);
@@ -128,14 +139,14 @@ int k3moe_expert_ffn(k3moe_shape s, const uint16_t *x, const k3moe_weights *w, c
   if (!aligned16(x) || !aligned16(Y)) return K3MOE_ERR_ALIGN;
   const size_t need = ffn_workspace(s, resolved);
   if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u)) return K3MOE_ERR_WORKSPACE;
-  if ((rc = check_arch())) return rc;
+  if ((rc = abi_check_arch())) return rc;
   const cudaStream_t st = reinterpret_cast<k3moe_stream>(stream);
   if (resolved == K3MOE_FFN_STREAM)
-    return launched(k3moe::launch_ffn_stream(s, x, *w, offsets, perm, Y, ws, dev_status, st));
+    return abi_launched(k3moe::launch_ffn_stream(s, x, *w, offsets, perm, Y, ws, dev_status, st));
   if (resolved == K3MOE_FFN_GEMM || resolved == K3MOE_FFN_W4A4)
-    return launched(k3moe::launch_ffn_gemm(s, x, *w, offsets, perm, Y, ws, dev_status, st,
+    return abi_launched(k3moe::launch_ffn_gemm(s, x, *w, offsets, perm, Y, ws, dev_status, st,
                                            resolved == K3MOE_FFN_W4A4));
-  return launched(k3moe::launch_ffn_gemv(s, x, *w, offsets, perm, Y, ws, dev_status, st));
+  return abi_launched(k3moe::launch_ffn_gemv(s, x, *w, offsets, perm, Y, ws, dev_status, st));
 }
 
 int k3moe_quantize_mxfp4(int64_t n, const uint16_t *x, uint8_t *codes, uint8_t *scales, k3moe_stream_t stream) {
@@ -144,20 +155,20 @@ int k3moe_quantize_mxfp4(int64_t n, const uint16_t *x, uint8_t *codes, uint8_t *
   if (!x || !codes || !scales) return K3MOE_ERR_ARG;
   if (!aligned16(x) || !aligned16(codes)) return K3MOE_ERR_ALIGN;
   int rc;
-  if ((rc = check_arch())) return rc;
-  return launched(k3moe::launch_quantize_mxfp4(static_cast<long long>(n), x, codes, scales,
+  if ((rc = abi_check_arch())) return rc;
+  return abi_launched(k3moe::launch_quantize_mxfp4(static_cast<long long>(n), x, codes, scales,
                                                reinterpret_cast<k3moe_stream>(stream)));
 }
 
 int k3moe_combine(k3moe_shape s, const float *Y, const float *w, const int32_t *inv, uint16_t *out,
                   float *out_f32, k3moe_stream_t stream) {
-  int rc = check_shape(s);
+  int rc = abi_check_shape(s);
   if (rc) return rc;
   if (s.T == 0) return K3MOE_OK;
   if (!Y || !w || !inv || !out) return K3MOE_ERR_ARG;
   if (!aligned16(Y) || !aligned16(out) || (out_f32 && !aligned16(out_f32))) return K3MOE_ERR_ALIGN;
-  if ((rc = check_arch())) return rc;
-  return launched(k3moe::launch_combine(s, Y, w, inv, out, out_f32, reinterpret_cast<k3moe_stream>(stream)));
+  if ((rc = abi_check_arch())) return rc;
+  return abi_launched(k3moe::launch_combine(s, Y, w, inv, out, out_f32, reinterpret_cast<k3moe_stream>(stream)));
 }
 
 const char *k3moe_last_cuda_error(void) { return t_last_cuda_error; }

@@ -7,6 +7,14 @@
 
 namespace k3moe {
 
+// Shared by every C-ABI entry point (defined in k3moe.cu).
+int abi_check_shape(const k3moe_shape &s);  // K3MOE_OK or K3MOE_ERR_SHAPE
+int abi_check_arch();                       // K3MOE_OK or K3MOE_ERR_ARCH (current device)
+// Status of a launch sequence: rc != 0 or a pending CUDA error gives
+// K3MOE_ERR_LAUNCH, with the error consumed and its text kept for
+// k3moe_last_cuda_error().
+int abi_launched(int rc);
+
 // Launch with programmatic stream serialization, so a kernel's prologue may
 // overlap the tail of its predecessor; every kernel calls pdl_wait() before it
 // reads anything a predecessor wrote.

@@ -10,6 +10,10 @@
 // g_noalloc_scratch below, a file-scope device array of
 // K3MOE_NOALLOC_SCRATCH_BYTES that every GPU which loads this library holds
 // until the process exits.
+//
+// It serves the CUDA-core modes only (GEMV, STREAM; AUTO means GEMV): those are
+// the decode-sized paths whose scratch fits the array.  GEMM and W4A4 return
+// K3MOE_ERR_UNSUPPORTED.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -23,22 +27,24 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[K3MOE_NOALLOC_S
 
 // Device address of g_noalloc_scratch per device ordinal.  In host code the
 // array's name is only a host-side stand-in, so the address comes from
-// cudaGetSymbolAddress, called once per device with that device current.
+// cudaGetSymbolAddress, called once per device with that device current.  The
+// cached address belongs to the device's context at that time: calls after a
+// cudaDeviceReset of that device are not supported.
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void *g_scratch_ptr[kMaxDevices] = {};
 
 int scratch_for_current_device(void **out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return K3MOE_ERR_ARCH;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return K3MOE_ERR_ARCH;
+  }
   std::lock_guard<std::mutex> lock(g_mu);
   if (!g_scratch_ptr[dev]) {
     void *p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || !p) {
-      cudaGetLastError();  // clear the error state left by the failed lookup
-      return K3MOE_ERR_LAUNCH;
-    }
+    if (e != cudaSuccess || !p) return k3moe::abi_launched(-1);  // records the error text
     g_scratch_ptr[dev] = p;
   }
   *out = g_scratch_ptr[dev];
@@ -52,13 +58,11 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 extern "C" int k3moe_expert_ffn_noalloc(k3moe_shape s, const uint16_t *x, const k3moe_weights *w,
                                         const int32_t *offsets, const int32_t *perm, float *Y, int mode,
                                         int32_t *dev_status, k3moe_stream_t stream) {
-  // same argument checks as k3moe_expert_ffn
-  if (s.T < 0 || s.E < 1 || s.E > 4096 || s.k < 1 || s.k > 32 || s.k > s.E) return K3MOE_ERR_SHAPE;
-  if (s.H < 32 || s.H > 16384 || s.H % 32 || s.I < 32 || s.I > 16384 || s.I % 32) return K3MOE_ERR_SHAPE;
-  if (static_cast<long long>(s.T) * s.k >= (1LL << 31)) return K3MOE_ERR_SHAPE;
-  if (mode < K3MOE_FFN_AUTO || mode > K3MOE_FFN_STREAM) return K3MOE_ERR_ARG;
-  int resolved = mode;
-  if (mode == K3MOE_FFN_AUTO) resolved = K3MOE_FFN_GEMV;
+  int rc = k3moe::abi_check_shape(s);
+  if (rc) return rc;
+  if (mode < K3MOE_FFN_AUTO || mode > K3MOE_FFN_W4A4) return K3MOE_ERR_ARG;
+  if (mode == K3MOE_FFN_GEMM || mode == K3MOE_FFN_W4A4) return K3MOE_ERR_UNSUPPORTED;
+  const int resolved = mode == K3MOE_FFN_AUTO ? K3MOE_FFN_GEMV : mode;
   if (resolved == K3MOE_FFN_STREAM && !k3moe::ffn_stream_supported(s)) return K3MOE_ERR_UNSUPPORTED;
   if (s.T == 0) return K3MOE_OK;
   if (!x || !w || !offsets || !perm || !Y) return K3MOE_ERR_ARG;
@@ -67,20 +71,13 @@ extern "C" int k3moe_expert_ffn_noalloc(k3moe_shape s, const uint16_t *x, const 
   const size_t need =
       resolved == K3MOE_FFN_STREAM ? k3moe::ffn_stream_workspace(s) : k3moe::ffn_gemv_workspace(s);
   if (need > K3MOE_NOALLOC_SCRATCH_BYTES) return K3MOE_ERR_NOALLOC_LIMIT;
-  int major = 0, minor = 0, dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return K3MOE_ERR_ARCH;
-  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-  if (major != 10 || minor != 3) return K3MOE_ERR_ARCH;
+  if ((rc = k3moe::abi_check_arch())) return rc;
   void *ws = nullptr;
-  const int rc = scratch_for_current_device(&ws);
-  if (rc != K3MOE_OK) return rc;
+  if ((rc = scratch_for_current_device(&ws))) return rc;
   // Nothing in the scratch has to start at zero: the first kernel of each call
   // (the prep kernel) writes every counter, table and maximum the call reads.
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const int lrc = resolved == K3MOE_FFN_STREAM
-                      ? k3moe::launch_ffn_stream(s, x, *w, offsets, perm, Y, ws, dev_status, st)
-                      : k3moe::launch_ffn_gemv(s, x, *w, offsets, perm, Y, ws, dev_status, st);
-  if (lrc != 0) return K3MOE_ERR_LAUNCH;
-  return cudaPeekAtLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ERR_LAUNCH;
+  return k3moe::abi_launched(resolved == K3MOE_FFN_STREAM
+                                 ? k3moe::launch_ffn_stream(s, x, *w, offsets, perm, Y, ws, dev_status, st)
+                                 : k3moe::launch_ffn_gemv(s, x, *w, offsets, perm, Y, ws, dev_status, st));
 }

@@ -163,3 +163,24 @@ def test_auto_mode_resolution(L, T, E, k, gemm):
     assert ws[k3.K3MOE_FFN_GEMM] != ws[k3.K3MOE_FFN_GEMV]
     assert ws[k3.K3MOE_FFN_AUTO] == ws[k3.K3MOE_FFN_GEMM if gemm else k3.K3MOE_FFN_GEMV]
     assert _bench_module().resolved_mode(s, k3.K3MOE_FFN_AUTO) == (3 if gemm else 1)
+
+
+def test_noalloc_modes_on_the_host(L):
+    """The allocation-free entry point serves the CUDA-core modes only: GEMM and
+    W4A4 are refused as unsupported and an unknown mode as a bad argument, before
+    any device call (so on a machine without a GPU too)."""
+    s = _shape()
+    d = ctypes.c_void_p(256)
+    wz = k3._WeightsC(256, 256, 256, 256)
+    for mode in (k3.K3MOE_FFN_GEMM, k3.K3MOE_FFN_W4A4):
+        assert L.k3moe_expert_ffn_noalloc(s, d, ctypes.byref(wz), d, d, d, mode, None, None) == \
+            k3.K3MOE_ERR_UNSUPPORTED
+    for mode in (-1, 5, 99):
+        assert L.k3moe_expert_ffn_noalloc(s, d, ctypes.byref(wz), d, d, d, mode, None, None) == k3.K3MOE_ERR_ARG
+    big = _shape(T=4096, H=7168, I=2048, E=896, k=16)
+    assert L.k3moe_expert_ffn_noalloc(big, d, ctypes.byref(wz), d, d, d, k3.K3MOE_FFN_GEMV, None, None) == \
+        k3.K3MOE_ERR_NOALLOC_LIMIT
+    # the limit is checked against the GEMV workspace whatever AUTO resolves to elsewhere
+    mid = _shape(T=8, H=7168, I=2048, E=48, k=16)
+    assert L.k3moe_workspace_bytes(mid, k3.K3MOE_OP_EXPERT_FFN, k3.K3MOE_FFN_GEMV) <= k3.K3MOE_NOALLOC_SCRATCH_BYTES
+    assert L.k3moe_expert_ffn_noalloc(_shape(T=0), None, None, None, None, None, 0, None, None) == k3.K3MOE_OK

@@ -61,6 +61,37 @@ def test_noalloc_matches_workspace_entry_point_twice(T, H, I, E, k, mode):
         assert max_rel_err(got, ref) <= TOL, (call, max_rel_err(got, ref))
 
 
+def test_noalloc_auto_is_gemv_where_the_workspace_entry_point_picks_the_gemm():
+    """T=8, E=48, k=16: k3moe_expert_ffn's AUTO takes the tensor-core GEMM (2A >= 3
+    min(A, E)); the allocation-free entry point's AUTO takes the GEMV kernels.  Its
+    output is bitwise the workspace entry point's GEMV output and within the parity
+    tolerance of its AUTO (GEMM) output; GEMM and W4A4 are refused."""
+    T, H, I, E, k = 8, 7168, 2048, 48, 16
+    s, x, W, buf = _setup(T, H, I, E, k, k3.K3MOE_FFN_AUTO)
+    assert k3.k3moe_workspace_bytes(s, k3.K3MOE_OP_EXPERT_FFN, k3.K3MOE_FFN_AUTO) == \
+        k3.k3moe_workspace_bytes(s, k3.K3MOE_OP_EXPERT_FFN, k3.K3MOE_FFN_GEMM)
+    A = s.T * s.k
+    outs = {}
+    for mode in (k3.K3MOE_FFN_AUTO, k3.K3MOE_FFN_GEMV):
+        ws = torch.empty(k3.k3moe_workspace_bytes(s, k3.K3MOE_OP_EXPERT_FFN, mode), dtype=torch.uint8,
+                         device="cuda")
+        Y = torch.empty((A, s.H), dtype=torch.float32, device="cuda")
+        k3.k3moe_expert_ffn(s, x, W, buf["offsets"], buf["perm"], Y, mode, ws, buf["status"])
+        torch.cuda.synchronize()
+        outs[mode] = Y.cpu().numpy()
+    assert int(buf["status"].item()) == 0
+    Y = torch.full((A, s.H), float("nan"), dtype=torch.float32, device="cuda")
+    k3.k3moe_expert_ffn_noalloc(s, x, W, buf["offsets"], buf["perm"], Y, k3.K3MOE_FFN_AUTO, buf["status"])
+    torch.cuda.synchronize()
+    got = Y.cpu().numpy()
+    np.testing.assert_array_equal(got.view(np.int32), outs[k3.K3MOE_FFN_GEMV].view(np.int32))
+    assert max_rel_err(got, outs[k3.K3MOE_FFN_AUTO].astype(np.float64)) <= TOL
+    for mode in (k3.K3MOE_FFN_GEMM, k3.K3MOE_FFN_W4A4):
+        with pytest.raises(k3.K3moeError) as err:
+            k3.k3moe_expert_ffn_noalloc(s, x, W, buf["offsets"], buf["perm"], Y, mode, buf["status"])
+        assert err.value.code == k3.K3MOE_ERR_UNSUPPORTED
+
+
 def test_noalloc_refuses_problem_beyond_its_scratch():
     s = gen.Shape(4096, 7168, 2048, 896, 16)  # needs hundreds of MB of scratch
     assert k3.k3moe_workspace_bytes(s, k3.K3MOE_OP_EXPERT_FFN, 0) > k3.K3MOE_NOALLOC_SCRATCH_BYTES
