@@ -58,6 +58,11 @@ def parse():
                    help="override E (small cases for profiling; 0 = the workload's own)")
     p.add_argument("--tokens", type=int, default=0,
                    help="override T (small cases for profiling; 0 = the workload's own)")
+    p.add_argument("--legs", default="all", choices=["all", "none"],
+                   help="also time the other workloads (batch8, speculative-verify batches, prefill, "
+                        "skewed, probe) into the line's workloads object")
+    p.add_argument("--leg-steps", type=int, default=20, help="timed steps per extra workload (at most --steps)")
+    p.add_argument("--leg-cpu-seconds", type=float, default=2.0, help="oracle sample budget per extra workload")
     return p.parse_args()
 
 
@@ -84,17 +89,27 @@ def whole_job_rate(units_per_rank: int, slowest_ms: float, ws: int) -> float:
 
 
 def host_cpu() -> dict:
-    """The host the oracle is timed on: logical CPUs and the CPU model."""
-    model = platform.machine()
+    """The host the oracle is timed on: logical CPUs and the CPU model (lscpu's
+    "Model name", else /proc/cpuinfo, else the machine type)."""
+    model = None
     try:
-        for line in open("/proc/cpuinfo"):
-            key = line.split(":")[0].strip().lower()
-            if key in ("model name", "hardware", "cpu model"):
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for line in r.stdout.splitlines():
+            if line.split(":")[0].strip().lower() == "model name":
                 model = line.split(":", 1)[1].strip()
                 break
-    except OSError:
+    except Exception:
         pass
-    return {"nproc": os.cpu_count(), "model": model, "oracle_threads": 1}
+    if not model:
+        try:
+            for line in open("/proc/cpuinfo"):
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "hardware", "cpu model"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except OSError:
+            pass
+    return {"nproc": os.cpu_count(), "model": model or platform.machine(), "oracle_threads": 1}
 
 
 def expert_bytes(s) -> int:
@@ -139,6 +154,7 @@ class ClockSampler:
         setattr(self, which, time.time())
 
     def stop(self):
+        """End sampling and keep the samples; returns the summary of [t0, t1]."""
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -147,20 +163,25 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.f.close()
-        rows = []
+        self.rows = []
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 10:
                 continue
             try:
                 ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
-                rows.append((ts, float(parts[2]), float(parts[3]), parts[5:]))
+                self.rows.append((ts, float(parts[2]), float(parts[3]), parts[5:]))
             except Exception:
                 continue
         os.unlink(self.path)
+        return self.window(self.t0, self.t1)
+
+    def window(self, t0, t1):
+        """Median SM clock, maximum clock and throttle reasons seen in [t0, t1]."""
+        rows = getattr(self, "rows", None)
         if not rows:
             return None
-        lo, hi = (self.t0 or 0) - 1.0, (self.t1 or 1e18) + 1.0
+        lo, hi = (t0 or 0) - 1.0, (t1 or 1e18) + 1.0
         sel = [r for r in rows if lo <= r[0] <= hi] or rows
         names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = set()
@@ -201,24 +222,27 @@ def recorded_traffic(config: str):
 
 
 # ----------------------------------------------------------------------------- oracle
-def oracle_sample(name, s, sets, budget_s):
+def oracle_sample(name, s, sets, budget_s, whole_layers=None, a4=False):
     """Time the float64 oracle on whole layers of the first input sets (decode-
-    sized workloads) or on a token sample (prefill), within ~budget_s seconds."""
+    sized workloads) or on a token sample (route+bucket of every token, then the
+    FFN and combine token by token), within ~budget_s seconds, one thread."""
     import oracle
     t_tokens, t_sec, n = 0, 0.0, 0
-    if s.T <= 8:
+    whole = s.T <= 8 if whole_layers is None else whole_layers
+    tag = " (A4 path)" if a4 else ""
+    if whole:
         for logits, xbits in sets:
             ids = np.unique(routed_experts(s, logits))
             W = oracle.Weights(s.E, {int(e): tuple(z[0] for z in gen.expert_arrays(s.H, s.I, int(e), int(e) + 1))
                                      for e in ids})
             t = time.perf_counter()
-            oracle.moe_layer(s, logits, xbits, W)
+            oracle.moe_layer(s, logits, xbits, W, a4=a4)
             t_sec += time.perf_counter() - t
             t_tokens += s.T
             n += 1
             if t_sec >= budget_s:
                 break
-        return t_tokens / t_sec, f"{n} whole layers of {s.T} token(s) ({name}), 1 thread"
+        return t_tokens / t_sec, f"{n} whole layers of {s.T} token(s) ({name}){tag}, 1 thread"
     logits, xbits = sets[0]
     t = time.perf_counter()
     idx, w, _ = oracle.route(s, logits)
@@ -231,14 +255,14 @@ def oracle_sample(name, s, sets, budget_s):
                 cache[int(e)] = tuple(z[0] for z in gen.expert_arrays(s.H, s.I, int(e), int(e) + 1))
         W = oracle.Weights(s.E, {int(e): cache[int(e)] for e in idx[tok]})
         t = time.perf_counter()
-        oracle.moe_token(s, xbits[tok], idx[tok], w[tok], W)
+        oracle.moe_token(s, xbits[tok], idx[tok], w[tok], W, a4=a4)
         t_sec += time.perf_counter() - t
         n += 1
         if t_sec >= budget_s:
             break
     per_tok = t_sec / n + t_rb / s.T
     return 1.0 / per_tok, (f"route+bucket of all {s.T} tokens plus the FFN+combine of {n} tokens "
-                           f"({name}), 1 thread")
+                           f"({name}){tag}, 1 thread")
 
 
 def workload_shape(a):
@@ -365,15 +389,205 @@ def tensor_figures(s, mode, ffn_s):
             "frac": tf / (bf16 * ratio), "fp4_dense_frac": tf / (bf16 * 6.0)}
 
 
-def workload_config(a, s):
-    return {"workload": f"{a.config}: T={s.T} tokens, H={s.H}, I={s.I}, E={s.E}, top-{s.k}, "
+def workload_config(a, s, name=None):
+    name = name or a.config
+    return {"workload": f"{name}: T={s.T} tokens, H={s.H}, I={s.I}, E={s.E}, top-{s.k}, "
                         f"MXFP4 experts resident",
             "tokens": s.T, "hidden": s.H, "intermediate": s.I, "experts": s.E, "top_k": s.k,
             "l2": f"{getattr(a, 'l2_mode', 'L2 flushed between steps')}; inputs rotate over {a.sets} sets",
             "parallelism": f"replicas x{a.gpus}"}
 
 
+def hbm_peak():
+    peaks = measured_peaks()
+    if peaks and "hbm_gbs" in peaks:
+        return float(peaks["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def ffn_bytes_per_call(s, n_unique):
+    """Algorithmic bytes of one expert FFN call: the routed experts' MXFP4 codes
+    and scales (each read once), x read (bf16), h written and read (bf16), Y
+    written (fp32)."""
+    A = s.T * s.k
+    return n_unique * expert_bytes(s) + s.T * s.H * 2 + A * s.I * 4 + A * s.H * 4
+
+
+def per_expert_roofline_s(s, counts, mode):
+    """Roofline time of one expert FFN call taken expert by expert: each routed
+    expert costs the longer of streaming its weights (B_e / HBM peak) and its
+    FLOPs (n_e * 6 H I / tensor peak of the mode's MMA kind); the activation, h
+    and Y bytes add their HBM time.  GEMV and STREAM run on the CUDA cores: their
+    bound is the HBM term alone."""
+    bw = hbm_peak()[0] * 1e9
+    m = resolved_mode(s, mode)
+    peaks = measured_peaks()
+    bf16 = float(peaks["bf16_tflops"]) if peaks and "bf16_tflops" in peaks else 1900.0
+    f_peak = {3: bf16, 4: 6.0 * bf16}.get(m)
+    be = expert_bytes(s)
+    t = 0.0
+    for n in counts[counts > 0]:
+        t_w = be / bw
+        t_f = n * 6.0 * s.H * s.I / (f_peak * 1e12) if f_peak else 0.0
+        t += max(t_w, t_f)
+    A = s.T * s.k
+    return t + (s.T * s.H * 2 + A * s.I * 4 + A * s.H * 4) / bw
+
+
+def mode_name(s, mode):
+    return {1: "gemv", 2: "stream", 3: "gemm_w4a16", 4: "w4a4"}[resolved_mode(s, mode)]
+
+
 # ----------------------------------------------------------------------------- GPU arm
+class LayerBench:
+    """One workload's timed steps through the C ABI: route -> bucket -> expert
+    FFN -> combine on the launching stream, inputs rotating over host-generated
+    sets that are uploaded once (resident in HBM when the timed region starts)."""
+
+    def __init__(self, a, name, s, mode, W, nsets, dev, flush_always=False):
+        import torch
+
+        import mxfp4_expert_ffn_router_gb300 as k3
+        self.k3, self.a, self.name, self.s, self.mode, self.W, self.dev = k3, a, name, s, mode, W, dev
+        self.sets = [input_set(name, s, i) for i in range(nsets)]
+        self.nsets = nsets
+        A = s.T * s.k
+        self.logits_d = [torch.from_numpy(l).to(dev) for l, _ in self.sets]
+        self.x_d = [torch.from_numpy(x.view(np.int16)).to(dev) for _, x in self.sets]
+        picks = [routed_experts(s, l) for l, _ in self.sets]
+        self.uniq = [len(np.unique(p)) for p in picks]
+        self.counts = [np.bincount(p.ravel(), minlength=s.E) for p in picks]
+        i32, f32 = torch.int32, torch.float32
+        self.st = torch.zeros(1, dtype=i32, device=dev)
+        self.idx = torch.empty((s.T, s.k), dtype=i32, device=dev)
+        self.w = torch.empty((s.T, s.k), dtype=f32, device=dev)
+        self.cnt = torch.empty(s.E, dtype=i32, device=dev)
+        self.offsets = torch.empty(s.E + 1, dtype=i32, device=dev)
+        self.perm = torch.empty(A, dtype=i32, device=dev)
+        self.inv = torch.empty(A, dtype=i32, device=dev)
+        self.wsb = torch.empty(max(1, k3.k3moe_workspace_bytes(s, k3.K3MOE_OP_BUCKET)), dtype=torch.uint8,
+                               device=dev)
+        self.wsf = torch.empty(max(1, k3.k3moe_workspace_bytes(s, k3.K3MOE_OP_EXPERT_FFN, mode)),
+                               dtype=torch.uint8, device=dev)
+        self.Y = torch.empty((A, s.H), dtype=f32, device=dev)
+        self.out = torch.empty((s.T, s.H), dtype=torch.bfloat16, device=dev)
+        self.do_flush, self.l2_mode = l2_policy(a, s, self.sets)
+        self.do_flush = self.do_flush or flush_always
+        self.flush = torch.empty(L2_FLUSH_BYTES if self.do_flush else 1, dtype=torch.uint8, device=dev)
+        self.stream = torch.cuda.current_stream()
+        self.launches_per_step = 1 + (1 if A <= 4096 else 3) + ffn_kernel_count(s, mode) + 1
+
+    def layer(self, i, ev=None, phases=False):
+        """One step; ev[0] / ev[3] bracket it, ev[1] / ev[2] (phases only) bracket
+        the expert FFN call.  Events between calls end the launch overlap of the
+        kernels around them, so the step timing records only the outer two."""
+        k3, s, st, stream = self.k3, self.s, self.st, self.stream
+        j = i % self.nsets
+        if ev is not None:
+            ev[0].record(stream)
+        k3.k3moe_route(s, self.logits_d[j], self.idx, self.w, st, stream=stream)
+        k3.k3moe_bucket(s, self.idx, self.cnt, self.offsets, self.perm, self.inv, self.wsb, st, stream=stream)
+        if phases:
+            ev[1].record(stream)
+        k3.k3moe_expert_ffn(s, self.x_d[j], self.W, self.offsets, self.perm, self.Y, self.mode, self.wsf, st,
+                            stream=stream)
+        if phases:
+            ev[2].record(stream)
+        k3.k3moe_combine(s, self.Y, self.w, self.inv, self.out, None, stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    def run(self, steps, warmup, clocks=None, barrier=None):
+        """Warm-up, then K timed steps (events around each step only), then the same
+        K steps again with the expert FFN call bracketed (phase split)."""
+        import torch
+        for i in range(warmup):
+            if self.do_flush:
+                self.flush.fill_(i & 0xFF)
+            self.layer(i)
+        torch.cuda.synchronize()
+        if int(self.st.item()) != 0:
+            raise RuntimeError(f"{self.name}: device status {int(self.st.item())} during warm-up")
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        pevs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        if barrier:
+            barrier()
+        torch.cuda.synchronize()
+        t0 = time.time()
+        t_wall = time.perf_counter()
+        for i in range(steps):
+            if self.do_flush:
+                self.flush.fill_((i + 1) & 0xFF)
+            self.layer(warmup + i, evs[i])
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+        for i in range(steps):
+            if self.do_flush:
+                self.flush.fill_((i + 1) & 0xFF)
+            self.layer(warmup + i, pevs[i], phases=True)
+        torch.cuda.synchronize()
+        t1 = time.time()
+        if barrier:
+            barrier()
+        if int(self.st.item()) != 0:
+            raise RuntimeError(f"{self.name}: device status {int(self.st.item())} in the timed steps")
+        self.step_ms = np.array([e[0].elapsed_time(e[3]) for e in evs])
+        self.rb_ms = np.array([e[0].elapsed_time(e[1]) for e in pevs])
+        self.ffn_ms = np.array([e[1].elapsed_time(e[2]) for e in pevs])
+        self.comb_ms = np.array([e[2].elapsed_time(e[3]) for e in pevs])
+        self.pstep_ms = np.array([e[0].elapsed_time(e[3]) for e in pevs])
+        self.steps, self.warmup, self.t_wall, self.t0, self.t1 = steps, warmup, t_wall, t0, t1
+
+    def roofline(self):
+        s = self.s
+        sel = [(self.warmup + i) % self.nsets for i in range(self.steps)]
+        ffn_bytes = np.array([ffn_bytes_per_call(s, self.uniq[j]) for j in sel], dtype=np.float64)
+        achieved = float(ffn_bytes.sum() / (self.ffn_ms.sum() / 1e3) / 1e9)
+        peak, src = hbm_peak()
+        t_roof = np.array([per_expert_roofline_s(s, self.counts[j], self.mode) for j in sel])
+        med = float(np.median(self.ffn_ms)) / 1e3
+        return {"bound": "hbm", "kernel": ffn_kernel_label(s, self.mode), "achieved": achieved, "peak": peak,
+                "peak_source": src, "unit": "GB/s", "frac": achieved / peak,
+                "bytes_per_call": float(ffn_bytes.mean()), "ffn_us_median": med * 1e6,
+                "per_expert_roofline": {"t_us": float(t_roof.mean() * 1e6),
+                                        "frac": float(t_roof.sum() / (self.ffn_ms.sum() / 1e3))},
+                "tensor": tensor_figures(s, self.mode, med)}
+
+
+def run_leg(a, name, mode, W, dev, ws, clocks, cpu_cache, rank):
+    """One entry of the line's "workloads" object."""
+    s = gen.CONFIGS[name]
+    nsets = max(1, min(a.sets, 64 if s.T <= 64 else 4 if s.T <= 4096 else 2))
+    lb = LayerBench(a, name, s, mode, W, nsets, dev)
+    steps = max(1, min(a.steps, a.leg_steps))
+    warmup = max(3, min(a.warmup, 5))
+    lb.run(steps, warmup)
+    tot_ms = slowest_rank_ms(float(lb.step_ms.sum()), ws, dev)
+    ent = {"mode": mode_name(s, mode), "tokens": s.T, "experts": s.E, "top_k": s.k,
+           "tokens_per_s": whole_job_rate(s.T * steps, tot_ms, ws), "ms_per_step": tot_ms / steps,
+           "steps": steps, "warmup": warmup, "unique_experts_mean": float(np.mean(lb.uniq)),
+           "expert_ffn_us_median": float(np.median(lb.ffn_ms) * 1e3),
+           "phase_us_median": {"route_bucket": float(np.median(lb.rb_ms) * 1e3),
+                               "expert_ffn": float(np.median(lb.ffn_ms) * 1e3),
+                               "combine": float(np.median(lb.comb_ms) * 1e3)},
+           "roofline": lb.roofline(), "gpu_launches": lb.launches_per_step * steps, "l2": lb.l2_mode,
+           "clocks": clocks.window(lb.t0, lb.t1) if clocks else None}
+    a4 = resolved_mode(s, mode) == 4
+    if rank == 0 and not a.no_cpu_baseline:
+        key = (name, a4)
+        if key not in cpu_cache:
+            v, sample = oracle_sample(name, s, lb.sets[:1], a.leg_cpu_seconds, whole_layers=False, a4=a4)
+            cpu_cache[key] = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample}
+        ent["cpu_baseline"] = cpu_cache[key]
+    del lb
+    return ent
+
+
+LEGS = [("batch8", 0), ("batch8", 3), ("spec2", 1), ("spec2", 3), ("spec4", 1), ("spec4", 3),
+        ("spec12", 1), ("spec12", 3), ("spec16", 1), ("spec16", 3),
+        ("prefill", 0), ("prefill", 4), ("skewed", 0), ("skewed", 4), ("probe", 4), ("probe", 3)]
+
+
 def run_gpu(a):
     import torch
 
@@ -391,133 +605,58 @@ def run_gpu(a):
         k3build.build()
     if ws > 1:
         dist.barrier()
+    barrier = dist.barrier if ws > 1 else None
     s = workload_shape(a)
-    A = s.T * s.k
     nsets = max(1, a.sets)
-    sets = [input_set(a.config, s, i) for i in range(nsets)]
     experts = DeviceExperts(s.H, s.I, s.E, device=dev)
     W = k3.Weights.from_stacked(*experts.tensors)
-    logits_d = [torch.from_numpy(l).to(dev) for l, _ in sets]
-    x_d = [torch.from_numpy(x.view(np.int16)).to(dev) for _, x in sets]
-    uniq = [len(np.unique(routed_experts(s, l))) for l, _ in sets]
-    i32, f32 = torch.int32, torch.float32
-    st = torch.zeros(1, dtype=i32, device=dev)
-    idx = torch.empty((s.T, s.k), dtype=i32, device=dev)
-    w = torch.empty((s.T, s.k), dtype=f32, device=dev)
-    counts = torch.empty(s.E, dtype=i32, device=dev)
-    offsets = torch.empty(s.E + 1, dtype=i32, device=dev)
-    perm = torch.empty(A, dtype=i32, device=dev)
-    inv = torch.empty(A, dtype=i32, device=dev)
-    wsb = torch.empty(max(1, k3.k3moe_workspace_bytes(s, k3.K3MOE_OP_BUCKET)), dtype=torch.uint8, device=dev)
-    wsf = torch.empty(max(1, k3.k3moe_workspace_bytes(s, k3.K3MOE_OP_EXPERT_FFN, a.mode)), dtype=torch.uint8,
-                      device=dev)
-    Y = torch.empty((A, s.H), dtype=f32, device=dev)
-    out = torch.empty((s.T, s.H), dtype=torch.bfloat16, device=dev)
-    do_flush, a.l2_mode = l2_policy(a, s, sets)
-    flush = torch.empty(L2_FLUSH_BYTES if do_flush else 1, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
-    launches_per_step = 1 + (1 if A <= 4096 else 3) + ffn_kernel_count(s, a.mode) + 1
-
-    def layer(i, ev=None, phases=False):
-        """One step; ev[0] / ev[3] bracket it, ev[1] / ev[2] (phases only) bracket
-        the expert FFN call.  Events between calls end the launch overlap of the
-        kernels around them, so the step timing records only the outer two."""
-        j = i % nsets
-        if ev is not None:
-            ev[0].record(stream)
-        k3.k3moe_route(s, logits_d[j], idx, w, st, stream=stream)
-        k3.k3moe_bucket(s, idx, counts, offsets, perm, inv, wsb, st, stream=stream)
-        if phases:
-            ev[1].record(stream)
-        k3.k3moe_expert_ffn(s, x_d[j], W, offsets, perm, Y, a.mode, wsf, st, stream=stream)
-        if phases:
-            ev[2].record(stream)
-        k3.k3moe_combine(s, Y, w, inv, out, None, stream=stream)
-        if ev is not None:
-            ev[3].record(stream)
-
-    for i in range(a.warmup):
-        if do_flush:
-            flush.fill_(i & 0xFF)
-        layer(i)
-    torch.cuda.synchronize()
-    if int(st.item()) != 0:
-        raise RuntimeError(f"device status {int(st.item())} during warm-up")
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(a.steps)]
-    pevs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(a.steps)]
+    lb = LayerBench(a, a.config, s, a.mode, W, nsets, dev)
+    a.l2_mode = lb.l2_mode
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()
     time.sleep(0.3)
-    if ws > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    clocks.mark("t0")
-    t_wall = time.perf_counter()
-    for i in range(a.steps):
-        if do_flush:
-            flush.fill_((i + 1) & 0xFF)
-        layer(a.warmup + i, evs[i])
-    torch.cuda.synchronize()
-    t_wall = time.perf_counter() - t_wall
-    # the same K steps again with the phases bracketed: the expert FFN call's own
-    # duration (roofline) and the per-phase split
-    for i in range(a.steps):
-        if do_flush:
-            flush.fill_((i + 1) & 0xFF)
-        layer(a.warmup + i, pevs[i], phases=True)
-    torch.cuda.synchronize()
-    clocks.mark("t1")
-    if ws > 1:
-        dist.barrier()
-    time.sleep(0.2)
-    clk = clocks.stop()
-    step_ms = np.array([e[0].elapsed_time(e[3]) for e in evs])
-    rb_ms = np.array([e[0].elapsed_time(e[1]) for e in pevs])
-    ffn_ms = np.array([e[1].elapsed_time(e[2]) for e in pevs])
-    comb_ms = np.array([e[2].elapsed_time(e[3]) for e in pevs])
-    pstep_ms = np.array([e[0].elapsed_time(e[3]) for e in pevs])
-    tot_ms = slowest_rank_ms(float(step_ms.sum()), ws, dev)
+    lb.run(a.steps, a.warmup, barrier=barrier)
+    clocks.t0, clocks.t1 = lb.t0, lb.t1
+    tot_ms = slowest_rank_ms(float(lb.step_ms.sum()), ws, dev)
     value = whole_job_rate(s.T * a.steps, tot_ms, ws)
-    # algorithmic bytes of the expert FFN per call: touched experts' codes+scales,
-    # x read, h written and read (bf16), Y written (fp32)
-    be = expert_bytes(s)
-    ffn_bytes = np.array([uniq[(a.warmup + i) % nsets] * be for i in range(a.steps)], dtype=np.float64)
-    ffn_bytes += s.T * s.H * 2 + A * s.I * 4 + A * s.H * 4
-    achieved = float(ffn_bytes.sum() / (ffn_ms.sum() / 1e3) / 1e9)
-    peaks = measured_peaks()
-    if peaks and "hbm_gbs" in peaks:
-        peak, peak_src = float(peaks["hbm_gbs"]), "measured"
-    else:
-        peak, peak_src = 6800.0, "fallback"
-    roof = {"bound": "hbm", "kernel": ffn_kernel_label(s, a.mode),
-            "achieved": achieved, "peak": peak, "peak_source": peak_src, "unit": "GB/s",
-            "frac": achieved / peak, "traffic": recorded_traffic(a.config),
-            "bytes_per_call": float(ffn_bytes.mean()), "ffn_us_median": float(np.median(ffn_ms) * 1e3),
-            "tensor": tensor_figures(s, a.mode, float(np.median(ffn_ms)) / 1e3)}
+    roof = lb.roofline()
+    roof["traffic"] = recorded_traffic(a.config)
+    head_launches = lb.launches_per_step * a.steps
+    head_step_us = {"median": float(np.median(lb.step_ms) * 1e3), "min": float(lb.step_ms.min() * 1e3),
+                    "max": float(lb.step_ms.max() * 1e3)}
+    head_phases = {"route_bucket": float(np.median(lb.rb_ms) * 1e3),
+                   "expert_ffn": float(np.median(lb.ffn_ms) * 1e3),
+                   "combine": float(np.median(lb.comb_ms) * 1e3),
+                   "step_with_phase_events": float(np.median(lb.pstep_ms) * 1e3),
+                   "note": "a second pass of the same K steps with events around the "
+                           "expert FFN call; value and step_us come from the first pass"}
+    head_wall = lb.t_wall
+    head_sets = lb.sets
 
     # ------------------------------------------------------------- end to end (host buffers)
     e2e = None
     if not a.no_e2e:
-        lg_h = [torch.from_numpy(l).pin_memory() for l, _ in sets]
-        x_h = [torch.from_numpy(x.view(np.int16)).pin_memory() for _, x in sets]
+        lg_h = [torch.from_numpy(l).pin_memory() for l, _ in lb.sets]
+        x_h = [torch.from_numpy(x.view(np.int16)).pin_memory() for _, x in lb.sets]
         out_h = torch.empty((s.T, s.H), dtype=torch.bfloat16).pin_memory()
-        lg_dev = torch.empty_like(logits_d[0])
-        x_dev = torch.empty_like(x_d[0])
+        lg_dev = torch.empty_like(lb.logits_d[0])
+        x_dev = torch.empty_like(lb.x_d[0])
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         n_e2e = max(1, min(a.steps, 500))
+        stream = lb.stream
         tot = 0.0
         for i in range(n_e2e + 3):
             j = i % nsets
-            if do_flush:
-                flush.fill_(i & 0xFF)
+            if lb.do_flush:
+                lb.flush.fill_(i & 0xFF)
             ev0.record(stream)
             lg_dev.copy_(lg_h[j], non_blocking=True)
             x_dev.copy_(x_h[j], non_blocking=True)
-            k3.k3moe_route(s, lg_dev, idx, w, st, stream=stream)
-            k3.k3moe_bucket(s, idx, counts, offsets, perm, inv, wsb, st, stream=stream)
-            k3.k3moe_expert_ffn(s, x_dev, W, offsets, perm, Y, a.mode, wsf, st, stream=stream)
-            k3.k3moe_combine(s, Y, w, inv, out, None, stream=stream)
-            out_h.copy_(out, non_blocking=True)
+            k3.k3moe_route(s, lg_dev, lb.idx, lb.w, lb.st, stream=stream)
+            k3.k3moe_bucket(s, lb.idx, lb.cnt, lb.offsets, lb.perm, lb.inv, lb.wsb, lb.st, stream=stream)
+            k3.k3moe_expert_ffn(s, x_dev, W, lb.offsets, lb.perm, lb.Y, a.mode, lb.wsf, lb.st, stream=stream)
+            k3.k3moe_combine(s, lb.Y, lb.w, lb.inv, lb.out, None, stream=stream)
+            out_h.copy_(lb.out, non_blocking=True)
             ev1.record(stream)
             ev1.synchronize()
             if i >= 3:
@@ -526,26 +665,39 @@ def run_gpu(a):
         e2e = {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": s.T * s.E * 4 + s.T * s.H * 2,
                "d2h_bytes_per_step": s.T * s.H * 2, "steps": n_e2e}
 
+    # ------------------------------------------------------------- the other workloads
+    workloads = None
+    legs = [] if a.legs == "none" or a.experts or a.tokens else LEGS
+    if legs and (s.H, s.I, s.E) != (7168, 2048, 896):
+        legs = []
+    if legs:
+        del lb
+        torch.cuda.empty_cache()
+        workloads = {}
+        cpu_cache = {}
+        for name, mode in legs:
+            ls = gen.CONFIGS[name]
+            Wl = W if ls.E == s.E else k3.Weights.from_stacked(*[t[: ls.E] for t in experts.tensors])
+            key = f"{name}/{mode_name(ls, mode)}"
+            workloads[key] = run_leg(a, name, mode, Wl, dev, ws, clocks, cpu_cache, rank)
+            torch.cuda.empty_cache()
+    time.sleep(0.2)
+    clk = clocks.stop()
+
     cpu = None
     if rank == 0 and not a.no_cpu_baseline:
-        v, sample = oracle_sample(a.config, s, sets, a.cpu_seconds)
+        v, sample = oracle_sample(a.config, s, head_sets, a.cpu_seconds)
         cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample, "host": host_cpu()}
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": a.steps,
                 "warmup": a.warmup, "ms_per_step": tot_ms / a.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "e2m1*bf16->f32",
                 "data": "synthetic", "config": workload_config(a, s),
-                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
-                "gpu_launches": launches_per_step * a.steps,
-                "step_us": {"median": float(np.median(step_ms) * 1e3), "min": float(step_ms.min() * 1e3),
-                            "max": float(step_ms.max() * 1e3)},
-                "phase_us_median": {"route_bucket": float(np.median(rb_ms) * 1e3),
-                                    "expert_ffn": float(np.median(ffn_ms) * 1e3),
-                                    "combine": float(np.median(comb_ms) * 1e3),
-                                    "step_with_phase_events": float(np.median(pstep_ms) * 1e3),
-                                    "note": "a second pass of the same K steps with events around the "
-                                            "expert FFN call; value and step_us come from the first pass"},
-                "wall_s_timed_region": t_wall}
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                "clocks": clk,
+                "gpu_launches": head_launches, "step_us": head_step_us, "phase_us_median": head_phases,
+                "wall_s_timed_region": head_wall, "workloads": workloads,
+                "clocks_all_timed_regions": clocks.window(None, None)}
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()

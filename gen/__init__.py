@@ -12,6 +12,8 @@ Workloads (shapes T tokens, H hidden, I expert intermediate, E experts, k top-k)
 * ``decode``    T=1,    H=7168, I=2048, E=896, k=16, logits N(0, sigma=2)
 * ``batch8``    T=8,    as decode; tokens 0-3 put their 8 largest logits on one
                 seeded set S of 8 experts (in S order), tokens 4-7 are plain
+* ``specN``     N in {2, 4, 12, 16}: the batch8 recipe at T=N (speculative-verify
+                batches); tokens 0..N/2-1 share S, the rest are plain
 * ``prefill``   T=4096, as decode, logits iid N(0,1) (uniform expected load)
 * ``skewed``    T=2048, logits z + 0.5 * ln p_e with p_e proportional to
                 rank(e)^-1.2 over a seeded permutation of the experts
@@ -185,6 +187,10 @@ CONFIGS = {
     "prefill": Shape(4096, 7168, 2048, 896, 16),
     "skewed": Shape(2048, 7168, 2048, 896, 16),
     "decode_i1536": Shape(1, 7168, 1536, 896, 16),
+    "spec2": Shape(2, 7168, 2048, 896, 16),
+    "spec4": Shape(4, 7168, 2048, 896, 16),
+    "spec12": Shape(12, 7168, 2048, 896, 16),
+    "spec16": Shape(16, 7168, 2048, 896, 16),
     "probe": Shape(32768, 7168, 2048, 16, 1),
 }
 
@@ -196,11 +202,11 @@ def make_logits(name: str, s: Shape | None = None, seed: int = INPUT_SEED) -> np
     ls = stream(KIND_LOGITS)
     if name in ("decode", "decode_i1536"):
         return normal_f32(seed, ls, T * E, 2.0).reshape(T, E)
-    if name == "batch8":
+    if name == "batch8" or name.startswith("spec"):
         l = normal_f32(seed, ls, T * E, 2.0).reshape(T, E)
         S = _fisher_yates(E, stream(KIND_AUX, 1), seed, 8)
         rest_pos = np.setdiff1d(np.arange(E), S)  # ascending
-        for t in range(min(4, T)):
+        for t in range(T // 2):
             row = l[t]
             order = np.argsort(-row.astype(np.float64), kind="stable")
             top, rest = order[:8], np.sort(order[8:])

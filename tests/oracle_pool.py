@@ -1,0 +1,81 @@
+"""The float64 oracle over large parity samples, run as N independent
+single-threaded oracle processes.
+
+The processes are started with ``spawn`` (never forked from a process that has
+used the GPU).  Work is split by expert: a task is one routed expert and the
+tokens of the sample routed to it, in the oracle's own bucket order.  Each
+worker draws that expert's MXFP4 weights from the seeded generator (one thread)
+and runs the oracle's expert FFN (``oracle.expert_ffn`` with one expert, k = 1)
+on those tokens, so no process holds more than one expert's weights.  The
+caller assembles the rows into the oracle's bucket order and runs the oracle's
+combine: the arithmetic is the oracle's throughout, only its work is divided.
+"""
+from __future__ import annotations
+
+import multiprocessing as mp
+import os
+
+import numpy as np
+
+import gen
+import oracle
+
+
+def _expert_rows(task):
+    """Y rows (float64 [n, H]) of expert e for the activation rows x_e ([n, H] bf16 bits)."""
+    H, I, e, x_e, a4, seed = task
+    n = x_e.shape[0]
+    arrs = gen.expert_arrays(H, I, e, e + 1, seed=seed, nthreads=1)
+    W = oracle.Weights(1, {0: tuple(z[0] for z in arrs)})
+    s1 = gen.Shape(n, H, I, 1, 1)
+    Y = oracle.expert_ffn(s1, x_e, W, np.array([0, n], np.int32), np.arange(n, dtype=np.int32), a4=a4)
+    return e, Y
+
+
+def workers() -> int:
+    return max(1, min(16, os.cpu_count() or 1))
+
+
+def sample_layer(s, xbits, idx, w, tokens, a4=False, seed=gen.WEIGHT_SEED, nproc=None):
+    """The oracle's layer restricted to the tokens ``tokens`` (sorted token ids).
+
+    Returns (Y', out', inv') for the sub-batch: Y' float64 [n k, H] in the
+    oracle's bucket order of the sub-batch, out' float64 [n, H], and inv' (the
+    position of assignment i k + j of the i-th sampled token in Y')."""
+    tokens = np.asarray(tokens, np.int64)
+    n = len(tokens)
+    sub = gen.Shape(n, s.H, s.I, s.E, s.k)
+    idx_s = np.ascontiguousarray(idx[tokens], np.int32)
+    w_s = np.ascontiguousarray(w[tokens], np.float64)
+    counts, offsets, perm, inv = oracle.bucket(sub, idx_s)
+    tasks = []
+    for e in np.flatnonzero(counts):
+        p0, p1 = int(offsets[e]), int(offsets[e + 1])
+        rows = tokens[perm[p0:p1] // s.k]
+        tasks.append((s.H, s.I, int(e), np.ascontiguousarray(xbits[rows]), bool(a4), seed))
+    tasks.sort(key=lambda t: -t[3].shape[0])  # longest first
+    Y = np.zeros((n * s.k, s.H), np.float64)
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(nproc or workers()) as pool:
+        for e, rows in pool.imap_unordered(_expert_rows, tasks):
+            Y[offsets[e]:offsets[e + 1]] = rows
+    out, _ = oracle.combine(sub, Y, w_s, inv)
+    return Y, out, inv
+
+
+def hot_expert_sample(s, counts, offsets, perm, n_hot=32, tile=128, total=256, rng_seed=123):
+    """Token ids covering every 128-token tile of the n_hot most loaded experts
+    (the first position of each tile and the expert's last bucket position),
+    the first and the last token, and seeded random tokens up to ``total``."""
+    hot = np.argsort(-counts, kind="stable")[:n_hot]
+    pick = {0, s.T - 1}
+    for e in hot:
+        p0, p1 = int(offsets[e]), int(offsets[e + 1])
+        if p1 <= p0:
+            continue
+        for p in list(range(p0, p1, tile)) + [p1 - 1]:
+            pick.add(int(perm[p] // s.k))
+    rng = np.random.default_rng(rng_seed)
+    while len(pick) < min(total, s.T):
+        pick.add(int(rng.integers(0, s.T)))
+    return np.array(sorted(pick), np.int64), hot

@@ -88,3 +88,35 @@ def test_traffic_record_follows_the_sources(bench, tmp_path, monkeypatch):
 def test_host_cpu_is_described(bench):
     h = bench.host_cpu()
     assert h["nproc"] >= 1 and h["oracle_threads"] == 1 and isinstance(h["model"], str) and h["model"]
+
+
+def test_ffn_bytes_and_per_expert_roofline(bench, monkeypatch):
+    monkeypatch.setattr(bench, "measured_peaks", lambda: {"hbm_gbs": 8000.0, "bf16_tflops": 2000.0})
+    s = gen.CONFIGS["decode"]
+    A = s.T * s.k
+    assert bench.ffn_bytes_per_call(s, 16) == 16 * 23_396_352 + 7168 * 2 + A * 2048 * 4 + A * 7168 * 4
+    counts = np.zeros(s.E, np.int64)
+    counts[:16] = 1
+    # CUDA-core GEMV: the HBM term alone, expert by expert, plus x, h and Y
+    t = bench.per_expert_roofline_s(s, counts, 1)
+    assert t == pytest.approx(bench.ffn_bytes_per_call(s, 16) / 8e12)
+    # a compute-bound expert on the FP4 tensor core: n * 6 H I / (6 x bf16 peak)
+    p = gen.CONFIGS["probe"]
+    cp = np.zeros(p.E, np.int64)
+    cp[:] = 2048
+    t4 = bench.per_expert_roofline_s(p, cp, 4)
+    extra = (p.T * p.H * 2 + p.T * p.I * 4 + p.T * p.H * 4) / 8e12
+    assert t4 == pytest.approx(16 * max(23_396_352 / 8e12, 2048 * 6.0 * 7168 * 2048 / 12e15) + extra)
+    t3 = bench.per_expert_roofline_s(p, cp, 3)
+    assert t3 == pytest.approx(16 * 2048 * 6.0 * 7168 * 2048 / 2e15 + extra)
+
+
+def test_extra_workloads_cover_the_configs_and_modes(bench):
+    names = {n for n, _ in bench.LEGS}
+    assert {"batch8", "prefill", "skewed", "probe", "spec2", "spec4", "spec12", "spec16"} <= names
+    for n in ("prefill", "skewed"):
+        modes = {bench.mode_name(gen.CONFIGS[n], m) for nn, m in bench.LEGS if nn == n}
+        assert modes == {"gemm_w4a16", "w4a4"}
+    for n in ("batch8", "spec2", "spec4", "spec12", "spec16"):
+        modes = {bench.mode_name(gen.CONFIGS[n], m) for nn, m in bench.LEGS if nn == n}
+        assert modes == {"gemv", "gemm_w4a16"}

@@ -1,11 +1,14 @@
 """GPU parity on the full-size workloads (896 experts, H=7168, I=2048; 21 GB of
 MXFP4 weights resident), in the launch configuration the benchmark times.
 
-Decode (T=1), the 8-token batch and the I=1536 decode layer are checked in
-full against the oracle.  For the 4096- and 2048-token prefill workloads the
-routing and bucketing are checked bit-exactly on every token, and the outputs
-of a sample of tokens (covering the most loaded experts, the first and the
-last token) are checked against the oracle's per-token path."""
+Decode (T=1), the 8-token batch (through the GEMV and the tensor-core GEMM
+modes, each against the same oracle), the speculative-verify batches of 2 to 16
+tokens and the I=1536 decode layer are checked in full against the oracle.
+For the 4096- and 2048-token prefill workloads the routing and bucketing are
+checked bit-exactly on every token; the outputs of at least 256 tokens --
+covering every 64-position span of the 32 most loaded experts' buckets and
+their last positions, the first and the last token -- are checked against the
+oracle, both the combined rows and every one of their expert output rows Y.""")
 import numpy as np
 import pytest
 import torch
@@ -14,6 +17,7 @@ import gen
 import oracle
 from gen.device import DeviceExperts, device_inputs
 from layer_run import alloc_layer, bf16_rne_bits_of, host, max_rel_err, run_layer
+from oracle_pool import hot_expert_sample, sample_layer
 import mxfp4_expert_ffn_router_gb300 as k3
 
 pytestmark = pytest.mark.gpu
@@ -32,14 +36,6 @@ def _weights(dx):
     return k3.Weights.from_stacked(*dx.tensors)
 
 
-def _host_experts(s, ids):
-    out = {}
-    for e in ids:
-        a, b, c, d = gen.expert_arrays(s.H, s.I, int(e), int(e) + 1)
-        out[int(e)] = (a[0], b[0], c[0], d[0])
-    return oracle.Weights(s.E, out)
-
-
 def _route_bucket_exact(s, logits, r):
     idx, w, _ = oracle.route(s, logits)
     np.testing.assert_array_equal(r["idx"], idx)
@@ -51,14 +47,15 @@ def _route_bucket_exact(s, logits, r):
 
 
 def _full(name, dx, s=None, mode=k3.K3MOE_FFN_AUTO):
+    """The whole layer against the oracle; the oracle's FFN runs as parallel
+    single-threaded processes (one task per routed expert) over all tokens."""
     s = s or gen.CONFIGS[name]
     lg, xd, logits, xbits = device_inputs(name, s)
     r = host(run_layer(s, lg, xd, _weights(dx), bufs=alloc_layer(s, mode=mode), mode=mode))
     assert r["status"][0] == 0
     idx, w, counts, offsets, perm, inv = _route_bucket_exact(s, logits, r)
-    W = _host_experts(s, np.unique(idx))
-    Y = oracle.expert_ffn(s, xbits, W, offsets, perm)
-    out, _ = oracle.combine(s, Y, w, inv)
+    Y, out, inv_s = sample_layer(s, xbits, idx, w, np.arange(s.T))
+    np.testing.assert_array_equal(inv_s, inv)  # all tokens: the oracle's own bucket order
     assert max_rel_err(r["Y"], Y) <= TOL
     assert max_rel_err(r["out_f32"], out) <= TOL
     np.testing.assert_array_equal(r["out"], bf16_rne_bits_of(r["out_f32"]))
@@ -71,11 +68,40 @@ def test_decode(experts_2048, mode):
     assert len(np.unique(r["idx"])) == 16
 
 
-def test_batch8_shared_experts(experts_2048):
-    r = _full("batch8", experts_2048)
+@pytest.mark.parametrize("mode", [k3.K3MOE_FFN_GEMV, k3.K3MOE_FFN_GEMM])
+def test_batch8_gemv_and_gemm_against_one_oracle(experts_2048, mode):
+    """The per-token (GEMV) and batched (tensor-core GEMM) paths each agree with the
+    same oracle on the 8-token batch; the chunk-union prefill of the kimi-k3-in-c
+    CHANGELOG ("[1.0.0] Added") requires the batched path to give the per-token
+    path's tokens."""
+    r = _full("batch8", experts_2048, mode=mode)
     shared = set(r["idx"][0, :8].tolist())
     for t in range(1, 4):
         assert set(r["idx"][t, :8].tolist()) == shared
+
+
+def test_batch8_modes_close_to_each_other(experts_2048):
+    s = gen.CONFIGS["batch8"]
+    lg, xd, _, _ = device_inputs("batch8", s)
+    outs = {}
+    for mode in (k3.K3MOE_FFN_GEMV, k3.K3MOE_FFN_GEMM):
+        r = host(run_layer(s, lg, xd, _weights(experts_2048), bufs=alloc_layer(s, mode=mode), mode=mode))
+        assert r["status"][0] == 0
+        outs[mode] = r["out_f32"]
+    assert max_rel_err(outs[k3.K3MOE_FFN_GEMV], outs[k3.K3MOE_FFN_GEMM].astype(np.float64)) <= TOL
+
+
+@pytest.mark.parametrize("T", [2, 4, 12, 16])
+@pytest.mark.parametrize("mode", [k3.K3MOE_FFN_GEMV, k3.K3MOE_FFN_GEMM])
+def test_spec_verify_batches(experts_2048, T, mode):
+    """Speculative-verify batches ("--spec N" of the kimi-k3-in-c CHANGELOG, block
+    "[1.0.0] Added"): T tokens, half of them sharing 8 of their top-16 experts."""
+    name = f"spec{T}"
+    r = _full(name, experts_2048, mode=mode)
+    if T >= 4:
+        shared = set(r["idx"][0, :8].tolist())
+        for t in range(1, T // 2):
+            assert set(r["idx"][t, :8].tolist()) == shared
 
 
 def test_decode_i1536():
@@ -86,23 +112,26 @@ def test_decode_i1536():
 @pytest.mark.parametrize("name,mode", [("prefill", k3.K3MOE_FFN_AUTO), ("skewed", k3.K3MOE_FFN_AUTO),
                                        ("prefill", k3.K3MOE_FFN_W4A4), ("skewed", k3.K3MOE_FFN_W4A4)])
 def test_prefill_sampled(experts_2048, name, mode):
-    """W4A4 runs the persistent block-scaled GEMM at about 94 (gate/up) and 165
-    (down) tiles per CTA here; its sample is checked against the oracle's A4 path."""
+    """AUTO takes the W4A16 tensor-core GEMM here; W4A4 takes the block-scaled FP4
+    GEMM and is checked against the oracle's A4 path.  The sample covers every
+    token tile of the 32 most loaded experts (the hottest skewed expert has
+    about 1,640 tokens, 13 tiles of 128)."""
     s = gen.CONFIGS[name]
     lg, xd, logits, xbits = device_inputs(name, s)
     r = host(run_layer(s, lg, xd, _weights(experts_2048), bufs=alloc_layer(s, mode=mode), mode=mode))
     assert r["status"][0] == 0
     idx, w, counts, offsets, perm, inv = _route_bucket_exact(s, logits, r)
     np.testing.assert_array_equal(r["out"], bf16_rne_bits_of(r["out_f32"]))
-    hot = np.argsort(-counts, kind="stable")[:3]
-    sample = {0, s.T - 1}
-    for e in hot:
-        sample.add(int(perm[offsets[e]] // s.k))
-    rng = np.random.default_rng(123)
-    sample |= set(int(t) for t in rng.integers(0, s.T, 3))
-    sample = sorted(sample)
-    W = _host_experts(s, np.unique(idx[sample]))
+    sample, hot = hot_expert_sample(s, counts, offsets, perm, n_hot=32, tile=64, total=256)
+    assert len(sample) >= 256
+    for e in hot:  # the last bucket position of every hot expert is in the sample
+        assert perm[offsets[e + 1] - 1] // s.k in set(sample.tolist())
     a4 = mode == k3.K3MOE_FFN_W4A4
-    ref = np.stack([oracle.moe_token(s, xbits[t], idx[t], w[t], W, a4=a4) for t in sample])
-    got = r["out_f32"][sample]
-    assert max_rel_err(got, ref) <= TOL, max_rel_err(got, ref)
+    Yref, outref, inv_s = sample_layer(s, xbits, idx, w, sample, a4=a4)
+    got_out = r["out_f32"][sample]
+    assert max_rel_err(got_out, outref) <= TOL, max_rel_err(got_out, outref)
+    # every expert output row of the sampled tokens, at its bucket position
+    a_ids = (sample[:, None] * s.k + np.arange(s.k)[None, :]).ravel()
+    got_Y = r["Y"][inv[a_ids]]
+    ref_Y = Yref[inv_s[np.arange(len(sample) * s.k)]]
+    assert max_rel_err(got_Y, ref_Y) <= TOL, max_rel_err(got_Y, ref_Y)
