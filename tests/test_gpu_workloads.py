@@ -8,7 +8,7 @@ For the 4096- and 2048-token prefill workloads the routing and bucketing are
 checked bit-exactly on every token; the outputs of at least 256 tokens --
 covering every 64-position span of the 32 most loaded experts' buckets and
 their last positions, the first and the last token -- are checked against the
-oracle, both the combined rows and every one of their expert output rows Y.""")
+oracle, both the combined rows and every one of their expert output rows Y."""
 import numpy as np
 import pytest
 import torch
