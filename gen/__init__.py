@@ -20,6 +20,8 @@ Workloads (shapes T tokens, H hidden, I expert intermediate, E experts, k top-k)
 * ``decode_i1536`` the decode layer with I=1536
 * ``probe``     E=16, k=1, T=32768, each expert receives exactly 2048 tokens
 
+Router matrix (for the router entry point): bf16 [E, H], N(0, 2/sqrt(H)).
+
 MXFP4 weights: code bytes uniform (both nibbles uniform over 0..15), e8m0 scale
 bytes uniform over {119..123}, i.e. block scales 2^-8 .. 2^-4.  Activations x
 are N(0,1) rounded to bf16.  Seeds: 0 for weights, 1 for activations and logits.
@@ -40,7 +42,7 @@ _lock = threading.Lock()
 _lib = None
 
 KIND_W13_CODES, KIND_W13_SCALES, KIND_W2_CODES, KIND_W2_SCALES = 1, 2, 3, 4
-KIND_X, KIND_LOGITS, KIND_AUX = 5, 6, 7
+KIND_X, KIND_LOGITS, KIND_AUX, KIND_ROUTER = 5, 6, 7, 8
 WEIGHT_SEED, INPUT_SEED = 0, 1
 SCALE_LO, SCALE_HI = 119, 123
 
@@ -229,6 +231,13 @@ def make_logits(name: str, s: Shape | None = None, seed: int = INPUT_SEED) -> np
         z[t, t % E] = 8.0 + np.abs(z[t, t % E])
         return z
     return normal_f32(seed, ls, T * E, 1.0).reshape(T, E)
+
+
+def make_router(s: Shape, seed: int = WEIGHT_SEED) -> np.ndarray:
+    """Router matrix as bf16 bit patterns, uint16 [E, H] (row e scores expert e),
+    N(0, sigma = 2 / sqrt(H)): with x ~ N(0, 1) the scores have standard
+    deviation 2, the decode workload's logit distribution."""
+    return normal_bf16_bits(seed, stream(KIND_ROUTER), s.E * s.H, 2.0 / np.sqrt(s.H)).reshape(s.E, s.H)
 
 
 def make_x(s: Shape, seed: int = INPUT_SEED) -> np.ndarray:

@@ -69,6 +69,10 @@ def lib():
             L.k3ref_combine.argtypes = [Shape, vp, vp, vp, vp, vp]
             L.k3ref_moe_token.restype = i32
             L.k3ref_moe_token.argtypes = [Shape, vp, vp, vp, vp, vp, vp, vp, i32, vp]
+            L.k3ref_router_logits.restype = i32
+            L.k3ref_router_logits.argtypes = [Shape, vp, vp, vp]
+            L.k3ref_router.restype = i32
+            L.k3ref_router.argtypes = [Shape, vp, vp, vp, vp, vp, vp, vp]
             L.k3ref_moe_layer.restype = i32
             L.k3ref_moe_layer.argtypes = [Shape, vp, vp, vp, vp, vp, vp, i32, vp, vp]
             _lib = L
@@ -142,6 +146,32 @@ def route(s, logits: np.ndarray):
     if n < 0:
         raise ValueError("k3ref_route: bad shape")
     return idx, w, bad
+
+
+def router_logits(s, x_bits: np.ndarray, wr_bits: np.ndarray) -> np.ndarray:
+    """float64 [T, E]: x [T, H] (bf16 bits) times the router rows wr [E, H] (bf16 bits)."""
+    x = _c(x_bits, np.uint16)
+    wr = _c(wr_bits, np.uint16)
+    out = np.zeros((s.T, s.E), np.float64)
+    if lib().k3ref_router_logits(_shape(s), x.ctypes.data, wr.ctypes.data, out.ctypes.data) != 0:
+        raise ValueError("k3ref_router_logits: bad shape")
+    return out
+
+
+def router(s, x_bits: np.ndarray, wr_bits: np.ndarray):
+    """Router then route: (logits float64, logits float32, idx, w, row_bad)."""
+    x = _c(x_bits, np.uint16)
+    wr = _c(wr_bits, np.uint16)
+    l64 = np.zeros((s.T, s.E), np.float64)
+    l32 = np.zeros((s.T, s.E), np.float32)
+    idx = np.zeros((s.T, s.k), np.int32)
+    w = np.zeros((s.T, s.k), np.float64)
+    bad = np.zeros(s.T, np.int32)
+    n = lib().k3ref_router(_shape(s), x.ctypes.data, wr.ctypes.data, l64.ctypes.data, l32.ctypes.data,
+                           idx.ctypes.data, w.ctypes.data, bad.ctypes.data)
+    if n < 0:
+        raise ValueError("k3ref_router: bad shape")
+    return l64, l32, idx, w, bad
 
 
 def bucket(s, idx: np.ndarray):

@@ -160,6 +160,45 @@ int k3ref_route(k3ref_shape s, const float *logits, int32_t *idx, double *w, int
   return nbad;
 }
 
+/* ---- router: the score of every expert for every token, the input of the
+ * top-16-of-896 selection ([changelog] "[0.1.0] Added"; [article] "01").  The
+ * score is the linear form x . wr[e]; bf16 products are exact in double and
+ * the sum runs in ascending h. ---- */
+int k3ref_router_logits(k3ref_shape s, const uint16_t *x, const uint16_t *wr, double *logits) {
+  if (!shape_ok(s)) return -1;
+  double *xv = (double *)malloc(sizeof(double) * (size_t)s.H);
+  if (!xv) return -1;
+  for (int t = 0; t < s.T; ++t) {
+    for (int h = 0; h < s.H; ++h) xv[h] = k3ref_bf16_value(x[(size_t)t * s.H + h]);
+    for (int e = 0; e < s.E; ++e) {
+      const uint16_t *row = wr + (size_t)e * s.H;
+      double acc = 0.0;
+      for (int h = 0; h < s.H; ++h) acc += xv[h] * k3ref_bf16_value(row[h]);
+      logits[(size_t)t * s.E + e] = acc;
+    }
+  }
+  free(xv);
+  return 0;
+}
+
+int k3ref_router(k3ref_shape s, const uint16_t *x, const uint16_t *wr, double *logits, float *logits_f32,
+                 int32_t *idx, double *w, int32_t *row_bad) {
+  if (!shape_ok(s)) return -1;
+  const size_t n = (size_t)s.T * s.E;
+  double *l64 = (double *)malloc(sizeof(double) * (n ? n : 1));
+  float *l32 = (float *)malloc(sizeof(float) * (n ? n : 1));
+  int rc = -1;
+  if (l64 && l32 && k3ref_router_logits(s, x, wr, l64) == 0) {
+    for (size_t i = 0; i < n; ++i) l32[i] = (float)l64[i]; /* one rounding, to nearest even */
+    rc = k3ref_route(s, l32, idx, w, row_bad);
+    if (logits) memcpy(logits, l64, sizeof(double) * n);
+    if (logits_f32) memcpy(logits_f32, l32, sizeof(float) * n);
+  }
+  free(l64);
+  free(l32);
+  return rc;
+}
+
 /* ---- bucketing: a stable counting sort of assignment ids a = t*k + j by the
  * routed expert idx[a] ([changelog] "[1.0.0] Added", chunk-union prefill: the
  * tokens of a chunk are grouped by routed expert so each unique expert is read

@@ -39,6 +39,10 @@
  *    I..2I-1 up), w2 = [H][I/2]; low nibble = even column; scales [rows][K/32].
  *  - an expert whose four pointers are not all non-NULL is absent: its rows of
  *    Y (and h) are zero.
+ *  - router: the pages name the selection (16 of 896 experts per token) but not
+ *    the score; the score of expert e is read as the linear form x . wr[e]
+ *    of the token's bf16 hidden state with a bf16 router row, and the route
+ *    selects on those scores rounded once to fp32.
  *  - W4A4 mode ("a4"): x and h are quantised to MXFP4 by the [OCP-MX] rule
  *    (round-to-nearest-even on the E2M1 grid, saturate at 6, all-zero block ->
  *    scale byte 0, code sign bit set iff the value is < 0) before the dot
@@ -89,6 +93,18 @@ int k3ref_combine(k3ref_shape s, const double *Y, const double *w, const int32_t
 int k3ref_moe_token(k3ref_shape s, const uint16_t *x_row, const int32_t *idx_row,
                     const double *w_row, const uint8_t *const *w13c, const uint8_t *const *w13s,
                     const uint8_t *const *w2c, const uint8_t *const *w2s, int a4, double *out_row);
+
+/* ---- router (the step before routing): one linear score per expert ----
+ * logits[t][e] = sum_h x[t][h] * wr[e][h] over bf16 x [T][H] and the bf16
+ * router matrix wr [E][H] (row e scores expert e); products and sum in double.
+ * Returns 0 or -1. */
+int k3ref_router_logits(k3ref_shape s, const uint16_t *x, const uint16_t *wr, double *logits);
+/* Router then route: the double logits rounded once to float (round to nearest
+ * even) are the fp32 logits that the route selects on; idx, w and row_bad as in
+ * k3ref_route.  logits (double [T][E]) and logits_f32 may be NULL.  Returns
+ * k3ref_route's value, or -1. */
+int k3ref_router(k3ref_shape s, const uint16_t *x, const uint16_t *wr, double *logits, float *logits_f32,
+                 int32_t *idx, double *w, int32_t *row_bad);
 
 /* ---- whole layer: route, bucket, FFN, combine (scratch allocated with malloc) ---- */
 int k3ref_moe_layer(k3ref_shape s, const float *logits, const uint16_t *x,

@@ -404,3 +404,64 @@ def test_expert_bytes_reproduce_pages_totals():
     assert round(be * p["expert_weight_sets"] / 1e12, 2) == p["expert_weights_total_tb"]
     assert p["expert_weight_sets"] == p["moe_layers"] * p["experts_per_layer"]
     assert abs(be / (3 * 7168 * 1536) - p["bytes_per_param_nominal"]) < 0.04
+
+
+# ----------------------------------------------------------------------------- router
+def _bf16_f64(bits):
+    """bf16 bit patterns -> float64 through torch (a library decode, not the oracle's)."""
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(
+        torch.float64).numpy()
+
+
+@pytest.mark.parametrize("T,H,E", [(3, 128, 8), (5, 512, 40), (2, 7168, 16)])
+def test_router_logits_match_library_matmul(T, H, E):
+    """The router scores against numpy's float64 matrix product of the library-
+    decoded bf16 operands (a different summation order: agreement to 1e-13 of
+    the sum of |products|)."""
+    s = gen.Shape(T, H, 64, E, 1)
+    x = gen.normal_bf16_bits(11, gen.stream(gen.KIND_X), T * H).reshape(T, H)
+    wr = gen.make_router(s)
+    got = oracle.router_logits(s, x, wr)
+    xv, wv = _bf16_f64(x), _bf16_f64(wr)
+    ref = xv @ wv.T
+    mag = np.abs(xv) @ np.abs(wv).T
+    assert np.all(np.abs(got - ref) <= 1e-13 * mag)
+    assert got.shape == (T, E)
+
+
+def test_router_logits_exact_on_integers_and_one_hot():
+    """Small integers are exact in bf16 and their products and sums exact in
+    double: the scores equal numpy's int64 product bit for bit.  A one-hot token
+    picks one column of the router matrix (catches a transposed operand)."""
+    rng = np.random.default_rng(3)
+    T, H, E = 4, 256, 24
+    s = gen.Shape(T, H, 64, E, 1)
+    xi = rng.integers(-15, 16, (T, H))
+    wi = rng.integers(-15, 16, (E, H))
+    as_bits = lambda a: (np.asarray(a, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    got = oracle.router_logits(s, as_bits(xi), as_bits(wi))
+    np.testing.assert_array_equal(got, (xi @ wi.T).astype(np.float64))
+    oh = np.zeros((T, H))
+    cols = [0, 7, 100, 255]
+    for t, c in enumerate(cols):
+        oh[t, c] = 1.0
+    got = oracle.router_logits(s, as_bits(oh), as_bits(wi))
+    np.testing.assert_array_equal(got, wi[:, cols].T.astype(np.float64))
+
+
+def test_router_routes_on_the_fp32_rounding_of_its_scores():
+    """Router then route = the route (itself pinned by brute force) applied to the
+    scores rounded once to float32 by numpy."""
+    s = gen.Shape(6, 512, 64, 96, 16)
+    x = gen.normal_bf16_bits(12, gen.stream(gen.KIND_X), s.T * s.H).reshape(s.T, s.H)
+    wr = gen.make_router(s)
+    l64, l32, idx, w, bad = oracle.router(s, x, wr)
+    np.testing.assert_array_equal(l64, oracle.router_logits(s, x, wr))
+    np.testing.assert_array_equal(l32, l64.astype(np.float32))
+    idx2, w2, _ = oracle.route(s, l64.astype(np.float32))
+    np.testing.assert_array_equal(idx, idx2)
+    np.testing.assert_array_equal(w, w2)
+    assert not bad.any()
+    # scores have the decode workload's spread (standard deviation about 2)
+    assert 1.5 < float(np.std(l64)) < 2.5
