@@ -65,6 +65,10 @@ def lib():
             L.k3ref_bucket.argtypes = [Shape, vp, vp, vp, vp, vp]
             L.k3ref_expert_ffn.restype = i32
             L.k3ref_expert_ffn.argtypes = [Shape, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp]
+            L.k3ref_expert_gateup.restype = i32
+            L.k3ref_expert_gateup.argtypes = [Shape, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp]
+            L.k3ref_expert_down.restype = i32
+            L.k3ref_expert_down.argtypes = [Shape, vp, vp, vp, vp, vp, vp, i32, vp]
             L.k3ref_combine.restype = i32
             L.k3ref_combine.argtypes = [Shape, vp, vp, vp, vp, vp]
             L.k3ref_moe_token.restype = i32
@@ -200,6 +204,32 @@ def expert_ffn(s, x_bits: np.ndarray, weights: Weights, offsets: np.ndarray, per
     if rc != 0:
         raise ValueError("k3ref_expert_ffn: bad arguments")
     return (Y, h) if want_h else Y
+
+
+def expert_gateup(s, x_bits: np.ndarray, weights: Weights, offsets: np.ndarray, perm: np.ndarray,
+                  a4: bool = False):
+    """(hpre float64 [A, I], h bf16 bits uint16 [A, I]) in bucket order."""
+    x = _c(x_bits, np.uint16)
+    o = _c(offsets, np.int32)
+    p = _c(perm, np.int32)
+    A = s.T * s.k
+    hpre = np.zeros((A, s.I), np.float64)
+    h = np.zeros((A, s.I), np.uint16)
+    if lib().k3ref_expert_gateup(_shape(s), x.ctypes.data, *weights.args(), o.ctypes.data, p.ctypes.data,
+                                 int(a4), hpre.ctypes.data, h.ctypes.data) != 0:
+        raise ValueError("k3ref_expert_gateup: bad arguments")
+    return hpre, h
+
+
+def expert_down(s, h_bits: np.ndarray, weights: Weights, offsets: np.ndarray, a4: bool = False):
+    """Y float64 [A, H] = W2 h for the given bf16 h rows [A, I] in bucket order."""
+    h = _c(h_bits, np.uint16)
+    o = _c(offsets, np.int32)
+    Y = np.zeros((s.T * s.k, s.H), np.float64)
+    if lib().k3ref_expert_down(_shape(s), h.ctypes.data, *weights.args(), o.ctypes.data, int(a4),
+                               Y.ctypes.data) != 0:
+        raise ValueError("k3ref_expert_down: bad arguments")
+    return Y
 
 
 def combine(s, Y: np.ndarray, w: np.ndarray, inv: np.ndarray):

@@ -269,14 +269,13 @@ static int expert_present(int e, const uint8_t *const *w13c, const uint8_t *cons
   return w13c[e] && w13s[e] && w2c[e] && w2s[e];
 }
 
-/* One expert FFN on one token: g = Wg x, u = Wu x, h = bf16(silu(g) u),
- * y = W2 h ([changelog] "[0.1.0] Added": GLU expert with MXFP4 weights). */
-static void expert_apply(k3ref_shape s, const double *xv, const uint8_t *w13c,
-                         const uint8_t *w13s, const uint8_t *w2c, const uint8_t *w2s, int a4,
-                         uint16_t *h_bits, double *hv, double *y) {
-  const int K = s.H > s.I ? s.H : s.I;
-  double *wg = (double *)malloc(sizeof(double) * (size_t)K);
-  double *wu = (double *)malloc(sizeof(double) * (size_t)K);
+/* Gate/up half of one expert on one token: g = Wg x, u = Wu x, hpre = silu(g) u
+ * in double, h = bf16(hpre) ([changelog] "[0.1.0] Added": GLU expert with MXFP4
+ * weights).  hpre may be NULL. */
+static void expert_gateup(k3ref_shape s, const double *xv, const uint8_t *w13c, const uint8_t *w13s,
+                          uint16_t *h_bits, double *hpre) {
+  double *wg = (double *)malloc(sizeof(double) * (size_t)s.H);
+  double *wu = (double *)malloc(sizeof(double) * (size_t)s.H);
   for (int r = 0; r < s.I; ++r) {
     mx_row(w13c, w13s, s.H, r, wg);        /* gate row r */
     mx_row(w13c, w13s, s.H, s.I + r, wu);  /* up row r   */
@@ -285,17 +284,82 @@ static void expert_apply(k3ref_shape s, const double *xv, const uint8_t *w13c,
       g += wg[c] * xv[c];
       u += wu[c] * xv[c];
     }
-    h_bits[r] = k3ref_bf16_rne(k3ref_silu(g) * u);
-  }
-  activation_values(h_bits, s.I, a4, hv);
-  for (int r = 0; r < s.H; ++r) {
-    mx_row(w2c, w2s, s.I, r, wg);
-    double acc = 0.0;
-    for (int c = 0; c < s.I; ++c) acc += wg[c] * hv[c];
-    y[r] = acc;
+    const double v = k3ref_silu(g) * u;
+    if (hpre) hpre[r] = v;
+    h_bits[r] = k3ref_bf16_rne(v);
   }
   free(wg);
   free(wu);
+}
+
+/* Down half: y = W2 h, with h the bf16 row (quantised to MXFP4 first with a4). */
+static void expert_down(k3ref_shape s, const uint16_t *h_bits, const uint8_t *w2c, const uint8_t *w2s, int a4,
+                        double *hv, double *y) {
+  double *wd = (double *)malloc(sizeof(double) * (size_t)s.I);
+  activation_values(h_bits, s.I, a4, hv);
+  for (int r = 0; r < s.H; ++r) {
+    mx_row(w2c, w2s, s.I, r, wd);
+    double acc = 0.0;
+    for (int c = 0; c < s.I; ++c) acc += wd[c] * hv[c];
+    y[r] = acc;
+  }
+  free(wd);
+}
+
+/* One expert FFN on one token: the gate/up half, then the down half on its h. */
+static void expert_apply(k3ref_shape s, const double *xv, const uint8_t *w13c,
+                         const uint8_t *w13s, const uint8_t *w2c, const uint8_t *w2s, int a4,
+                         uint16_t *h_bits, double *hv, double *y) {
+  expert_gateup(s, xv, w13c, w13s, h_bits, NULL);
+  expert_down(s, h_bits, w2c, w2s, a4, hv, y);
+}
+
+int k3ref_expert_gateup(k3ref_shape s, const uint16_t *x, const uint8_t *const *w13c,
+                        const uint8_t *const *w13s, const uint8_t *const *w2c,
+                        const uint8_t *const *w2s, const int32_t *offsets, const int32_t *perm,
+                        int a4, double *hpre, uint16_t *h) {
+  if (!shape_ok(s)) return -1;
+  double *xv = (double *)malloc(sizeof(double) * (size_t)s.H);
+  if (!xv) return -1;
+  for (int e = 0; e < s.E; ++e) {
+    const int present = expert_present(e, w13c, w13s, w2c, w2s);
+    for (int p = offsets[e]; p < offsets[e + 1]; ++p) {
+      double *hp = hpre + (size_t)p * s.I;
+      uint16_t *hb = h + (size_t)p * s.I;
+      if (!present) { /* [changelog] "[Unreleased] Fixed": a missing expert adds zero */
+        for (int i = 0; i < s.I; ++i) {
+          hp[i] = 0.0;
+          hb[i] = 0;
+        }
+        continue;
+      }
+      activation_values(x + (size_t)(perm[p] / s.k) * s.H, s.H, a4, xv);
+      expert_gateup(s, xv, w13c[e], w13s[e], hb, hp);
+    }
+  }
+  free(xv);
+  return 0;
+}
+
+int k3ref_expert_down(k3ref_shape s, const uint16_t *h, const uint8_t *const *w13c,
+                      const uint8_t *const *w13s, const uint8_t *const *w2c,
+                      const uint8_t *const *w2s, const int32_t *offsets, int a4, double *Y) {
+  if (!shape_ok(s)) return -1;
+  double *hv = (double *)malloc(sizeof(double) * (size_t)s.I);
+  if (!hv) return -1;
+  for (int e = 0; e < s.E; ++e) {
+    const int present = expert_present(e, w13c, w13s, w2c, w2s);
+    for (int p = offsets[e]; p < offsets[e + 1]; ++p) {
+      double *y = Y + (size_t)p * s.H;
+      if (!present) {
+        for (int r = 0; r < s.H; ++r) y[r] = 0.0;
+        continue;
+      }
+      expert_down(s, h + (size_t)p * s.I, w2c[e], w2s[e], a4, hv, y);
+    }
+  }
+  free(hv);
+  return 0;
 }
 
 int k3ref_expert_ffn(k3ref_shape s, const uint16_t *x, const uint8_t *const *w13c,

@@ -84,6 +84,19 @@ int k3ref_expert_ffn(k3ref_shape s, const uint16_t *x, const uint8_t *const *w13
                      const uint8_t *const *w13s, const uint8_t *const *w2c,
                      const uint8_t *const *w2s, const int32_t *offsets, const int32_t *perm,
                      int a4, double *Y, uint16_t *h_out);
+/* The two halves of k3moe_ref_expert_ffn, for checking a path that takes the
+ * bf16 rounding of h as its own decision: hpre[A][I] = silu(g) u in double and
+ * h[A][I] = its bf16 rounding, in bucket order; and Y[A][H] = W2 h for given
+ * bf16 h rows in bucket order (a4: each h row quantised to MXFP4 first).  An
+ * absent expert gives zero rows.  expert_ffn = gateup, then down on its h.
+ * Return 0 or -1. */
+int k3ref_expert_gateup(k3ref_shape s, const uint16_t *x, const uint8_t *const *w13c,
+                        const uint8_t *const *w13s, const uint8_t *const *w2c,
+                        const uint8_t *const *w2s, const int32_t *offsets, const int32_t *perm,
+                        int a4, double *hpre, uint16_t *h);
+int k3ref_expert_down(k3ref_shape s, const uint16_t *h, const uint8_t *const *w13c,
+                      const uint8_t *const *w13s, const uint8_t *const *w2c,
+                      const uint8_t *const *w2s, const int32_t *offsets, int a4, double *Y);
 /* out[T][H] = sum_j w[t][j] * Y[inv[t*k+j]] in j order; out_bf16 may be NULL. */
 int k3ref_combine(k3ref_shape s, const double *Y, const double *w, const int32_t *inv, double *out,
                   uint16_t *out_bf16);

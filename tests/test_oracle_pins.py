@@ -465,3 +465,35 @@ def test_router_routes_on_the_fp32_rounding_of_its_scores():
     assert not bad.any()
     # scores have the decode workload's spread (standard deviation about 2)
     assert 1.5 < float(np.std(l64)) < 2.5
+
+
+# ----------------------------------------------------------------------------- FFN halves
+@pytest.mark.parametrize("a4", [False, True])
+def test_ffn_halves_compose_to_the_ffn_and_match_dense_math(a4):
+    """gate/up then down on its own h is bitwise the oracle's expert FFN; hpre is
+    silu(g) u from dense dequantised matrices (golden E2M1 table, library silu)
+    to 1e-12 and h its bf16 rounding; down on arbitrary bf16 rows is the dense
+    product W2 h (A4: of the h row's MXFP4 values)."""
+    s, logits, xbits, experts = _tiny_case(5, 128, 64, 6, 2, 11)
+    W = oracle.Weights(s.E, experts)
+    idx, w, _ = oracle.route(s, logits)
+    counts, offsets, perm, inv = oracle.bucket(s, idx)
+    Y, h_ffn = oracle.expert_ffn(s, xbits, W, offsets, perm, a4=a4, want_h=True)
+    hpre, h = oracle.expert_gateup(s, xbits, W, offsets, perm, a4=a4)
+    np.testing.assert_array_equal(h, h_ffn)
+    np.testing.assert_array_equal(oracle.expert_down(s, h, W, offsets, a4=a4), Y)
+    assert all(oracle.bf16_rne(float(v)) == int(b) for v, b in zip(hpre.ravel(), h.ravel()))
+    x = _bf16_values(xbits).reshape(s.T, s.H)
+    hr = gen.normal_bf16_bits(13, gen.stream(gen.KIND_X), s.T * s.k * s.I).reshape(s.T * s.k, s.I)
+    Yr = oracle.expert_down(s, hr, W, offsets, a4=a4)
+    for e in range(s.E):
+        W13 = _dense_weights(experts[e][0], experts[e][1])
+        W2 = _dense_weights(experts[e][2], experts[e][3])
+        for p in range(offsets[e], offsets[e + 1]):
+            xt = _a4_values(xbits[perm[p] // s.k]) if a4 else x[perm[p] // s.k]
+            g, u = W13[: s.I] @ xt, W13[s.I:] @ xt
+            ref = torch.nn.functional.silu(torch.from_numpy(g)).numpy() * u
+            np.testing.assert_allclose(hpre[p], ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+            hv = _a4_values(hr[p]) if a4 else _bf16_values(hr[p])
+            ref_y = W2 @ hv
+            np.testing.assert_allclose(Yr[p], ref_y, rtol=1e-12, atol=1e-12 * np.abs(ref_y).max())
