@@ -571,7 +571,7 @@ def run_leg(a, name, mode, W, dev, ws, clocks, cpu_cache, rank):
                                "expert_ffn": float(np.median(lb.ffn_ms) * 1e3),
                                "combine": float(np.median(lb.comb_ms) * 1e3)},
            "roofline": lb.roofline(), "gpu_launches": lb.launches_per_step * steps, "l2": lb.l2_mode,
-           "clocks": clocks.window(lb.t0, lb.t1) if clocks else None}
+           "timed_window": (lb.t0, lb.t1)}
     a4 = resolved_mode(s, mode) == 4
     if rank == 0 and not a.no_cpu_baseline:
         key = (name, a4)
@@ -683,6 +683,8 @@ def run_gpu(a):
             torch.cuda.empty_cache()
     time.sleep(0.2)
     clk = clocks.stop()
+    for ent in (workloads or {}).values():  # clocks seen during each workload's timed steps
+        ent["clocks"] = clocks.window(*ent.pop("timed_window"))
 
     cpu = None
     if rank == 0 and not a.no_cpu_baseline:

@@ -121,6 +121,14 @@ typedef struct {
 #define K3MOE_OP_BUCKET 1
 #define K3MOE_OP_EXPERT_FFN 2
 size_t k3moe_workspace_bytes(k3moe_shape s, int op, int mode);
+/* Where the expert FFN leaves h: after a k3moe_expert_ffn call with shape s and
+ * mode, its workspace holds h = bf16_rne(silu(g) * u) -- the GLU expert's one
+ * rounding point, before the down projection (in W4A4 mode: before its MXFP4
+ * quantisation) -- as uint16 [A][I] bf16 bit patterns in bucket order, starting
+ * this many bytes into the workspace (256-byte aligned).  Lets a caller check or
+ * reuse the intermediate without another kernel.  (size_t)-1 for a bad shape or
+ * an unsupported mode. */
+size_t k3moe_workspace_h_offset(k3moe_shape s, int mode);
 
 /* Route: for each token t, the k experts with the largest logits, ordered by
  * (logit descending, expert index ascending) -- ties go to the lower index, -0
@@ -133,6 +141,29 @@ size_t k3moe_workspace_bytes(k3moe_shape s, int op, int mode);
  *   dev_status : int32 device word (may be NULL: NaN rows are then unreported). */
 int k3moe_route(k3moe_shape s, const float *logits, int32_t *idx, float *w,
                 int32_t *dev_status, k3moe_stream_t stream);
+
+/* Router: the score of every expert for every token, then the route above on
+ * those scores (the step that feeds the top-16-of-896 selection: kimi-k3-in-c
+ * CHANGELOG walkthrough "[0.1.0] Added"; article section "01").  The pages
+ * name the selection but not the score; it is the linear form
+ *   logits[t][e] = sum_h x[t][h] * wr[e][h]
+ * of the token's bf16 hidden state and the bf16 router row of expert e, with
+ * exact products accumulated in fp32, and the route selects on these fp32
+ * logits exactly as k3moe_route does (same order, ties and weights).
+ *   x      : uint16 [T][H] bf16 bit patterns, 16-byte aligned
+ *   wr     : uint16 [E][H] bf16 bit patterns (row e scores expert e), 16-byte aligned
+ *   logits : float [T][E], written (the fp32 scores the route selected on)
+ *   idx, w, dev_status : as in k3moe_route
+ * Accumulation: below 64 tokens a CUDA-core kernel sums each score in a fixed
+ * order whose longest chain of fp32 roundings is ceil(H/256) + 7 (so |error| <=
+ * gamma(ceil(H/256) + 7) * sum_h |x[t][h] wr[e][h]|, gamma(d) = d u / (1 - d u),
+ * u = 2^-24); from 64 tokens the tcgen05 tensor cores accumulate in fp32 in
+ * steps of K = 16 (fixed, deterministic order), for which the stated bound is
+ * gamma(ceil(H/16) + 16) with u = 2^-23.  Scores that differ by less than
+ * twice the bound can therefore order differently from an exact sum.
+ * Errors: as k3moe_route; x or wr misaligned -> K3MOE_ERR_ALIGN. */
+int k3moe_router(k3moe_shape s, const uint16_t *x, const uint16_t *wr, float *logits, int32_t *idx, float *w,
+                 int32_t *dev_status, k3moe_stream_t stream);
 
 /* Bucket: a stable counting sort of the A = T*k assignments a = t*k + j by
  * expert idx[a] (the chunk-union grouping).

@@ -67,8 +67,12 @@ def lib():
             vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
             L.k3moe_workspace_bytes.restype = sz
             L.k3moe_workspace_bytes.argtypes = [Shape, i32, i32]
+            L.k3moe_workspace_h_offset.restype = sz
+            L.k3moe_workspace_h_offset.argtypes = [Shape, i32]
             L.k3moe_route.restype = i32
             L.k3moe_route.argtypes = [Shape, vp, vp, vp, vp, vp]
+            L.k3moe_router.restype = i32
+            L.k3moe_router.argtypes = [Shape, vp, vp, vp, vp, vp, vp, vp]
             L.k3moe_bucket.restype = i32
             L.k3moe_bucket.argtypes = [Shape, vp, vp, vp, vp, vp, vp, sz, vp, vp]
             L.k3moe_expert_ffn.restype = i32
@@ -155,11 +159,27 @@ def k3moe_workspace_bytes(shape, op: int, mode: int = 0) -> int:
     return int(lib().k3moe_workspace_bytes(Shape.of(shape), op, mode))
 
 
+def k3moe_workspace_h_offset(shape, mode: int = 0) -> int:
+    """Byte offset of h (bf16 [A, I], bucket order) in the expert FFN workspace."""
+    v = int(lib().k3moe_workspace_h_offset(Shape.of(shape), mode))
+    return -1 if v == (1 << 64) - 1 else v
+
+
 def k3moe_route(shape, logits, idx, w, dev_status=None, stream=None):
     rc = lib().k3moe_route(Shape.of(shape), _ptr(logits, torch.float32, "logits"),
                            _ptr(idx, torch.int32, "idx"), _ptr(w, torch.float32, "w"),
                            _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
     _check("k3moe_route", rc)
+
+
+def k3moe_router(shape, x, wr, logits, idx, w, dev_status=None, stream=None):
+    """Router scores logits [T, E] = x [T, H] . wr [E, H]^T (bf16 in, fp32 out),
+    then the top-k route on them (idx, w)."""
+    rc = lib().k3moe_router(Shape.of(shape), _ptr(x, _BF16, "x"), _ptr(wr, _BF16, "wr"),
+                            _ptr(logits, torch.float32, "logits"), _ptr(idx, torch.int32, "idx"),
+                            _ptr(w, torch.float32, "w"), _ptr(dev_status, torch.int32, "dev_status"),
+                            _stream(stream))
+    _check("k3moe_router", rc)
 
 
 def k3moe_bucket(shape, idx, counts, offsets, perm, inv, ws=None, dev_status=None, stream=None):

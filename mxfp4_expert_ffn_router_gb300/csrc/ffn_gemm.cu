@@ -47,6 +47,7 @@
 #include "k3moe_dev.cuh"
 #include "k3moe_launch.h"
 #include "mx_quant.cuh"
+#include "tc_sm103.cuh"
 
 namespace k3moe {
 
@@ -72,38 +73,8 @@ constexpr int kWStages = 2;
 constexpr int kWBoxRows = 64;
 constexpr int kWStageB = kTileM * (kWK / 2);    // 16 KiB
 constexpr int kMapBytes = 128;                  // one CUtensorMap
-constexpr long long kSpinG = 1LL << 22;
+constexpr long long kSpinG = kSpinTc;
 
-__device__ __forceinline__ uint32_t su32(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
-
-// ---- mbarrier ----
-__device__ __forceinline__ void mb_init(uint64_t *b, uint32_t n) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(n) : "memory");
-}
-__device__ __forceinline__ bool mb_try(uint64_t *b, uint32_t parity) {
-  uint32_t ok;
-  asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-               : "=r"(ok)
-               : "r"(su32(b)), "r"(parity)
-               : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ void mb_arrive(uint64_t *b) {
-  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(su32(b)) : "memory");
-}
-__device__ __forceinline__ void mb_arrive_tx(uint64_t *b, uint32_t bytes) {
-  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(su32(b)),
-               "r"(bytes)
-               : "memory");
-}
-// 2-D TMA tile load (tensor map in kernel-parameter space) completing on `bar`.
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
-          "r"(su32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(su32(bar))
-      : "memory");
-}
 // 2-D TMA prefetch of one box into L2 (no shared memory, no completion).
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
@@ -113,30 +84,7 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, i
 __device__ __forceinline__ void prefetch_l2(const void *p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
 }
-__device__ __forceinline__ bool mb_wait(uint64_t *b, uint32_t parity) {
-  for (long long i = 0; i < kSpinG; ++i) {
-    if (mb_try(b, parity)) return true;
-    if (i > 32) __nanosleep(20);
-  }
-  return false;
-}
-
 // ---- tcgen05 ----
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row atoms of
-// 1024 bytes (stride byte offset 1024), descriptor version 1.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFF) >> 4);       // start address
-  d |= static_cast<uint64_t>(1) << 16;                      // leading byte offset (unused for SW128 K-major)
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;              // stride byte offset
-  d |= static_cast<uint64_t>(1) << 46;                      // version
-  d |= static_cast<uint64_t>(2) << 61;                      // SWIZZLE_128B
-  return d;
-}
-
 // Instruction descriptor, kind::f16: f16 A and B, fp32 accumulator, both K-major.
 __device__ __forceinline__ uint32_t idesc_f16(int M, int N) {
   return (1u << 4)                                   // D format: f32
@@ -164,23 +112,6 @@ __device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&r)[16])
       "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tc_commit(uint64_t *bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
-               : "memory");
-}
-// 32 lanes x 32 bit, 16 consecutive columns per thread.
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 
@@ -1159,20 +1090,6 @@ EncodeTiledFn encode_tiled() {
   return fn;
 }
 
-// 2-D map over rows x K of 16-bit values: box = 64 (K) x 128 rows, 128B swizzle,
-// rows past the end read as zero.
-bool make_row_map(CUtensorMap *m, void *base, int rows, int K) {
-  EncodeTiledFn fn = encode_tiled();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-  const cuuint32_t box[2] = {kTileK, kTileN};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // 2-D map over the weight codes of one expert (rows x K/2 bytes): box = 128
 // bytes x 64 rows, 128B swizzle.  `base` is a placeholder address that the
 // device replaces per expert.
@@ -1238,7 +1155,22 @@ int launch_gemm_mxf4(const k3moe_shape &s, const uint16_t *x, const int32_t *per
 
 }  // namespace
 
+// 2-D map over rows x K of 16-bit values: box = 64 (K) x 128 rows, 128B swizzle,
+// rows past the end read as zero.
+bool make_row_map(CUtensorMap *m, void *base, int rows, int K) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  const cuuint32_t box[2] = {kTileK, kTileN};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 size_t ffn_gemm_workspace(const k3moe_shape &s) { return gemm_ws(s.T, s.H, s.I, s.E, s.k).total; }
+size_t ffn_gemm_h_offset(const k3moe_shape &s) { return gemm_ws(s.T, s.H, s.I, s.E, s.k).hrow; }
 
 bool ffn_gemm_supported(const k3moe_shape &s) {
   return (2 * s.I) % kTileM == 0 && s.H % kTileM == 0 && s.H % kTileK == 0 && s.I % kTileK == 0 &&

@@ -559,6 +559,7 @@ __global__ void __launch_bounds__(kGvWarps * 32, 2) gemv_rows_pipe_kernel(RowsPa
 
 // ----------------------------------------------------------------------------
 size_t ffn_gemv_workspace(const k3moe_shape &s) { return gemv_ws(s.T, s.H, s.I, s.E, s.k).total; }
+size_t ffn_gemv_h_offset(const k3moe_shape &s) { return gemv_ws(s.T, s.H, s.I, s.E, s.k).hrow; }
 
 namespace {
 

@@ -788,6 +788,7 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) ffn_stream_kernel(Params P) {
 
 // ----------------------------------------------------------------------------
 size_t ffn_stream_workspace(const k3moe_shape &s) { return stream_ws(s.T, s.H, s.I, s.E, s.k).total; }
+size_t ffn_stream_h_offset(const k3moe_shape &s) { return stream_ws(s.T, s.H, s.I, s.E, s.k).hrow; }
 
 static int stream_ntcap(const k3moe_shape &s) { return s.T < kNT ? s.T : kNT; }
 

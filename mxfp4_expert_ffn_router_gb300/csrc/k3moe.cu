@@ -94,6 +94,15 @@ static size_t ffn_workspace(const k3moe_shape &s, int resolved) {
   return 0;
 }
 
+size_t k3moe_workspace_h_offset(k3moe_shape s, int mode) {
+  if (abi_check_shape(s) != K3MOE_OK) return static_cast<size_t>(-1);
+  const int resolved = resolve_ffn_mode(s, mode);
+  if (resolved == K3MOE_FFN_GEMV) return k3moe::ffn_gemv_h_offset(s);
+  if (resolved == K3MOE_FFN_STREAM) return k3moe::ffn_stream_h_offset(s);
+  if (resolved == K3MOE_FFN_GEMM || resolved == K3MOE_FFN_W4A4) return k3moe::ffn_gemm_h_offset(s);
+  return static_cast<size_t>(-1);
+}
+
 size_t k3moe_workspace_bytes(k3moe_shape s, int op, int mode) {
   if (abi_check_shape(s) != K3MOE_OK) return 0;
   if (op == K3MOE_OP_BUCKET) return k3moe::bucket_workspace(s);
@@ -109,6 +118,18 @@ int k3moe_route(k3moe_shape s, const float *logits, int32_t *idx, float *w, int3
   if (!logits || !idx || !w) return K3MOE_ERR_ARG;
   if ((rc = abi_check_arch())) return rc;
   return abi_launched(k3moe::launch_route(s, logits, idx, w, dev_status, reinterpret_cast<k3moe_stream>(stream)));
+}
+
+int k3moe_router(k3moe_shape s, const uint16_t *x, const uint16_t *wr, float *logits, int32_t *idx, float *w,
+                 int32_t *dev_status, k3moe_stream_t stream) {
+  int rc = abi_check_shape(s);
+  if (rc) return rc;
+  if (s.T == 0) return K3MOE_OK;
+  if (!x || !wr || !logits || !idx || !w) return K3MOE_ERR_ARG;
+  if (!aligned16(x) || !aligned16(wr)) return K3MOE_ERR_ALIGN;
+  if ((rc = abi_check_arch())) return rc;
+  return abi_launched(
+      k3moe::launch_router(s, x, wr, logits, idx, w, dev_status, reinterpret_cast<k3moe_stream>(stream)));
 }
 
 int k3moe_bucket(k3moe_shape s, const int32_t *idx, int32_t *counts, int32_t *offsets, int32_t *perm,

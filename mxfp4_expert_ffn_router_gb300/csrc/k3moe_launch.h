@@ -1,5 +1,6 @@
 // k3moe_launch.h -- host-side launch helpers and the internal kernel entry points.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -40,18 +41,28 @@ size_t bucket_workspace(const k3moe_shape &s);
 int launch_bucket(const k3moe_shape &s, const int32_t *idx, int32_t *counts, int32_t *offsets,
                   int32_t *perm, int32_t *inv, void *ws, int32_t *status, cudaStream_t st);
 size_t ffn_gemv_workspace(const k3moe_shape &s);
+size_t ffn_gemv_h_offset(const k3moe_shape &s);
 int launch_ffn_gemv(const k3moe_shape &s, const uint16_t *x, const k3moe_weights &w,
                     const int32_t *offsets, const int32_t *perm, float *Y, void *ws,
                     int32_t *status, cudaStream_t st);
 size_t ffn_stream_workspace(const k3moe_shape &s);
+size_t ffn_stream_h_offset(const k3moe_shape &s);
 bool ffn_stream_supported(const k3moe_shape &s);
 int launch_ffn_stream(const k3moe_shape &s, const uint16_t *x, const k3moe_weights &w,
                       const int32_t *offsets, const int32_t *perm, float *Y, void *ws,
                       int32_t *status, cudaStream_t st);
 size_t ffn_gemm_workspace(const k3moe_shape &s);
+size_t ffn_gemm_h_offset(const k3moe_shape &s);
 bool ffn_gemm_supported(const k3moe_shape &s);
 int launch_ffn_gemm(const k3moe_shape &s, const uint16_t *x, const k3moe_weights &w, const int32_t *offsets,
                     const int32_t *perm, float *Y, void *ws, int32_t *status, cudaStream_t st, bool a4);
+// 2-D TMA map over rows x K 16-bit values (row stride 2K bytes, 16-byte aligned
+// base): boxes of 64 values x 128 rows, 128-byte swizzle, rows and columns past
+// the end read as zero.  False when the driver's encoder is unavailable or refuses.
+bool make_row_map(CUtensorMap *m, void *base, int rows, int K);
+int launch_router(const k3moe_shape &s, const uint16_t *x, const uint16_t *wr, float *logits, int32_t *idx,
+                  float *w, int32_t *status, cudaStream_t st);
+bool router_gemm_supported(const k3moe_shape &s);
 int launch_quantize_mxfp4(long long n, const uint16_t *x, uint8_t *codes, uint8_t *scales, cudaStream_t st);
 int launch_combine(const k3moe_shape &s, const float *Y, const float *w, const int32_t *inv,
                    uint16_t *out, float *out_f32, cudaStream_t st);

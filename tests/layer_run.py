@@ -31,6 +31,7 @@ def alloc_layer(s, device="cuda", mode=k3.K3MOE_FFN_AUTO, with_f32=True):
 
 def run_layer(s, logits, x, weights, bufs=None, mode=k3.K3MOE_FFN_AUTO, stream=None):
     b = bufs if bufs is not None else alloc_layer(s, logits.device, mode)
+    b["mode"] = mode  # which workspace layout holds h (see ffn_check.gpu_h)
     k3.k3moe_route(s, logits, b["idx"], b["w"], b["status"], stream=stream)
     k3.k3moe_bucket(s, b["idx"], b["counts"], b["offsets"], b["perm"], b["inv"], b["ws_bucket"],
                     b["status"], stream=stream)

@@ -10,6 +10,7 @@ import torch
 import gen
 import mxfp4_expert_ffn_router_gb300 as k3
 import oracle
+from ffn_check import check_staged, gpu_h
 from layer_run import alloc_layer, bf16_rne_bits_of, host, max_rel_err, run_layer
 
 pytestmark = pytest.mark.gpu
@@ -45,15 +46,18 @@ def _check_bucket(s, idx, r):
 
 
 def _full_check(s, logits, xbits, experts_np, r, a4=False, absent=()):
+    """Routing and bucketing bit-exact; the FFN staged at its bf16 rounding of h
+    (ffn_check): near-tie flips only, then Y and out against the oracle applied to
+    the GPU's h; the bf16 output equal to RNE(fp32 output)."""
     idx, w, _ = _check_route(s, logits, r)
     counts, offsets, perm, inv = _check_bucket(s, idx, r)
     exps = {e: tuple(z[e] for z in experts_np) for e in np.unique(idx) if e not in absent}
     W = oracle.Weights(s.E, exps)
-    Y = oracle.expert_ffn(s, xbits, W, offsets, perm, a4=a4)
-    out, _ = oracle.combine(s, Y, w, inv)
-    assert max_rel_err(r["Y"], Y) <= TOL, max_rel_err(r["Y"], Y)
-    assert max_rel_err(r["out_f32"], out) <= TOL, max_rel_err(r["out_f32"], out)
+    st = check_staged(s, r, xbits, W, offsets, perm, w, inv, gpu_h(r, s), a4=a4)
     np.testing.assert_array_equal(r["out"], bf16_rne_bits_of(r["out_f32"]))
+    Y = oracle.expert_down(s, gpu_h(r, s), W, offsets, a4=a4)
+    out, _ = oracle.combine(s, Y, w, inv)
+    assert st["out_err"] <= TOL
     return out
 
 

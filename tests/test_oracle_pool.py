@@ -32,3 +32,26 @@ def test_sample_layer_is_the_oracle_layer():
         for i, t in enumerate(sample):
             ref = oracle.moe_token(s, xbits[t], idx[t], w[t], W, a4=a4)
             np.testing.assert_array_equal(out[i], ref)
+
+
+def test_staged_sample_uses_the_given_h():
+    """With the oracle's own h in place of the GPU's, the staged rows are the
+    oracle's layer bit for bit, and the h it reports is the oracle's rounding."""
+    s = gen.Shape(32, 128, 64, 12, 3)
+    rng = np.random.default_rng(6)
+    logits = rng.standard_normal((s.T, s.E)).astype(np.float32)
+    xbits = gen.normal_bf16_bits(14, gen.stream(gen.KIND_X), s.T * s.H).reshape(s.T, s.H)
+    idx, w, _ = oracle.route(s, logits)
+    counts, offsets, perm, inv = oracle.bucket(s, idx)
+    arrs = gen.expert_arrays(s.H, s.I, 0, s.E)
+    W = oracle.Weights(s.E, {e: tuple(z[e] for z in arrs) for e in range(s.E)})
+    for a4 in (False, True):
+        hpre, h = oracle.expert_gateup(s, xbits, W, offsets, perm, a4=a4)
+        sample = np.array([0, 3, 7, 31])
+        d = sample_layer(s, xbits, idx, w, sample, a4=a4, nproc=2, h_gpu=h, inv_gpu=inv)
+        Y, out, inv_s = sample_layer(s, xbits, idx, w, sample, a4=a4, nproc=2)
+        np.testing.assert_array_equal(d["Y"], Y)
+        np.testing.assert_array_equal(d["out"], out)
+        np.testing.assert_array_equal(d["h_ref"], d["h_gpu"])
+        a_full = sample[:, None] * s.k + np.arange(s.k)[None, :]
+        np.testing.assert_array_equal(d["h_gpu"][inv_s[np.arange(len(sample) * s.k)]], h[inv[a_full.ravel()]])
