@@ -583,6 +583,60 @@ def run_leg(a, name, mode, W, dev, ws, clocks, cpu_cache, rank):
     return ent
 
 
+def run_router_leg(a, name, dev, ws, rank):
+    """The router entry point alone (scores x . wr^T, then the top-k route) on a
+    workload's tokens: tokens/s, and its roofline -- HBM bytes (router matrix,
+    x, logits) below 64 tokens (CUDA-core kernel), bf16 tensor FLOPs 2 T E H from
+    64 tokens (tcgen05 kernel)."""
+    import torch
+
+    import mxfp4_expert_ffn_router_gb300 as k3
+    s = gen.CONFIGS[name]
+    wr = torch.from_numpy(gen.make_router(s).view(np.int16)).to(dev)
+    nsets = 8 if s.T <= 64 else 2
+    xs = [torch.from_numpy(gen.make_x(s, seed=gen.INPUT_SEED + 1000 * i).view(np.int16)).to(dev)
+          for i in range(nsets)]
+    logits = torch.empty((s.T, s.E), dtype=torch.float32, device=dev)
+    idx = torch.empty((s.T, s.k), dtype=torch.int32, device=dev)
+    w = torch.empty((s.T, s.k), dtype=torch.float32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    steps = max(1, min(a.steps, a.leg_steps))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for i in range(3 + steps):
+        flush.fill_(i & 0xFF)  # the router matrix (12.8 MB) would otherwise stay in L2
+        if i >= 3:
+            evs[i - 3][0].record(stream)
+        k3.k3moe_router(s, xs[i % nsets], wr, logits, idx, w, st, stream=stream)
+        if i >= 3:
+            evs[i - 3][1].record(stream)
+    torch.cuda.synchronize()
+    if int(st.item()) != 0:
+        raise RuntimeError(f"router {name}: device status {int(st.item())}")
+    ms = np.array([e[0].elapsed_time(e[1]) for e in evs])
+    tot = slowest_rank_ms(float(ms.sum()), ws, dev)
+    med = float(np.median(ms)) / 1e3
+    ent = {"tokens": s.T, "experts": s.E, "hidden": s.H, "top_k": s.k, "steps": steps, "warmup": 3,
+           "tokens_per_s": whole_job_rate(s.T * steps, tot, ws), "us_median": med * 1e6,
+           "l2": f"{L2_FLUSH_BYTES >> 20} MiB buffer written between timed calls"}
+    if s.T < 64:
+        by = s.E * s.H * 2 + s.T * s.H * 2 + s.T * s.E * 4
+        peak, src = hbm_peak()
+        ent["roofline"] = {"bound": "hbm", "kernel": "router_gemv_kernel + route_kernel", "bytes_per_call": by,
+                           "achieved": by / med / 1e9, "peak": peak, "peak_source": src, "unit": "GB/s",
+                           "frac": by / med / 1e9 / peak}
+    else:
+        fl = 2.0 * s.T * s.E * s.H
+        peaks = measured_peaks()
+        bf16 = float(peaks["bf16_tflops"]) if peaks and "bf16_tflops" in peaks else 1900.0
+        ent["roofline"] = {"bound": "tensor", "kernel": "router_gemm_kernel (tcgen05 kind::f16, bf16) + route_kernel",
+                           "flops_per_call": fl, "achieved": fl / med / 1e12, "peak": bf16,
+                           "peak_source": "measured bf16" if peaks else "fallback", "unit": "TFLOP/s",
+                           "frac": fl / med / 1e12 / bf16}
+    return ent
+
+
 LEGS = [("batch8", 0), ("batch8", 3), ("spec2", 1), ("spec2", 3), ("spec4", 1), ("spec4", 3),
         ("spec12", 1), ("spec12", 3), ("spec16", 1), ("spec16", 3),
         ("prefill", 0), ("prefill", 4), ("skewed", 0), ("skewed", 4), ("probe", 4), ("probe", 3)]
@@ -681,6 +735,8 @@ def run_gpu(a):
             key = f"{name}/{mode_name(ls, mode)}"
             workloads[key] = run_leg(a, name, mode, Wl, dev, ws, clocks, cpu_cache, rank)
             torch.cuda.empty_cache()
+        for name in ("decode", "batch8", "prefill"):
+            workloads[f"router/{name}"] = run_router_leg(a, name, dev, ws, rank)
     time.sleep(0.2)
     clk = clocks.stop()
     for ent in (workloads or {}).values():  # clocks seen during each workload's timed steps
