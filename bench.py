@@ -740,7 +740,8 @@ def run_gpu(a):
     time.sleep(0.2)
     clk = clocks.stop()
     for ent in (workloads or {}).values():  # clocks seen during each workload's timed steps
-        ent["clocks"] = clocks.window(*ent.pop("timed_window"))
+        if "timed_window" in ent:
+            ent["clocks"] = clocks.window(*ent.pop("timed_window"))
 
     cpu = None
     if rank == 0 and not a.no_cpu_baseline:

@@ -636,47 +636,69 @@ int launch_rows(RowsParams P, int nsm, cudaStream_t st, int A, uint4 *h16, int32
 
 }  // namespace
 
+GemvBufs gemv_bufs(const k3moe_shape &s, void *ws) {
+  const GemvWs L = gemv_ws(s.T, s.H, s.I, s.E, s.k);
+  char *base = static_cast<char *>(ws);
+  GemvBufs b;
+  b.slots = reinterpret_cast<int4 *>(base + L.slots);
+  b.meta = reinterpret_cast<int32_t *>(base + L.meta);
+  b.xexp = reinterpret_cast<int32_t *>(base + L.xexp);
+  b.x16 = reinterpret_cast<uint4 *>(base + L.x16);
+  b.hrow = reinterpret_cast<uint16_t *>(base + L.hrow);
+  b.hmax = reinterpret_cast<int32_t *>(base + L.hmax);
+  b.h16 = reinterpret_cast<uint4 *>(base + L.h16);
+  b.hexp = reinterpret_cast<int32_t *>(base + L.hexp);
+  return b;
+}
+
+int launch_gemv_prep(const k3moe_shape &s, const uint16_t *x, const k3moe_weights &w, const int32_t *offsets,
+                     const GemvBufs &b, int32_t *status, cudaStream_t st) {
+  return launch_pdl(gemv_prep_kernel, dim3(1 + s.T), dim3(256), 0, st, w, x, s.T, s.H, s.E, s.T * s.k, offsets,
+                    b.slots, b.meta, b.xexp, b.x16, b.hmax, status) == cudaSuccess
+             ? 0
+             : -1;
+}
+
+int launch_gemv_h16(const k3moe_shape &s, const GemvBufs &b, cudaStream_t st) {
+  return launch_pdl(gemv_h16_kernel, dim3(s.T * s.k), dim3(256), 0, st, static_cast<const uint16_t *>(b.hrow),
+                    static_cast<const int32_t *>(b.hmax), s.I, b.h16, b.hexp) == cudaSuccess
+             ? 0
+             : -1;
+}
+
+int sm_count() {
+  static int nsm = 0;
+  if (nsm == 0) {
+    int dev = 0, v = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    nsm = v < 1 ? 1 : v;
+  }
+  return nsm;
+}
+
 int launch_ffn_gemv(const k3moe_shape &s, const uint16_t *x, const k3moe_weights &w,
                     const int32_t *offsets, const int32_t *perm, float *Y, void *ws,
                     int32_t *status, cudaStream_t st) {
   if (s.T == 0) return 0;
-  const GemvWs L = gemv_ws(s.T, s.H, s.I, s.E, s.k);
-  char *base = static_cast<char *>(ws);
-  int4 *slots = reinterpret_cast<int4 *>(base + L.slots);
-  int32_t *meta = reinterpret_cast<int32_t *>(base + L.meta);
-  int32_t *xexp = reinterpret_cast<int32_t *>(base + L.xexp);
-  uint4 *x16 = reinterpret_cast<uint4 *>(base + L.x16);
-  uint16_t *hrow = reinterpret_cast<uint16_t *>(base + L.hrow);
-  int32_t *hmax = reinterpret_cast<int32_t *>(base + L.hmax);
-  uint4 *h16 = reinterpret_cast<uint4 *>(base + L.h16);
-  int32_t *hexp = reinterpret_cast<int32_t *>(base + L.hexp);
-  const int A = s.T * s.k;
-  static int nsm = 0;
-  if (nsm == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-    if (nsm < 1) nsm = 1;
-  }
-  if (launch_pdl(gemv_prep_kernel, dim3(1 + s.T), dim3(256), 0, st, w, x, s.T, s.H, s.E, A, offsets, slots, meta,
-                 xexp, x16, hmax, status) != cudaSuccess)
-    return -1;
+  const GemvBufs b = gemv_bufs(s, ws);
+  if (launch_gemv_prep(s, x, w, offsets, b, status, st)) return -1;
   RowsParams P;
   P.w = w;
   P.H = s.H;
   P.I = s.I;
   P.k = s.k;
-  P.A = A;
+  P.A = s.T * s.k;
   P.perm = perm;
-  P.slots = slots;
-  P.meta = meta;
-  P.aexp = xexp;
-  P.act = x16;
-  P.hrow = hrow;
-  P.hmax = hmax;
+  P.slots = b.slots;
+  P.meta = b.meta;
+  P.aexp = b.xexp;
+  P.act = b.x16;
+  P.hrow = b.hrow;
+  P.hmax = b.hmax;
   P.Y = Y;
   P.status = status;
-  return launch_rows(P, nsm, st, A, h16, hexp);
+  return launch_rows(P, sm_count(), st, P.A, b.h16, b.hexp);
 }
 
 }  // namespace k3moe

@@ -45,6 +45,23 @@ size_t ffn_gemv_h_offset(const k3moe_shape &s);
 int launch_ffn_gemv(const k3moe_shape &s, const uint16_t *x, const k3moe_weights &w,
                     const int32_t *offsets, const int32_t *perm, float *Y, void *ws,
                     int32_t *status, cudaStream_t st);
+// The GEMV mode's workspace pieces, and its front (active slots, x to prescaled
+// f16) and middle (h to prescaled f16) kernels, shared with the STREAM mode.
+struct GemvBufs {
+  int4 *slots;      // {expert, first bucket position, tokens, present} per active slot
+  int32_t *meta;    // [0] = active slots
+  int32_t *xexp;    // prescale exponent per token
+  uint4 *x16;       // x as prescaled f16, piece-major [T][H/8]
+  uint16_t *hrow;   // h, bf16 [A][I] (the rounding point)
+  int32_t *hmax;    // max |h| per bucket position (float bits)
+  uint4 *h16;       // h as prescaled f16, piece-major [A][I/8]
+  int32_t *hexp;    // prescale exponent per bucket position
+};
+GemvBufs gemv_bufs(const k3moe_shape &s, void *ws);
+int launch_gemv_prep(const k3moe_shape &s, const uint16_t *x, const k3moe_weights &w, const int32_t *offsets,
+                     const GemvBufs &b, int32_t *status, cudaStream_t st);
+int launch_gemv_h16(const k3moe_shape &s, const GemvBufs &b, cudaStream_t st);
+int sm_count();
 size_t ffn_stream_workspace(const k3moe_shape &s);
 size_t ffn_stream_h_offset(const k3moe_shape &s);
 bool ffn_stream_supported(const k3moe_shape &s);

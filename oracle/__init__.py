@@ -66,7 +66,7 @@ def lib():
             L.k3ref_expert_ffn.restype = i32
             L.k3ref_expert_ffn.argtypes = [Shape, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp]
             L.k3ref_expert_gateup.restype = i32
-            L.k3ref_expert_gateup.argtypes = [Shape, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp]
+            L.k3ref_expert_gateup.argtypes = [Shape, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp]
             L.k3ref_expert_down.restype = i32
             L.k3ref_expert_down.argtypes = [Shape, vp, vp, vp, vp, vp, vp, i32, vp]
             L.k3ref_combine.restype = i32
@@ -207,18 +207,21 @@ def expert_ffn(s, x_bits: np.ndarray, weights: Weights, offsets: np.ndarray, per
 
 
 def expert_gateup(s, x_bits: np.ndarray, weights: Weights, offsets: np.ndarray, perm: np.ndarray,
-                  a4: bool = False):
-    """(hpre float64 [A, I], h bf16 bits uint16 [A, I]) in bucket order."""
+                  a4: bool = False, sums: bool = False):
+    """(hpre float64 [A, I], h bf16 bits uint16 [A, I]) in bucket order; with sums
+    also a dict of g, u, gabs = sum |Wg x|, uabs = sum |Wu x| (float64 [A, I])."""
     x = _c(x_bits, np.uint16)
     o = _c(offsets, np.int32)
     p = _c(perm, np.int32)
     A = s.T * s.k
     hpre = np.zeros((A, s.I), np.float64)
     h = np.zeros((A, s.I), np.uint16)
+    extra = {k: np.zeros((A, s.I), np.float64) for k in ("g", "u", "gabs", "uabs")} if sums else None
+    ptr = [extra[k].ctypes.data for k in ("g", "u", "gabs", "uabs")] if sums else [None] * 4
     if lib().k3ref_expert_gateup(_shape(s), x.ctypes.data, *weights.args(), o.ctypes.data, p.ctypes.data,
-                                 int(a4), hpre.ctypes.data, h.ctypes.data) != 0:
+                                 int(a4), hpre.ctypes.data, h.ctypes.data, *ptr) != 0:
         raise ValueError("k3ref_expert_gateup: bad arguments")
-    return hpre, h
+    return (hpre, h, extra) if sums else (hpre, h)
 
 
 def expert_down(s, h_bits: np.ndarray, weights: Weights, offsets: np.ndarray, a4: bool = False):

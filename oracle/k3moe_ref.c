@@ -271,21 +271,29 @@ static int expert_present(int e, const uint8_t *const *w13c, const uint8_t *cons
 
 /* Gate/up half of one expert on one token: g = Wg x, u = Wu x, hpre = silu(g) u
  * in double, h = bf16(hpre) ([changelog] "[0.1.0] Added": GLU expert with MXFP4
- * weights).  hpre may be NULL. */
+ * weights).  Optional outputs (NULL to skip): hpre; g and u; gabs = sum |Wg x|
+ * and uabs = sum |Wu x| (the magnitudes that bound a finite-precision sum). */
 static void expert_gateup(k3ref_shape s, const double *xv, const uint8_t *w13c, const uint8_t *w13s,
-                          uint16_t *h_bits, double *hpre) {
+                          uint16_t *h_bits, double *hpre, double *g_out, double *u_out, double *gabs,
+                          double *uabs) {
   double *wg = (double *)malloc(sizeof(double) * (size_t)s.H);
   double *wu = (double *)malloc(sizeof(double) * (size_t)s.H);
   for (int r = 0; r < s.I; ++r) {
     mx_row(w13c, w13s, s.H, r, wg);        /* gate row r */
     mx_row(w13c, w13s, s.H, s.I + r, wu);  /* up row r   */
-    double g = 0.0, u = 0.0;
+    double g = 0.0, u = 0.0, ga = 0.0, ua = 0.0;
     for (int c = 0; c < s.H; ++c) {
       g += wg[c] * xv[c];
       u += wu[c] * xv[c];
+      ga += fabs(wg[c] * xv[c]);
+      ua += fabs(wu[c] * xv[c]);
     }
     const double v = k3ref_silu(g) * u;
     if (hpre) hpre[r] = v;
+    if (g_out) g_out[r] = g;
+    if (u_out) u_out[r] = u;
+    if (gabs) gabs[r] = ga;
+    if (uabs) uabs[r] = ua;
     h_bits[r] = k3ref_bf16_rne(v);
   }
   free(wg);
@@ -310,31 +318,36 @@ static void expert_down(k3ref_shape s, const uint16_t *h_bits, const uint8_t *w2
 static void expert_apply(k3ref_shape s, const double *xv, const uint8_t *w13c,
                          const uint8_t *w13s, const uint8_t *w2c, const uint8_t *w2s, int a4,
                          uint16_t *h_bits, double *hv, double *y) {
-  expert_gateup(s, xv, w13c, w13s, h_bits, NULL);
+  expert_gateup(s, xv, w13c, w13s, h_bits, NULL, NULL, NULL, NULL, NULL);
   expert_down(s, h_bits, w2c, w2s, a4, hv, y);
 }
 
 int k3ref_expert_gateup(k3ref_shape s, const uint16_t *x, const uint8_t *const *w13c,
                         const uint8_t *const *w13s, const uint8_t *const *w2c,
                         const uint8_t *const *w2s, const int32_t *offsets, const int32_t *perm,
-                        int a4, double *hpre, uint16_t *h) {
+                        int a4, double *hpre, uint16_t *h, double *g, double *u, double *gabs,
+                        double *uabs) {
   if (!shape_ok(s)) return -1;
   double *xv = (double *)malloc(sizeof(double) * (size_t)s.H);
   if (!xv) return -1;
   for (int e = 0; e < s.E; ++e) {
     const int present = expert_present(e, w13c, w13s, w2c, w2s);
     for (int p = offsets[e]; p < offsets[e + 1]; ++p) {
-      double *hp = hpre + (size_t)p * s.I;
-      uint16_t *hb = h + (size_t)p * s.I;
+      const size_t o = (size_t)p * s.I;
       if (!present) { /* [changelog] "[Unreleased] Fixed": a missing expert adds zero */
         for (int i = 0; i < s.I; ++i) {
-          hp[i] = 0.0;
-          hb[i] = 0;
+          hpre[o + i] = 0.0;
+          h[o + i] = 0;
+          if (g) g[o + i] = 0.0;
+          if (u) u[o + i] = 0.0;
+          if (gabs) gabs[o + i] = 0.0;
+          if (uabs) uabs[o + i] = 0.0;
         }
         continue;
       }
       activation_values(x + (size_t)(perm[p] / s.k) * s.H, s.H, a4, xv);
-      expert_gateup(s, xv, w13c[e], w13s[e], hb, hp);
+      expert_gateup(s, xv, w13c[e], w13s[e], h + o, hpre + o, g ? g + o : NULL, u ? u + o : NULL,
+                    gabs ? gabs + o : NULL, uabs ? uabs + o : NULL);
     }
   }
   free(xv);

@@ -86,14 +86,16 @@ int k3ref_expert_ffn(k3ref_shape s, const uint16_t *x, const uint8_t *const *w13
                      int a4, double *Y, uint16_t *h_out);
 /* The two halves of k3moe_ref_expert_ffn, for checking a path that takes the
  * bf16 rounding of h as its own decision: hpre[A][I] = silu(g) u in double and
- * h[A][I] = its bf16 rounding, in bucket order; and Y[A][H] = W2 h for given
- * bf16 h rows in bucket order (a4: each h row quantised to MXFP4 first).  An
- * absent expert gives zero rows.  expert_ffn = gateup, then down on its h.
- * Return 0 or -1. */
+ * h[A][I] = its bf16 rounding, in bucket order (optionally g, u and the sums
+ * gabs = sum_c |Wg[c] x[c]|, uabs = sum_c |Wu[c] x[c]|, [A][I] each, NULL to
+ * skip); and Y[A][H] = W2 h for given bf16 h rows in bucket order (a4: each h row
+ * quantised to MXFP4 first).  An absent expert gives zero rows.  expert_ffn =
+ * gateup, then down on its h.  Return 0 or -1. */
 int k3ref_expert_gateup(k3ref_shape s, const uint16_t *x, const uint8_t *const *w13c,
                         const uint8_t *const *w13s, const uint8_t *const *w2c,
                         const uint8_t *const *w2s, const int32_t *offsets, const int32_t *perm,
-                        int a4, double *hpre, uint16_t *h);
+                        int a4, double *hpre, uint16_t *h, double *g, double *u, double *gabs,
+                        double *uabs);
 int k3ref_expert_down(k3ref_shape s, const uint16_t *h, const uint8_t *const *w13c,
                       const uint8_t *const *w13s, const uint8_t *const *w2c,
                       const uint8_t *const *w2s, const int32_t *offsets, int a4, double *Y);

@@ -24,7 +24,8 @@ import oracle
 def _expert_rows(task):
     """One routed expert's oracle rows for the activation rows x_e ([n, H] bf16 bits):
     Y float64 [n, H]; with the GPU's h rows h_e ([n, I]) also the oracle's
-    unrounded and rounded h (gate/up) and Y from the GPU's h (down)."""
+    unrounded and rounded h, g, u and their magnitude sums (gate/up) and Y from
+    the GPU's h (down)."""
     H, I, e, x_e, h_e, a4, seed = task
     n = x_e.shape[0]
     arrs = gen.expert_arrays(H, I, e, e + 1, seed=seed, nthreads=1)
@@ -32,10 +33,10 @@ def _expert_rows(task):
     s1 = gen.Shape(n, H, I, 1, 1)
     off, perm = np.array([0, n], np.int32), np.arange(n, dtype=np.int32)
     if h_e is None:
-        return e, oracle.expert_ffn(s1, x_e, W, off, perm, a4=a4), None, None
-    hpre, h_ref = oracle.expert_gateup(s1, x_e, W, off, perm, a4=a4)
+        return e, oracle.expert_ffn(s1, x_e, W, off, perm, a4=a4), None, None, None
+    hpre, h_ref, sums = oracle.expert_gateup(s1, x_e, W, off, perm, a4=a4, sums=True)
     Y = oracle.expert_down(s1, h_e, W, off, a4=a4)
-    return e, Y, hpre, h_ref
+    return e, Y, hpre, h_ref, sums
 
 
 def workers() -> int:
@@ -51,7 +52,8 @@ def sample_layer(s, xbits, idx, w, tokens, a4=False, seed=gen.WEIGHT_SEED, nproc
 
     With the GPU's h (``h_gpu`` [A, I] in the GPU's bucket order, ``inv_gpu`` its
     inverse permutation): a dict with the sub-batch's GPU h rows, the oracle's
-    unrounded and rounded h, Y' and out' computed from the GPU's h, and inv'."""
+    unrounded and rounded h, its g, u, sum |Wg x| and sum |Wu x| ("sums"), Y' and
+    out' computed from the GPU's h, and inv'."""
     tokens = np.asarray(tokens, np.int64)
     n = len(tokens)
     sub = gen.Shape(n, s.H, s.I, s.E, s.k)
@@ -73,17 +75,20 @@ def sample_layer(s, xbits, idx, w, tokens, a4=False, seed=gen.WEIGHT_SEED, nproc
     Y = np.zeros((n * s.k, s.H), np.float64)
     hpre = np.zeros((n * s.k, s.I), np.float64) if staged else None
     h_ref = np.zeros((n * s.k, s.I), np.uint16) if staged else None
+    sums = {k: np.zeros((n * s.k, s.I), np.float64) for k in ("g", "u", "gabs", "uabs")} if staged else None
     ctx = mp.get_context("spawn")
     with ctx.Pool(nproc or workers()) as pool:
-        for e, rows, hp, hr in pool.imap_unordered(_expert_rows, tasks):
+        for e, rows, hp, hr, sm in pool.imap_unordered(_expert_rows, tasks):
             Y[offsets[e]:offsets[e + 1]] = rows
             if staged:
                 hpre[offsets[e]:offsets[e + 1]] = hp
                 h_ref[offsets[e]:offsets[e + 1]] = hr
+                for key in sums:
+                    sums[key][offsets[e]:offsets[e + 1]] = sm[key]
     out, _ = oracle.combine(sub, Y, w_s, inv)
     if not staged:
         return Y, out, inv
-    return {"Y": Y, "out": out, "inv": inv, "hpre": hpre, "h_ref": h_ref, "h_gpu": h_sub}
+    return {"Y": Y, "out": out, "inv": inv, "hpre": hpre, "h_ref": h_ref, "h_gpu": h_sub, "sums": sums}
 
 
 def hot_expert_sample(s, counts, offsets, perm, n_hot=32, tile=128, total=256, rng_seed=123):

@@ -73,8 +73,11 @@ CASES = [  # T, H, I, E, k: several tiles and ragged tails
 ]
 
 
-STREAM_CASES = [  # shapes the TMA-fed streaming kernel accepts (H/32, I/32 multiples of 16)
+STREAM_CASES = [  # shapes the TMA-fed streaming kernels accept (H a multiple of 64, H and I <= 8192)
     (1, 512, 512, 8, 2),
+    (4, 192, 96, 8, 2),         # rows shorter than a warp's 32 chunks, guarded loops
+    (70, 64, 32, 5, 3),         # smallest rows; 40+ tokens per expert: two g/u exchange groups
+    (2, 8192, 8192, 3, 2),      # largest rows: two- and three-stage rings
     (5, 512, 512, 8, 2),
     (37, 1024, 512, 24, 6),
     (130, 512, 1024, 7, 3),
@@ -122,13 +125,31 @@ def test_gemv_mode_on_stream_shapes(T, H, I, E, k):
     _run_case(T, H, I, E, k, k3.K3MOE_FFN_GEMV)
 
 
+@pytest.mark.parametrize("T,H,I,E,k", STREAM_CASES)
+def test_stream_mode_is_bitwise_the_gemv_mode(T, H, I, E, k):
+    """The TMA-fed kernels sum in the GEMV kernels' order: same h, same Y, bit for bit."""
+    s = gen.Shape(T, H, I, E, k)
+    rng = np.random.default_rng(T * 1000 + E + 1)
+    logits = torch.from_numpy(rng.standard_normal((T, E)).astype(np.float32)).cuda()
+    xbits = gen.normal_bf16_bits(4, gen.stream(gen.KIND_X), T * H).reshape(T, H)
+    Wd = _device_weights(_experts_host(H, I, E))
+    got = {}
+    for mode in (k3.K3MOE_FFN_GEMV, k3.K3MOE_FFN_STREAM):
+        r = host(run_layer(s, logits, torch.from_numpy(xbits.view(np.int16)).cuda(), Wd,
+                           bufs=alloc_layer(s, mode=mode), mode=mode))
+        assert r["status"][0] == 0
+        got[mode] = (gpu_h(r, s), r["Y"])
+    np.testing.assert_array_equal(got[k3.K3MOE_FFN_GEMV][0], got[k3.K3MOE_FFN_STREAM][0])
+    np.testing.assert_array_equal(got[k3.K3MOE_FFN_GEMV][1].view(np.int32), got[k3.K3MOE_FFN_STREAM][1].view(np.int32))
+
+
 def test_stream_mode_refuses_unsupported_shape():
-    s = gen.Shape(2, 128, 64, 4, 1)
+    s = gen.Shape(2, 96, 64, 4, 1)  # H not a multiple of 64
     assert k3.k3moe_workspace_bytes(s, k3.K3MOE_OP_EXPERT_FFN, k3.K3MOE_FFN_STREAM) == 0
     b = alloc_layer(s)
     with pytest.raises(k3.K3moeError) as ei:
-        k3.k3moe_expert_ffn(s, torch.zeros((2, 128), dtype=torch.int16, device="cuda"),
-                            _device_weights(_experts_host(128, 64, 4)), b["offsets"], b["perm"], b["Y"],
+        k3.k3moe_expert_ffn(s, torch.zeros((2, 96), dtype=torch.int16, device="cuda"),
+                            _device_weights(_experts_host(96, 64, 4)), b["offsets"], b["perm"], b["Y"],
                             k3.K3MOE_FFN_STREAM, b["ws_ffn"], b["status"])
     assert ei.value.code == k3.K3MOE_ERR_UNSUPPORTED
 

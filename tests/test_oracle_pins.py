@@ -479,7 +479,7 @@ def test_ffn_halves_compose_to_the_ffn_and_match_dense_math(a4):
     idx, w, _ = oracle.route(s, logits)
     counts, offsets, perm, inv = oracle.bucket(s, idx)
     Y, h_ffn = oracle.expert_ffn(s, xbits, W, offsets, perm, a4=a4, want_h=True)
-    hpre, h = oracle.expert_gateup(s, xbits, W, offsets, perm, a4=a4)
+    hpre, h, sums = oracle.expert_gateup(s, xbits, W, offsets, perm, a4=a4, sums=True)
     np.testing.assert_array_equal(h, h_ffn)
     np.testing.assert_array_equal(oracle.expert_down(s, h, W, offsets, a4=a4), Y)
     assert all(oracle.bf16_rne(float(v)) == int(b) for v, b in zip(hpre.ravel(), h.ravel()))
@@ -494,6 +494,9 @@ def test_ffn_halves_compose_to_the_ffn_and_match_dense_math(a4):
             g, u = W13[: s.I] @ xt, W13[s.I:] @ xt
             ref = torch.nn.functional.silu(torch.from_numpy(g)).numpy() * u
             np.testing.assert_allclose(hpre[p], ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+            for key, ref_v in (("g", g), ("u", u), ("gabs", np.abs(W13[: s.I]) @ np.abs(xt)),
+                               ("uabs", np.abs(W13[s.I:]) @ np.abs(xt))):
+                np.testing.assert_allclose(sums[key][p], ref_v, rtol=1e-12, atol=1e-12 * np.abs(ref_v).max())
             hv = _a4_values(hr[p]) if a4 else _bf16_values(hr[p])
             ref_y = W2 @ hv
             np.testing.assert_allclose(Yr[p], ref_y, rtol=1e-12, atol=1e-12 * np.abs(ref_y).max())

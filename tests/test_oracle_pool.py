@@ -46,12 +46,15 @@ def test_staged_sample_uses_the_given_h():
     arrs = gen.expert_arrays(s.H, s.I, 0, s.E)
     W = oracle.Weights(s.E, {e: tuple(z[e] for z in arrs) for e in range(s.E)})
     for a4 in (False, True):
-        hpre, h = oracle.expert_gateup(s, xbits, W, offsets, perm, a4=a4)
+        hpre, h, sums = oracle.expert_gateup(s, xbits, W, offsets, perm, a4=a4, sums=True)
         sample = np.array([0, 3, 7, 31])
         d = sample_layer(s, xbits, idx, w, sample, a4=a4, nproc=2, h_gpu=h, inv_gpu=inv)
         Y, out, inv_s = sample_layer(s, xbits, idx, w, sample, a4=a4, nproc=2)
         np.testing.assert_array_equal(d["Y"], Y)
         np.testing.assert_array_equal(d["out"], out)
         np.testing.assert_array_equal(d["h_ref"], d["h_gpu"])
+        for key in ("g", "u", "gabs", "uabs"):  # the sub-batch's rows of the whole batch's sums
+            np.testing.assert_array_equal(d["sums"][key][inv_s[np.arange(len(sample) * s.k)]],
+                                          sums[key][inv[(sample[:, None] * s.k + np.arange(s.k)[None, :]).ravel()]])
         a_full = sample[:, None] * s.k + np.arange(s.k)[None, :]
         np.testing.assert_array_equal(d["h_gpu"][inv_s[np.arange(len(sample) * s.k)]], h[inv[a_full.ravel()]])
