@@ -79,7 +79,8 @@ def _check(s, x_bits, wr_bits):
         assert set(g_idx[t].tolist()) == set(idx_o[t].tolist()), t
     for t in np.flatnonzero(order_clear):
         np.testing.assert_array_equal(g_idx[t], idx_o[t])
-    assert set_clear.mean() > 0.5
+    if s.T >= 50:
+        assert set_clear.mean() > 0.5  # the bound is tight enough to decide most tokens
     return g_logits, g_idx
 
 
