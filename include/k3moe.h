@@ -101,9 +101,11 @@ typedef struct {
                               and the shape allows it, else GEMV                      */
 #define K3MOE_FFN_GEMV 1   /* CUDA-core GEMV kernels, 128-bit register loads (any shape);
                               each routed expert's weights are read once per call     */
-#define K3MOE_FFN_STREAM 2 /* one persistent CUDA-core kernel fed by 1-D TMA bulk copies
-                              into a shared-memory ring; needs H/32 and I/32 multiples of
-                              16 and H, I <= 8192 (else K3MOE_ERR_UNSUPPORTED)          */
+#define K3MOE_FFN_STREAM 2 /* the GEMV mode's arithmetic (bitwise the same h and Y) with the
+                              weight rows streamed by 1-D TMA bulk copies into a shared-
+                              memory ring, one persistent CTA per SM; needs H a multiple
+                              of 128 and at most 8192, and I at most 4800 (else
+                              K3MOE_ERR_UNSUPPORTED)                                   */
 #define K3MOE_FFN_GEMM 3   /* grouped GEMMs on the tcgen05 tensor cores (weights dequantised
                               exactly to bf16, fp32 accumulators in tensor memory) for
                               token chunks; needs H and 2I multiples of 128 and I a

@@ -73,11 +73,11 @@ CASES = [  # T, H, I, E, k: several tiles and ragged tails
 ]
 
 
-STREAM_CASES = [  # shapes the TMA-fed streaming kernels accept (H a multiple of 64, H and I <= 8192)
+STREAM_CASES = [  # shapes the TMA-fed streaming kernels accept (H a multiple of 128 up to 8192, I up to 4800)
     (1, 512, 512, 8, 2),
-    (4, 192, 96, 8, 2),         # rows shorter than a warp's 32 chunks, guarded loops
-    (70, 64, 32, 5, 3),         # smallest rows; 40+ tokens per expert: two g/u exchange groups
-    (2, 8192, 8192, 3, 2),      # largest rows: two- and three-stage rings
+    (4, 384, 96, 8, 2),         # rows shorter than a warp's 32 chunks, guarded loops
+    (70, 128, 32, 5, 3),        # smallest rows, 40+ tokens per expert
+    (2, 8192, 4096, 3, 2),      # long rows: the shortest rings (5 stages)
     (5, 512, 512, 8, 2),
     (37, 1024, 512, 24, 6),
     (130, 512, 1024, 7, 3),
@@ -144,7 +144,7 @@ def test_stream_mode_is_bitwise_the_gemv_mode(T, H, I, E, k):
 
 
 def test_stream_mode_refuses_unsupported_shape():
-    s = gen.Shape(2, 96, 64, 4, 1)  # H not a multiple of 64
+    s = gen.Shape(2, 96, 64, 4, 1)  # H not a multiple of 128
     assert k3.k3moe_workspace_bytes(s, k3.K3MOE_OP_EXPERT_FFN, k3.K3MOE_FFN_STREAM) == 0
     b = alloc_layer(s)
     with pytest.raises(k3.K3moeError) as ei:
