@@ -63,6 +63,8 @@ def parse():
                         "skewed, probe) into the line's workloads object")
     p.add_argument("--leg-steps", type=int, default=20, help="timed steps per extra workload (at most --steps)")
     p.add_argument("--leg-cpu-seconds", type=float, default=2.0, help="oracle sample budget per extra workload")
+    p.add_argument("--no-stack", action="store_true",
+                   help="skip the 92-layer decode over host-resident experts (63 GB of page-locked host memory)")
     return p.parse_args()
 
 
@@ -637,6 +639,76 @@ def run_router_leg(a, name, dev, ws, rank):
     return ent
 
 
+def run_stack_leg(a, dev, ws, budgets_gb=(8, 32, 64, 128), layers=92, physical=4, warm_tokens=6,
+                  timed_tokens=4):
+    """The pages' per-token expert workload: 92 MoE layers (I = 1536, 896 experts,
+    top-16, one token) whose experts live in page-locked host memory, through one
+    LRU arena of expert slots in HBM, at several arena budgets.  Per layer and
+    token the inputs are drawn from the generator (logits N(0, sigma 2), x N(0,1);
+    the attention that would produce them is not part of the path).  Reports
+    seconds per token, bytes read from host memory per token, raw and true
+    resident hit rates, and the host-to-arena copy rate."""
+    import torch
+
+    from mxfp4_expert_ffn_router_gb300.stack import CachedMoEStack, HostExpertStore
+    s = gen.Shape(1, 7168, 1536, 896, 16)
+
+    def fill(p, ptrs):
+        gen.fill_experts(s.H, s.I, 0, s.E, *ptrs, seed=gen.WEIGHT_SEED + p)
+
+    t0 = time.perf_counter()
+    store = HostExpertStore(s.H, s.I, s.E, physical, layers, fill, device=dev)
+    setup_s = time.perf_counter() - t0
+    n_in = 16
+    inputs = []
+    for i in range(n_in):
+        seed = 500 + i
+        lg = gen.normal_f32(seed, gen.stream(gen.KIND_LOGITS), s.E, 2.0).reshape(1, s.E)
+        x = gen.make_x(s, seed=seed)
+        inputs.append((torch.from_numpy(lg).to(dev), torch.from_numpy(x.view(np.int16)).to(dev)))
+    out = torch.empty((1, s.H), dtype=torch.bfloat16, device=dev)
+    be = expert_bytes(s)
+    res = {"layers": layers, "physical_layers_in_host_memory": physical,
+           "host_store_gb": store.bytes / 1e9, "host_store_setup_s": setup_s,
+           "expert_bytes": be, "requests_per_token": layers * s.k, "budgets": {}}
+    stream = torch.cuda.current_stream()
+    for gb in budgets_gb:
+        slots = int(gb * 1e9 // be)
+        stack = CachedMoEStack(s, store, slots, device=dev)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        tok_ms = []
+        for tkn in range(warm_tokens + timed_tokens):
+            if tkn == warm_tokens:
+                torch.cuda.synchronize()
+                before = stack.counters()
+            ev0.record(stream)
+            for l in range(layers):
+                lg, x = inputs[(tkn * layers + l) % n_in]
+                stack.layer(l, lg, x, out, stream=stream)
+            ev1.record(stream)
+            ev1.synchronize()
+            if tkn >= warm_tokens:
+                tok_ms.append(ev0.elapsed_time(ev1))
+        if int(stack.status.item()) != 0:
+            raise RuntimeError(f"stack: device status {int(stack.status.item())}")
+        after = stack.counters()
+        d = {key: after[key] - before[key] for key in after}
+        tot_ms = slowest_rank_ms(float(sum(tok_ms)), ws, dev)
+        res["budgets"][f"{gb}GB"] = {
+            "slots": slots, "s_per_token": tot_ms / 1e3 / timed_tokens,
+            "tokens_per_s": whole_job_rate(timed_tokens, tot_ms, ws),
+            "bytes_from_host_per_token": d["bytes_from_host"] / timed_tokens,
+            "requests_per_token": d["requests"] / timed_tokens,
+            "raw_hit_rate": d["raw_hits"] / max(1, d["requests"]),
+            "true_resident_hit_rate": d["true_resident_hits"] / max(1, d["requests"]),
+            "host_to_hbm_gbs": d["bytes_from_host"] / (tot_ms / 1e3) / 1e9,
+            "warm_tokens": warm_tokens, "timed_tokens": timed_tokens}
+        del stack
+        torch.cuda.empty_cache()
+    del store
+    return res
+
+
 LEGS = [("batch8", 0), ("batch8", 3), ("spec2", 1), ("spec2", 3), ("spec4", 1), ("spec4", 3),
         ("spec12", 1), ("spec12", 3), ("spec16", 1), ("spec16", 3),
         ("prefill", 0), ("prefill", 4), ("skewed", 0), ("skewed", 4), ("probe", 4), ("probe", 3)]
@@ -737,6 +809,10 @@ def run_gpu(a):
             torch.cuda.empty_cache()
         for name in ("decode", "batch8", "prefill"):
             workloads[f"router/{name}"] = run_router_leg(a, name, dev, ws, rank)
+        if not a.no_stack:
+            del W, Wl, experts
+            torch.cuda.empty_cache()
+            workloads["stack92/decode_i1536_host_experts"] = run_stack_leg(a, dev, ws)
     time.sleep(0.2)
     clk = clocks.stop()
     for ent in (workloads or {}).values():  # clocks seen during each workload's timed steps

@@ -249,6 +249,63 @@ int k3moe_quantize_mxfp4(int64_t n, const uint16_t *x, uint8_t *codes, uint8_t *
 int k3moe_combine(k3moe_shape s, const float *Y, const float *w, const int32_t *inv, uint16_t *out,
                   float *out_f32, k3moe_stream_t stream);
 
+/* Expert cache: MXFP4 experts resident in host memory, read by the GPU, and a
+ * least-recently-used arena of expert slots in device memory (no counterpart
+ * API on the pages; it follows the expert-cache design of "running a 2.78T
+ * model in 8 GB", section on the trunk and the expert cache: an LRU arena with
+ * a batch prefetch of the step's experts, and two hit counts -- raw hits, the
+ * expert is in the arena when the FFN asks for it, near 100% because of the
+ * prefetch; and TRUE resident hits, the expert stayed in the arena since the
+ * previous step, the measure of reads avoided).
+ *   slots      : expert slots in the arena, 1 .. 2^20; a step needs at least as
+ *                many as the distinct experts it routes to (else the step is
+ *                refused: K3MOE_DEV_BOUNDS, nothing copied)
+ *   arena      : caller-owned device memory of k3moe_cache_bytes(s, slots) bytes,
+ *                256-byte aligned; it holds the bookkeeping, four device tables
+ *                of E expert pointers and the slots.  Only s.H, s.I and s.E
+ *                matter for its size.
+ *   host_w     : the experts in host memory, in the layout of k3moe_weights: four
+ *                DEVICE-readable arrays of E pointers to host arrays that the GPU
+ *                can read (page-locked memory from cudaHostAlloc, or registered
+ *                with cudaHostRegister), each 16-byte aligned; NULL = absent
+ *   s          : the arena's shape: H, I and E = every expert it caches (up to
+ *                2^20: for a stack of layers, E = layers x experts per layer, and
+ *                expert l * E_layer + e is expert e of layer l); T and k unused
+ *   counts     : int32 [count_n] from k3moe_bucket: the step requests expert
+ *                count_base + i when counts[i] > 0 (a layer's slice of the arena's
+ *                experts); count_base + count_n <= E
+ *   stats      : device uint64 [4] accumulating requests, raw hits, true resident
+ *                hits and bytes copied host -> arena (zero it before the first
+ *                step), or NULL
+ * k3moe_cache_init marks every slot empty.  k3moe_cache_fetch makes every
+ * requested expert resident: hits stay; each miss, in ascending expert order,
+ * takes the least recently used slot that the step does not request (ties by
+ * slot index; empty slots first) and its four arrays are copied from host
+ * memory by a device kernel in the same stream (no host synchronisation).
+ * k3moe_cache_weights (host only, no device call) fills a k3moe_weights whose
+ * four device tables inside the arena point at the resident experts' slots
+ * (NULL for others): pass it to k3moe_expert_ffn after k3moe_cache_fetch (for
+ * layer l of a stack, offset each table by l * E_layer).  The
+ * arena's contents are the cache's state: steps on one arena must be ordered on
+ * one stream. */
+size_t k3moe_cache_bytes(k3moe_shape s, int slots);
+int k3moe_cache_weights(k3moe_shape s, int slots, void *arena, k3moe_weights *w);
+int k3moe_cache_init(k3moe_shape s, int slots, void *arena, size_t arena_bytes, k3moe_stream_t stream);
+int k3moe_cache_fetch(k3moe_shape s, int slots, void *arena, size_t arena_bytes, const k3moe_weights *host_w,
+                      const int32_t *counts, int32_t count_base, int32_t count_n, uint64_t *stats,
+                      int32_t *dev_status, k3moe_stream_t stream);
+
+/* Combine into a residual stream (a stack of MoE layers: x_next = x + MoE(x);
+ * the pages' engine adds each layer's routed experts into the residual stream):
+ * out_f32[t] = residual[t] + (sum_{j} w[t][j] * Y[inv[t*k+j]], fp32 in increasing
+ * j, as k3moe_combine), the residual added once after the sum; out[t] =
+ * bf16_rne(out_f32[t]).  residual : uint16 [T][H] bf16 bit patterns, 16-byte
+ * aligned; it may be the same buffer as out (each element is read before it is
+ * written, by the same thread).  Errors as k3moe_combine; NULL residual ->
+ * K3MOE_ERR_ARG. */
+int k3moe_combine_residual(k3moe_shape s, const float *Y, const float *w, const int32_t *inv, const uint16_t *residual,
+                           uint16_t *out, float *out_f32, k3moe_stream_t stream);
+
 /* Human-readable name of a k3moe_status value. */
 const char *k3moe_status_string(int code);
 

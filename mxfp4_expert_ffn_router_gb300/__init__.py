@@ -81,10 +81,21 @@ def lib():
             L.k3moe_expert_ffn_noalloc.restype = i32
             L.k3moe_expert_ffn_noalloc.argtypes = [Shape, vp, ctypes.POINTER(_WeightsC), vp, vp, vp, i32,
                                                    vp, vp]
+            L.k3moe_cache_bytes.restype = sz
+            L.k3moe_cache_bytes.argtypes = [Shape, i32]
+            L.k3moe_cache_weights.restype = i32
+            L.k3moe_cache_weights.argtypes = [Shape, i32, vp, ctypes.POINTER(_WeightsC)]
+            L.k3moe_cache_init.restype = i32
+            L.k3moe_cache_init.argtypes = [Shape, i32, vp, sz, vp]
+            L.k3moe_cache_fetch.restype = i32
+            L.k3moe_cache_fetch.argtypes = [Shape, i32, vp, sz, ctypes.POINTER(_WeightsC), vp, i32, i32, vp, vp,
+                                             vp]
             L.k3moe_quantize_mxfp4.restype = i32
             L.k3moe_quantize_mxfp4.argtypes = [ctypes.c_int64, vp, vp, vp, vp]
             L.k3moe_combine.restype = i32
             L.k3moe_combine.argtypes = [Shape, vp, vp, vp, vp, vp, vp]
+            L.k3moe_combine_residual.restype = i32
+            L.k3moe_combine_residual.argtypes = [Shape, vp, vp, vp, vp, vp, vp, vp]
             L.k3moe_status_string.restype = ctypes.c_char_p
             L.k3moe_status_string.argtypes = [i32]
             L.k3moe_last_cuda_error.restype = ctypes.c_char_p
@@ -214,6 +225,46 @@ def k3moe_expert_ffn_noalloc(shape, x, weights: Weights, offsets, perm, Y, mode=
     _check("k3moe_expert_ffn_noalloc", rc)
 
 
+class ExpertCache:
+    """Host-resident experts with a least-recently-used arena of expert slots in
+    device memory (k3moe_cache_*).  ``host`` is a Weights whose pointer tables
+    (device tensors) point at page-locked host arrays; ``arena`` is a uint8 CUDA
+    tensor of at least k3moe_cache_bytes(shape, slots) bytes."""
+
+    def __init__(self, shape, slots: int, host: "Weights", arena, stream=None):
+        self.shape, self.slots, self.host, self.arena = Shape.of(shape), int(slots), host, arena
+        self.nbytes = arena.numel() * arena.element_size()
+        _check("k3moe_cache_init", lib().k3moe_cache_init(self.shape, self.slots, _ptr(arena, torch.uint8, "arena"),
+                                                           self.nbytes, _stream(stream)))
+        wc = _WeightsC()
+        _check("k3moe_cache_weights", lib().k3moe_cache_weights(self.shape, self.slots, arena.data_ptr(),
+                                                                ctypes.byref(wc)))
+        self.weights = Weights.__new__(Weights)
+        self.weights.ptrs, self.weights.keep, self.weights._c = [], [arena], wc
+
+    @staticmethod
+    def bytes_needed(shape, slots: int) -> int:
+        return int(lib().k3moe_cache_bytes(Shape.of(shape), int(slots)))
+
+    def fetch(self, counts, base: int = 0, stats=None, dev_status=None, stream=None):
+        """Make the step's routed experts resident: expert base + i for counts[i] > 0
+        (counts: int32 from k3moe_bucket)."""
+        rc = lib().k3moe_cache_fetch(self.shape, self.slots, self.arena.data_ptr(), self.nbytes,
+                                     self.host.cstruct(), _ptr(counts, torch.int32, "counts"), int(base),
+                                     int(counts.numel()), _ptr(stats, torch.int64, "stats"),
+                                     _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+        _check("k3moe_cache_fetch", rc)
+
+    def layer_weights(self, layer: int, experts_per_layer: int) -> "Weights":
+        """The device tables of one layer of a stack (offset by layer * experts_per_layer)."""
+        w = Weights.__new__(Weights)
+        off = 8 * layer * experts_per_layer
+        c = self.weights._c
+        w.ptrs, w.keep = [], [self.arena]
+        w._c = _WeightsC(c.w13_codes + off, c.w13_scales + off, c.w2_codes + off, c.w2_scales + off)
+        return w
+
+
 def k3moe_quantize_mxfp4(x, codes, scales, stream=None):
     """MXFP4 quantisation of bf16 values x [n] (n a multiple of 32) into codes
     uint8 [n/2] (low nibble = even element) and E8M0 scales uint8 [n/32]."""
@@ -228,3 +279,12 @@ def k3moe_combine(shape, Y, w, inv, out, out_f32=None, stream=None):
                              _ptr(inv, torch.int32, "inv"), _ptr(out, _BF16, "out"),
                              _ptr(out_f32, torch.float32, "out_f32"), _stream(stream))
     _check("k3moe_combine", rc)
+
+
+def k3moe_combine_residual(shape, Y, w, inv, residual, out, out_f32=None, stream=None):
+    """out = bf16(residual + sum_j w[t, j] Y[inv[t k + j]]) (out may be residual)."""
+    rc = lib().k3moe_combine_residual(Shape.of(shape), _ptr(Y, torch.float32, "Y"), _ptr(w, torch.float32, "w"),
+                                      _ptr(inv, torch.int32, "inv"), _ptr(residual, _BF16, "residual"),
+                                      _ptr(out, _BF16, "out"), _ptr(out_f32, torch.float32, "out_f32"),
+                                      _stream(stream))
+    _check("k3moe_combine_residual", rc)

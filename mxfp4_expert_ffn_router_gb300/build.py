@@ -15,7 +15,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 OUT = os.path.join(HERE, "libk3moe.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 SOURCES = ["k3moe.cu", "route.cu", "bucket.cu", "ffn_gemv.cu", "ffn_stream.cu", "ffn_gemm.cu", "combine.cu",
-           "quant.cu", "k3moe_noalloc.cu", "router.cu"]
+           "quant.cu", "k3moe_noalloc.cu", "router.cu", "expert_cache.cu"]
 NVCC = os.environ.get("NVCC", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

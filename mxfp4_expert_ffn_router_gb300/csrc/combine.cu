@@ -10,10 +10,12 @@
 
 namespace k3moe {
 
+// residual (bf16 [T][H] or NULL): the sum is added to it once, after the j loop
+// (the residual stream of a stack of MoE layers: x_next = x + MoE(x)).
 __global__ void __launch_bounds__(256, 4)
     combine_kernel(const float *__restrict__ Y, const float *__restrict__ w,
                    const int32_t *__restrict__ inv, int T, int H, int k, int A,
-                   uint16_t *__restrict__ out, float *__restrict__ out_f32) {
+                   const uint16_t *residual, uint16_t *out, float *__restrict__ out_f32) {
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.y;
@@ -31,6 +33,13 @@ __global__ void __launch_bounds__(256, 4)
     acc.w = fmaf(wj, y.w, acc.w);
   }
   const size_t o = static_cast<size_t>(t) * H + 4 * c4;
+  if (residual) {
+    const uint2 r = *reinterpret_cast<const uint2 *>(residual + o);
+    acc.x += bf16_bits_to_f32(static_cast<uint16_t>(r.x & 0xFFFFu));
+    acc.y += bf16_bits_to_f32(static_cast<uint16_t>(r.x >> 16));
+    acc.z += bf16_bits_to_f32(static_cast<uint16_t>(r.y & 0xFFFFu));
+    acc.w += bf16_bits_to_f32(static_cast<uint16_t>(r.y >> 16));
+  }
   if (out_f32) *reinterpret_cast<float4 *>(out_f32 + o) = acc;
   const uint32_t lo = f32_to_bf16_rne(acc.x) | (static_cast<uint32_t>(f32_to_bf16_rne(acc.y)) << 16);
   const uint32_t hi = f32_to_bf16_rne(acc.z) | (static_cast<uint32_t>(f32_to_bf16_rne(acc.w)) << 16);
@@ -38,10 +47,10 @@ __global__ void __launch_bounds__(256, 4)
 }
 
 int launch_combine(const k3moe_shape &s, const float *Y, const float *w, const int32_t *inv,
-                   uint16_t *out, float *out_f32, cudaStream_t st) {
+                   const uint16_t *residual, uint16_t *out, float *out_f32, cudaStream_t st) {
   if (s.T == 0) return 0;
   const dim3 grid((s.H / 4 + 255) / 256, s.T), block(256);
-  return launch_pdl(combine_kernel, grid, block, 0, st, Y, w, inv, s.T, s.H, s.k, s.T * s.k, out,
+  return launch_pdl(combine_kernel, grid, block, 0, st, Y, w, inv, s.T, s.H, s.k, s.T * s.k, residual, out,
                     out_f32) == cudaSuccess
              ? 0
              : -1;

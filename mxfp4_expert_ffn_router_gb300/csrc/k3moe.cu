@@ -170,6 +170,57 @@ int k3moe_expert_ffn(k3moe_shape s, const uint16_t *x, const k3moe_weights *w, c
   return abi_launched(k3moe::launch_ffn_gemv(s, x, *w, offsets, perm, Y, ws, dev_status, st));
 }
 
+// The cache's shape may cache several layers' experts: E up to 2^20 (the
+// per-call shape rule E <= 4096 applies to the layer calls, not to the arena).
+static int cache_check_shape(const k3moe_shape &s) {
+  if (s.E < 1 || s.E > (1 << 20) || s.T < 0 || s.k < 1 || s.k > 32) return K3MOE_ERR_SHAPE;
+  if (s.H < 32 || s.H > 16384 || s.H % 32 || s.I < 32 || s.I > 16384 || s.I % 32) return K3MOE_ERR_SHAPE;
+  return K3MOE_OK;
+}
+
+size_t k3moe_cache_bytes(k3moe_shape s, int slots) {
+  if (cache_check_shape(s) != K3MOE_OK || slots < 1 || slots > (1 << 20)) return 0;
+  return k3moe::cache_arena_bytes(s, slots);
+}
+
+int k3moe_cache_weights(k3moe_shape s, int slots, void *arena, k3moe_weights *w) {
+  int rc = cache_check_shape(s);
+  if (rc) return rc;
+  if (slots < 1 || slots > (1 << 20)) return K3MOE_ERR_SHAPE;
+  if (!arena || !w) return K3MOE_ERR_ARG;
+  k3moe::cache_tables(s, slots, arena, w);
+  return K3MOE_OK;
+}
+
+int k3moe_cache_init(k3moe_shape s, int slots, void *arena, size_t arena_bytes, k3moe_stream_t stream) {
+  int rc = cache_check_shape(s);
+  if (rc) return rc;
+  if (slots < 1 || slots > (1 << 20)) return K3MOE_ERR_SHAPE;
+  if (!arena) return K3MOE_ERR_ARG;
+  if (arena_bytes < k3moe::cache_arena_bytes(s, slots) || (reinterpret_cast<uintptr_t>(arena) & 255u))
+    return K3MOE_ERR_WORKSPACE;
+  if ((rc = abi_check_arch())) return rc;
+  return abi_launched(k3moe::launch_cache_init(s, slots, arena, reinterpret_cast<k3moe_stream>(stream)));
+}
+
+int k3moe_cache_fetch(k3moe_shape s, int slots, void *arena, size_t arena_bytes, const k3moe_weights *host_w,
+                      const int32_t *counts, int32_t count_base, int32_t count_n, uint64_t *stats,
+                      int32_t *dev_status, k3moe_stream_t stream) {
+  int rc = cache_check_shape(s);
+  if (rc) return rc;
+  if (slots < 1 || slots > (1 << 20)) return K3MOE_ERR_SHAPE;
+  if (count_base < 0 || count_n < 0 || count_base > s.E - count_n) return K3MOE_ERR_SHAPE;
+  if (count_n == 0) return K3MOE_OK;
+  if (!arena || !host_w || !counts) return K3MOE_ERR_ARG;
+  if (!host_w->w13_codes || !host_w->w13_scales || !host_w->w2_codes || !host_w->w2_scales) return K3MOE_ERR_ARG;
+  if (arena_bytes < k3moe::cache_arena_bytes(s, slots) || (reinterpret_cast<uintptr_t>(arena) & 255u))
+    return K3MOE_ERR_WORKSPACE;
+  if ((rc = abi_check_arch())) return rc;
+  return abi_launched(k3moe::launch_cache_fetch(s, slots, arena, *host_w, counts, count_base, count_n,
+                                                reinterpret_cast<unsigned long long *>(stats), dev_status,
+                                                reinterpret_cast<k3moe_stream>(stream)));
+}
+
 int k3moe_quantize_mxfp4(int64_t n, const uint16_t *x, uint8_t *codes, uint8_t *scales, k3moe_stream_t stream) {
   if (n < 0 || n % 32) return K3MOE_ERR_SHAPE;
   if (n == 0) return K3MOE_OK;
@@ -189,7 +240,21 @@ int k3moe_combine(k3moe_shape s, const float *Y, const float *w, const int32_t *
   if (!Y || !w || !inv || !out) return K3MOE_ERR_ARG;
   if (!aligned16(Y) || !aligned16(out) || (out_f32 && !aligned16(out_f32))) return K3MOE_ERR_ALIGN;
   if ((rc = abi_check_arch())) return rc;
-  return abi_launched(k3moe::launch_combine(s, Y, w, inv, out, out_f32, reinterpret_cast<k3moe_stream>(stream)));
+  return abi_launched(
+      k3moe::launch_combine(s, Y, w, inv, nullptr, out, out_f32, reinterpret_cast<k3moe_stream>(stream)));
+}
+
+int k3moe_combine_residual(k3moe_shape s, const float *Y, const float *w, const int32_t *inv, const uint16_t *residual,
+                           uint16_t *out, float *out_f32, k3moe_stream_t stream) {
+  int rc = abi_check_shape(s);
+  if (rc) return rc;
+  if (s.T == 0) return K3MOE_OK;
+  if (!Y || !w || !inv || !residual || !out) return K3MOE_ERR_ARG;
+  if (!aligned16(Y) || !aligned16(out) || !aligned16(residual) || (out_f32 && !aligned16(out_f32)))
+    return K3MOE_ERR_ALIGN;
+  if ((rc = abi_check_arch())) return rc;
+  return abi_launched(
+      k3moe::launch_combine(s, Y, w, inv, residual, out, out_f32, reinterpret_cast<k3moe_stream>(stream)));
 }
 
 const char *k3moe_last_cuda_error(void) { return t_last_cuda_error; }

@@ -80,8 +80,14 @@ bool make_row_map(CUtensorMap *m, void *base, int rows, int K);
 int launch_router(const k3moe_shape &s, const uint16_t *x, const uint16_t *wr, float *logits, int32_t *idx,
                   float *w, int32_t *status, cudaStream_t st);
 bool router_gemm_supported(const k3moe_shape &s);
+size_t cache_arena_bytes(const k3moe_shape &s, int slots);
+void cache_tables(const k3moe_shape &s, int slots, void *arena, k3moe_weights *out);
+int launch_cache_init(const k3moe_shape &s, int slots, void *arena, cudaStream_t st);
+int launch_cache_fetch(const k3moe_shape &s, int slots, void *arena, const k3moe_weights &host_w,
+                       const int32_t *counts, int cbase, int cn, unsigned long long *stats, int32_t *status,
+                       cudaStream_t st);
 int launch_quantize_mxfp4(long long n, const uint16_t *x, uint8_t *codes, uint8_t *scales, cudaStream_t st);
 int launch_combine(const k3moe_shape &s, const float *Y, const float *w, const int32_t *inv,
-                   uint16_t *out, float *out_f32, cudaStream_t st);
+                   const uint16_t *residual, uint16_t *out, float *out_f32, cudaStream_t st);
 
 }  // namespace k3moe

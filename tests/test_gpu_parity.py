@@ -1,8 +1,11 @@
 """GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
 
 Bars: expert indices, counts, offsets, perm and inv bit-exact; routing weights
-within 1 fp32 ulp of the oracle; Y and the fp32 output within
-max|err| <= 2e-3 * RMS(reference); the bf16 output equal to RNE(fp32 output)."""
+within 1 fp32 ulp of the oracle; the FFN staged at its bf16 rounding of h
+(ffn_check): every GPU h element a bf16 rounding of a value within the kernel's
+fp32 summation bound of the exact silu(g) u, then Y and the fp32 output within
+max|err| <= 2e-3 * RMS of the oracle applied to the GPU's h; the bf16 output
+equal to RNE(fp32 output)."""
 import numpy as np
 import pytest
 import torch
