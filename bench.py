@@ -47,7 +47,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--config", default="decode", choices=sorted(gen.CONFIGS))
     p.add_argument("--impl", default="k3moe", choices=["k3moe", "reference"])
-    p.add_argument("--mode", type=int, default=0, help="expert FFN mode (0 auto, 1 gemv, 2 stream, 3 gemm, 4 w4a4)")
+    p.add_argument("--mode", type=int, default=0, help="expert FFN mode (0 auto, 1 gemv, 3 gemm, 4 w4a4; 2, the retired stream mode, runs gemv)")
     p.add_argument("--sets", type=int, default=64, help="rotating input sets")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -347,6 +347,8 @@ def l2_policy(a, s, sets):
 
 def resolved_mode(s, mode):
     """The expert FFN mode the library resolves AUTO (0) to for this shape."""
+    if mode == 2:
+        return 1  # the retired STREAM mode runs the GEMV kernels
     if mode != 0:
         return mode
     A = s.T * s.k
@@ -356,14 +358,13 @@ def resolved_mode(s, mode):
 
 def ffn_kernel_count(s, mode):
     """Kernels one k3moe_expert_ffn call launches."""
-    return {1: 4, 2: 2, 3: 6, 4: 6}[resolved_mode(s, mode)]
+    return {1: 4, 3: 6, 4: 6}[resolved_mode(s, mode)]
 
 
 def ffn_kernel_label(s, mode):
     """The kernels of one k3moe_expert_ffn call in the mode the library resolves."""
     mode = resolved_mode(s, mode)
     return {1: "k3moe_expert_ffn, GEMV mode (gemv_prep + gemv_rows gate/up + gemv_h16 + gemv_rows down)",
-            2: "k3moe_expert_ffn, STREAM mode (stream_prep + ffn_stream_kernel)",
             3: "k3moe_expert_ffn, GEMM mode (gemm_prep + gemm_sched + rows_to_f16 + ffn_gemm_kernel gate/up "
                "+ rows_to_f16 + ffn_gemm_kernel down; kind::f16 after in-kernel e2m1 dequantisation)",
             4: "k3moe_expert_ffn, W4A4 mode (gemm_prep + gemm_sched + rows_to_mxfp4 + ffn_gemm_mxf4_kernel "
@@ -437,7 +438,7 @@ def per_expert_roofline_s(s, counts, mode):
 
 
 def mode_name(s, mode):
-    return {1: "gemv", 2: "stream", 3: "gemm_w4a16", 4: "w4a4"}[resolved_mode(s, mode)]
+    return {1: "gemv", 3: "gemm_w4a16", 4: "w4a4"}[resolved_mode(s, mode)]
 
 
 # ----------------------------------------------------------------------------- GPU arm

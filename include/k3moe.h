@@ -101,11 +101,10 @@ typedef struct {
                               and the shape allows it, else GEMV                      */
 #define K3MOE_FFN_GEMV 1   /* CUDA-core GEMV kernels, 128-bit register loads (any shape);
                               each routed expert's weights are read once per call     */
-#define K3MOE_FFN_STREAM 2 /* the GEMV mode's arithmetic (bitwise the same h and Y) with the
-                              weight rows streamed by 1-D TMA bulk copies into a shared-
-                              memory ring, one persistent CTA per SM; needs H a multiple
-                              of 128 and at most 8192, and I at most 4800 (else
-                              K3MOE_ERR_UNSUPPORTED)                                   */
+#define K3MOE_FFN_STREAM 2 /* retired: served by the GEMV kernels (kept so that callers
+                              passing it keep working); a shared-memory ring fed by
+                              1-D TMA bulk copies was measured slower than the
+                              register-pipelined GEMV kernels                           */
 #define K3MOE_FFN_GEMM 3   /* grouped GEMMs on the tcgen05 tensor cores (weights dequantised
                               exactly to bf16, fp32 accumulators in tensor memory) for
                               token chunks; needs H and 2I multiples of 128 and I a
@@ -202,14 +201,14 @@ int k3moe_expert_ffn(k3moe_shape s, const uint16_t *x, const k3moe_weights *w,
  * minus ws/ws_bytes; its scratch is a file-scope device array of
  * K3MOE_NOALLOC_SCRATCH_BYTES that every GPU loading the library keeps until the
  * process exits.  It calls no allocation routine.
- *  - Modes: it serves the CUDA-core kernels only.  K3MOE_FFN_AUTO means
- *    K3MOE_FFN_GEMV here (k3moe_expert_ffn's AUTO may pick the tensor-core GEMM
- *    for the same shape, so the two entry points can then differ within the
- *    parity tolerance, not bitwise); K3MOE_FFN_GEMV and K3MOE_FFN_STREAM compute
- *    bitwise what k3moe_expert_ffn computes in the same mode.  K3MOE_FFN_GEMM and
- *    K3MOE_FFN_W4A4 return K3MOE_ERR_UNSUPPORTED; other values K3MOE_ERR_ARG.
+ *  - Modes: it serves the CUDA-core GEMV kernels only.  K3MOE_FFN_AUTO (and
+ *    K3MOE_FFN_STREAM) mean K3MOE_FFN_GEMV here (k3moe_expert_ffn's AUTO may pick
+ *    the tensor-core GEMM for the same shape, so the two entry points can then
+ *    differ within the parity tolerance, not bitwise); in GEMV mode it computes
+ *    bitwise what k3moe_expert_ffn computes.  K3MOE_FFN_GEMM and K3MOE_FFN_W4A4
+ *    return K3MOE_ERR_UNSUPPORTED; other values K3MOE_ERR_ARG.
  *  - Limit: a problem whose scratch, k3moe_workspace_bytes(s, K3MOE_OP_EXPERT_FFN,
- *    K3MOE_FFN_GEMV) (STREAM: ..., K3MOE_FFN_STREAM), exceeds
+ *    K3MOE_FFN_GEMV), exceeds
  *    K3MOE_NOALLOC_SCRATCH_BYTES returns K3MOE_ERR_NOALLOC_LIMIT and launches
  *    nothing (decode-sized batches fit; large prefill chunks do not).
  *  - The first call on a device looks up the array's device address with that

@@ -14,7 +14,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 OUT = os.path.join(HERE, "libk3moe.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["k3moe.cu", "route.cu", "bucket.cu", "ffn_gemv.cu", "ffn_stream.cu", "ffn_gemm.cu", "combine.cu",
+SOURCES = ["k3moe.cu", "route.cu", "bucket.cu", "ffn_gemv.cu", "ffn_gemm.cu", "combine.cu",
            "quant.cu", "k3moe_noalloc.cu", "router.cu", "expert_cache.cu"]
 NVCC = os.environ.get("NVCC", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -80,7 +80,7 @@ static int resolve_ffn_mode(const k3moe_shape &s, int mode) {
       return K3MOE_FFN_GEMV;
     }
     case K3MOE_FFN_GEMV: return K3MOE_FFN_GEMV;
-    case K3MOE_FFN_STREAM: return k3moe::ffn_stream_supported(s) ? K3MOE_FFN_STREAM : -1;
+    case K3MOE_FFN_STREAM: return K3MOE_FFN_GEMV;  // retired: the GEMV kernels serve it
     case K3MOE_FFN_GEMM: return k3moe::ffn_gemm_supported(s) ? K3MOE_FFN_GEMM : -1;
     case K3MOE_FFN_W4A4: return k3moe::ffn_gemm_supported(s) ? K3MOE_FFN_W4A4 : -1;
     default: return -1;
@@ -88,7 +88,6 @@ static int resolve_ffn_mode(const k3moe_shape &s, int mode) {
 }
 
 static size_t ffn_workspace(const k3moe_shape &s, int resolved) {
-  if (resolved == K3MOE_FFN_STREAM) return k3moe::ffn_stream_workspace(s);
   if (resolved == K3MOE_FFN_GEMV) return k3moe::ffn_gemv_workspace(s);
   if (resolved == K3MOE_FFN_GEMM || resolved == K3MOE_FFN_W4A4) return k3moe::ffn_gemm_workspace(s);
   return 0;
@@ -98,7 +97,6 @@ size_t k3moe_workspace_h_offset(k3moe_shape s, int mode) {
   if (abi_check_shape(s) != K3MOE_OK) return static_cast<size_t>(-1);
   const int resolved = resolve_ffn_mode(s, mode);
   if (resolved == K3MOE_FFN_GEMV) return k3moe::ffn_gemv_h_offset(s);
-  if (resolved == K3MOE_FFN_STREAM) return k3moe::ffn_stream_h_offset(s);
   if (resolved == K3MOE_FFN_GEMM || resolved == K3MOE_FFN_W4A4) return k3moe::ffn_gemm_h_offset(s);
   return static_cast<size_t>(-1);
 }
@@ -162,8 +160,6 @@ int k3moe_expert_ffn(k3moe_shape s, const uint16_t *x, const k3moe_weights *w, c
   if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u)) return K3MOE_ERR_WORKSPACE;
   if ((rc = abi_check_arch())) return rc;
   const cudaStream_t st = reinterpret_cast<k3moe_stream>(stream);
-  if (resolved == K3MOE_FFN_STREAM)
-    return abi_launched(k3moe::launch_ffn_stream(s, x, *w, offsets, perm, Y, ws, dev_status, st));
   if (resolved == K3MOE_FFN_GEMM || resolved == K3MOE_FFN_W4A4)
     return abi_launched(k3moe::launch_ffn_gemm(s, x, *w, offsets, perm, Y, ws, dev_status, st,
                                            resolved == K3MOE_FFN_W4A4));

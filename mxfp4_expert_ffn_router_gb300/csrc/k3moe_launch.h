@@ -46,7 +46,7 @@ int launch_ffn_gemv(const k3moe_shape &s, const uint16_t *x, const k3moe_weights
                     const int32_t *offsets, const int32_t *perm, float *Y, void *ws,
                     int32_t *status, cudaStream_t st);
 // The GEMV mode's workspace pieces, and its front (active slots, x to prescaled
-// f16) and middle (h to prescaled f16) kernels, shared with the STREAM mode.
+// f16) and middle (h to prescaled f16) kernels.
 struct GemvBufs {
   int4 *slots;      // {expert, first bucket position, tokens, present} per active slot
   int32_t *meta;    // [0] = active slots
@@ -62,12 +62,6 @@ int launch_gemv_prep(const k3moe_shape &s, const uint16_t *x, const k3moe_weight
                      const GemvBufs &b, int32_t *status, cudaStream_t st);
 int launch_gemv_h16(const k3moe_shape &s, const GemvBufs &b, cudaStream_t st);
 int sm_count();
-size_t ffn_stream_workspace(const k3moe_shape &s);
-size_t ffn_stream_h_offset(const k3moe_shape &s);
-bool ffn_stream_supported(const k3moe_shape &s);
-int launch_ffn_stream(const k3moe_shape &s, const uint16_t *x, const k3moe_weights &w,
-                      const int32_t *offsets, const int32_t *perm, float *Y, void *ws,
-                      int32_t *status, cudaStream_t st);
 size_t ffn_gemm_workspace(const k3moe_shape &s);
 size_t ffn_gemm_h_offset(const k3moe_shape &s);
 bool ffn_gemm_supported(const k3moe_shape &s);

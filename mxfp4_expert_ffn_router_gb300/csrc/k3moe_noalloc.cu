@@ -11,8 +11,8 @@
 // K3MOE_NOALLOC_SCRATCH_BYTES that every GPU which loads this library holds
 // until the process exits.
 //
-// It serves the CUDA-core modes only (GEMV, STREAM; AUTO means GEMV): those are
-// the decode-sized paths whose scratch fits the array.  GEMM and W4A4 return
+// It serves the CUDA-core GEMV kernels only (AUTO and STREAM mean GEMV): the
+// decode-sized path whose scratch fits the array.  GEMM and W4A4 return
 // K3MOE_ERR_UNSUPPORTED.
 #include <cuda_runtime.h>
 
@@ -62,14 +62,11 @@ extern "C" int k3moe_expert_ffn_noalloc(k3moe_shape s, const uint16_t *x, const 
   if (rc) return rc;
   if (mode < K3MOE_FFN_AUTO || mode > K3MOE_FFN_W4A4) return K3MOE_ERR_ARG;
   if (mode == K3MOE_FFN_GEMM || mode == K3MOE_FFN_W4A4) return K3MOE_ERR_UNSUPPORTED;
-  const int resolved = mode == K3MOE_FFN_AUTO ? K3MOE_FFN_GEMV : mode;
-  if (resolved == K3MOE_FFN_STREAM && !k3moe::ffn_stream_supported(s)) return K3MOE_ERR_UNSUPPORTED;
   if (s.T == 0) return K3MOE_OK;
   if (!x || !w || !offsets || !perm || !Y) return K3MOE_ERR_ARG;
   if (!w->w13_codes || !w->w13_scales || !w->w2_codes || !w->w2_scales) return K3MOE_ERR_ARG;
   if (!aligned16(x) || !aligned16(Y)) return K3MOE_ERR_ALIGN;
-  const size_t need =
-      resolved == K3MOE_FFN_STREAM ? k3moe::ffn_stream_workspace(s) : k3moe::ffn_gemv_workspace(s);
+  const size_t need = k3moe::ffn_gemv_workspace(s);
   if (need > K3MOE_NOALLOC_SCRATCH_BYTES) return K3MOE_ERR_NOALLOC_LIMIT;
   if ((rc = k3moe::abi_check_arch())) return rc;
   void *ws = nullptr;
@@ -77,7 +74,5 @@ extern "C" int k3moe_expert_ffn_noalloc(k3moe_shape s, const uint16_t *x, const 
   // Nothing in the scratch has to start at zero: the first kernel of each call
   // (the prep kernel) writes every counter, table and maximum the call reads.
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  return k3moe::abi_launched(resolved == K3MOE_FFN_STREAM
-                                 ? k3moe::launch_ffn_stream(s, x, *w, offsets, perm, Y, ws, dev_status, st)
-                                 : k3moe::launch_ffn_gemv(s, x, *w, offsets, perm, Y, ws, dev_status, st));
+  return k3moe::abi_launched(k3moe::launch_ffn_gemv(s, x, *w, offsets, perm, Y, ws, dev_status, st));
 }

@@ -39,7 +39,7 @@ def _setup(T, H, I, E, k, mode):
 
 @pytest.mark.parametrize("T,H,I,E,k,mode", [
     (1, 7168, 2048, 32, 16, k3.K3MOE_FFN_AUTO),    # decode-sized: AUTO picks the GEMV kernels
-    (5, 512, 512, 8, 2, k3.K3MOE_FFN_STREAM),
+    (5, 512, 512, 8, 2, k3.K3MOE_FFN_STREAM),      # the retired STREAM mode: the GEMV kernels
     (4, 128, 64, 8, 2, k3.K3MOE_FFN_AUTO),         # the GEMV kernels
     (8, 7168, 2048, 48, 16, k3.K3MOE_FFN_GEMV),
 ])
