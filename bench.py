@@ -64,7 +64,7 @@ def parse():
     p.add_argument("--leg-steps", type=int, default=20, help="timed steps per extra workload (at most --steps)")
     p.add_argument("--leg-cpu-seconds", type=float, default=2.0, help="oracle sample budget per extra workload")
     p.add_argument("--no-stack", action="store_true",
-                   help="skip the 92-layer decode over host-resident experts (63 GB of page-locked host memory)")
+                   help="skip the 92-layer decode over host-resident experts (31 GB of page-locked host memory)")
     return p.parse_args()
 
 
@@ -361,6 +361,16 @@ def ffn_kernel_count(s, mode):
     return {1: 4, 3: 6, 4: 6}[resolved_mode(s, mode)]
 
 
+def layer_kernel_count(s, mode):
+    """Kernels one k3moe_layer call launches: the single-block front (route, bucket
+    and GEMV prep) + gate/up + h16 + down + combine for small GEMV batches, else
+    route + bucket (1 or 3) + the expert FFN's kernels + combine."""
+    A = s.T * s.k
+    if resolved_mode(s, mode) == 1 and s.T <= 32 and s.E <= 1024 and A <= 512:
+        return 5
+    return 1 + (1 if A <= 4096 else 3) + ffn_kernel_count(s, mode) + 1
+
+
 def ffn_kernel_label(s, mode):
     """The kernels of one k3moe_expert_ffn call in the mode the library resolves."""
     mode = resolved_mode(s, mode)
@@ -472,22 +482,31 @@ class LayerBench:
                                device=dev)
         self.wsf = torch.empty(max(1, k3.k3moe_workspace_bytes(s, k3.K3MOE_OP_EXPERT_FFN, mode)),
                                dtype=torch.uint8, device=dev)
+        self.wsl = torch.empty(max(1, k3.k3moe_workspace_bytes(s, k3.K3MOE_OP_LAYER, mode)),
+                               dtype=torch.uint8, device=dev)
         self.Y = torch.empty((A, s.H), dtype=f32, device=dev)
         self.out = torch.empty((s.T, s.H), dtype=torch.bfloat16, device=dev)
         self.do_flush, self.l2_mode = l2_policy(a, s, self.sets)
         self.do_flush = self.do_flush or flush_always
         self.flush = torch.empty(L2_FLUSH_BYTES if self.do_flush else 1, dtype=torch.uint8, device=dev)
         self.stream = torch.cuda.current_stream()
-        self.launches_per_step = 1 + (1 if A <= 4096 else 3) + ffn_kernel_count(s, mode) + 1
+        self.launches_per_step = layer_kernel_count(s, mode)
 
     def layer(self, i, ev=None, phases=False):
-        """One step; ev[0] / ev[3] bracket it, ev[1] / ev[2] (phases only) bracket
-        the expert FFN call.  Events between calls end the launch overlap of the
-        kernels around them, so the step timing records only the outer two."""
+        """One step; ev[0] / ev[3] bracket it.  A timed step is one k3moe_layer
+        call; with phases the four calls run instead, with ev[1] / ev[2]
+        bracketing the expert FFN call (events between calls end the launch
+        overlap of the kernels around them, so only the phase pass has them)."""
         k3, s, st, stream = self.k3, self.s, self.st, self.stream
         j = i % self.nsets
         if ev is not None:
             ev[0].record(stream)
+        if not phases:
+            k3.k3moe_layer(s, self.logits_d[j], self.x_d[j], self.W, self.idx, self.w, self.cnt, self.offsets,
+                           self.perm, self.inv, self.Y, self.out, None, self.mode, self.wsl, st, stream=stream)
+            if ev is not None:
+                ev[3].record(stream)
+            return
         k3.k3moe_route(s, self.logits_d[j], self.idx, self.w, st, stream=stream)
         k3.k3moe_bucket(s, self.idx, self.cnt, self.offsets, self.perm, self.inv, self.wsb, st, stream=stream)
         if phases:
@@ -640,7 +659,7 @@ def run_router_leg(a, name, dev, ws, rank):
     return ent
 
 
-def run_stack_leg(a, dev, ws, budgets_gb=(8, 32, 64, 128), layers=92, physical=4, warm_tokens=6,
+def run_stack_leg(a, dev, ws, budgets_gb=(8, 32, 64, 128), layers=92, physical=2, warm_tokens=6,
                   timed_tokens=4):
     """The pages' per-token expert workload: 92 MoE layers (I = 1536, 896 experts,
     top-16, one token) whose experts live in page-locked host memory, through one
@@ -779,10 +798,8 @@ def run_gpu(a):
             ev0.record(stream)
             lg_dev.copy_(lg_h[j], non_blocking=True)
             x_dev.copy_(x_h[j], non_blocking=True)
-            k3.k3moe_route(s, lg_dev, lb.idx, lb.w, lb.st, stream=stream)
-            k3.k3moe_bucket(s, lb.idx, lb.cnt, lb.offsets, lb.perm, lb.inv, lb.wsb, lb.st, stream=stream)
-            k3.k3moe_expert_ffn(s, x_dev, W, lb.offsets, lb.perm, lb.Y, a.mode, lb.wsf, lb.st, stream=stream)
-            k3.k3moe_combine(s, lb.Y, lb.w, lb.inv, lb.out, None, stream=stream)
+            k3.k3moe_layer(s, lg_dev, x_dev, W, lb.idx, lb.w, lb.cnt, lb.offsets, lb.perm, lb.inv, lb.Y, lb.out,
+                           None, a.mode, lb.wsl, lb.st, stream=stream)
             out_h.copy_(lb.out, non_blocking=True)
             ev1.record(stream)
             ev1.synchronize()

@@ -121,6 +121,7 @@ typedef struct {
 /* Workspace queries (bytes; 0 when the call needs none).  op is one of: */
 #define K3MOE_OP_BUCKET 1
 #define K3MOE_OP_EXPERT_FFN 2
+#define K3MOE_OP_LAYER 3
 size_t k3moe_workspace_bytes(k3moe_shape s, int op, int mode);
 /* Where the expert FFN leaves h: after a k3moe_expert_ffn call with shape s and
  * mode, its workspace holds h = bf16_rne(silu(g) * u) -- the GLU expert's one
@@ -293,6 +294,20 @@ int k3moe_cache_init(k3moe_shape s, int slots, void *arena, size_t arena_bytes, 
 int k3moe_cache_fetch(k3moe_shape s, int slots, void *arena, size_t arena_bytes, const k3moe_weights *host_w,
                       const int32_t *counts, int32_t count_base, int32_t count_n, uint64_t *stats,
                       int32_t *dev_status, k3moe_stream_t stream);
+
+/* The whole layer in one call: k3moe_route, k3moe_bucket, k3moe_expert_ffn and
+ * k3moe_combine on `stream`, with the same arguments, outputs and results (bit
+ * for bit) as the four calls; every intermediate (idx, wts, counts, offsets,
+ * perm, inv, Y) is written as those calls write it.  The workspace, of
+ * k3moe_workspace_bytes(s, K3MOE_OP_LAYER, mode) bytes (256-byte aligned),
+ * serves the bucketing and the expert FFN in turn.  When the FFN runs the GEMV
+ * kernels and the batch is small (T <= 32, E <= 1024, T*k <= 512) the route,
+ * the bucketing and the FFN's preparation run as one single-block kernel: a
+ * decode step is then five launches instead of seven.  Errors: the union of the
+ * four calls'. */
+int k3moe_layer(k3moe_shape s, const float *logits, const uint16_t *x, const k3moe_weights *w, int32_t *idx,
+                float *wts, int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv, float *Y, uint16_t *out,
+                float *out_f32, int mode, void *ws, size_t ws_bytes, int32_t *dev_status, k3moe_stream_t stream);
 
 /* Combine into a residual stream (a stack of MoE layers: x_next = x + MoE(x);
  * the pages' engine adds each layer's routed experts into the residual stream):

@@ -25,7 +25,7 @@ K3MOE_ERR_NOALLOC_LIMIT = -8
 K3MOE_NOALLOC_SCRATCH_BYTES = 8 << 20
 K3MOE_DEV_NONFINITE, K3MOE_DEV_BOUNDS, K3MOE_DEV_TIMEOUT = 1, 2, 4
 K3MOE_FFN_AUTO, K3MOE_FFN_GEMV, K3MOE_FFN_STREAM, K3MOE_FFN_GEMM, K3MOE_FFN_W4A4 = 0, 1, 2, 3, 4
-K3MOE_OP_BUCKET, K3MOE_OP_EXPERT_FFN = 1, 2
+K3MOE_OP_BUCKET, K3MOE_OP_EXPERT_FFN, K3MOE_OP_LAYER = 1, 2, 3
 
 
 class K3moeError(RuntimeError):
@@ -96,6 +96,9 @@ def lib():
             L.k3moe_combine.argtypes = [Shape, vp, vp, vp, vp, vp, vp]
             L.k3moe_combine_residual.restype = i32
             L.k3moe_combine_residual.argtypes = [Shape, vp, vp, vp, vp, vp, vp, vp]
+            L.k3moe_layer.restype = i32
+            L.k3moe_layer.argtypes = [Shape, vp, vp, ctypes.POINTER(_WeightsC), vp, vp, vp, vp, vp, vp, vp, vp, vp, i32,
+                                      vp, sz, vp, vp]
             L.k3moe_status_string.restype = ctypes.c_char_p
             L.k3moe_status_string.argtypes = [i32]
             L.k3moe_last_cuda_error.restype = ctypes.c_char_p
@@ -288,3 +291,18 @@ def k3moe_combine_residual(shape, Y, w, inv, residual, out, out_f32=None, stream
                                       _ptr(out, _BF16, "out"), _ptr(out_f32, torch.float32, "out_f32"),
                                       _stream(stream))
     _check("k3moe_combine_residual", rc)
+
+
+def k3moe_layer(shape, logits, x, weights: Weights, idx, w, counts, offsets, perm, inv, Y, out, out_f32=None,
+                mode=K3MOE_FFN_AUTO, ws=None, dev_status=None, stream=None):
+    """route -> bucket -> expert FFN -> combine in one call (one workspace of
+    k3moe_workspace_bytes(shape, K3MOE_OP_LAYER, mode) bytes)."""
+    ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
+    rc = lib().k3moe_layer(Shape.of(shape), _ptr(logits, torch.float32, "logits"), _ptr(x, _BF16, "x"),
+                           weights.cstruct(), _ptr(idx, torch.int32, "idx"), _ptr(w, torch.float32, "w"),
+                           _ptr(counts, torch.int32, "counts"), _ptr(offsets, torch.int32, "offsets"),
+                           _ptr(perm, torch.int32, "perm"), _ptr(inv, torch.int32, "inv"), _ptr(Y, torch.float32, "Y"),
+                           _ptr(out, _BF16, "out"), _ptr(out_f32, torch.float32, "out_f32"), mode,
+                           _ptr(ws, None, "ws"), ws_bytes, _ptr(dev_status, torch.int32, "dev_status"),
+                           _stream(stream))
+    _check("k3moe_layer", rc)

@@ -677,6 +677,231 @@ int sm_count() {
   return nsm;
 }
 
+// ----------------------------------------------------------------------------
+// Decode front in one block: route, bucket and the GEMV prep of a small batch
+// (T <= 32 tokens, E <= 1024 experts, A = T k <= 512), writing exactly what the
+// route, bucket and prep kernels write (same selection order, same weights bit
+// for bit, same stable bucket order, same slots and prescaled activations).
+//  * route: warp t takes token t; lane l holds the order-preserving keys of
+//    experts l, l + 32, ...; k rounds of a warp arg-max over (key desc, index
+//    asc) give the picks in output order; the weights are route_kernel's
+//    (double exp over the picks, xor-butterfly sum over the 32 lanes);
+//  * bucket: shared-memory counts, a block scan for the offsets, and each
+//    assignment's rank among the earlier assignments of its expert;
+//  * prep: active slots in expert order (block scan), x rows to prescaled f16.
+namespace {
+
+constexpr int kFrontMaxT = 32, kFrontMaxE = 1024, kFrontMaxA = 512;
+
+__device__ __forceinline__ uint32_t front_key(float v) {  // -0 and +0 share a key; 0 = no expert
+  uint32_t u = __float_as_uint(v);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Exclusive scan over a 1024-thread block; *total gets the sum.
+__device__ __forceinline__ int front_scan(int v, int *buf, int *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xFFFFFFFFu, inc, off);
+    if (lane >= off) inc += o;
+  }
+  __syncthreads();
+  if (lane == 31) buf[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int wv = buf[lane];
+    int wi = wv;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xFFFFFFFFu, wi, off);
+      if (lane >= off) wi += o;
+    }
+    buf[lane] = wi - wv;
+    if (lane == 31) buf[32] = wi;
+  }
+  __syncthreads();
+  *total = buf[32];
+  return buf[warp] + inc - v;
+}
+
+__device__ __forceinline__ float front_max(float mx, float *red) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  float r = red[0];
+  for (int i = 1; i < 32; ++i) r = fmaxf(r, red[i]);
+  return r;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(1024)
+    layer_front_kernel(const float *__restrict__ logits, const uint16_t *__restrict__ x, k3moe_weights w, int T,
+                       int H, int E, int k, int32_t *__restrict__ idx, float *__restrict__ wts,
+                       int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int32_t *__restrict__ perm,
+                       int32_t *__restrict__ inv, int4 *__restrict__ slots, int32_t *__restrict__ meta,
+                       int32_t *__restrict__ xexp, uint4 *__restrict__ x16, int32_t *__restrict__ hmax,
+                       int32_t *status) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ int s_idx[kFrontMaxA];
+  __shared__ int s_cnt[kFrontMaxE];
+  __shared__ int s_off[kFrontMaxE + 1];
+  __shared__ int buf[33];
+  __shared__ float red[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int A = T * k;
+  for (int e = tid; e < E; e += 1024) s_cnt[e] = 0;
+  // ---- route: warp t, token t
+  if (warp < T) {
+    const int t = warp;
+    const float *row = logits + static_cast<size_t>(t) * E;
+    uint32_t key[kFrontMaxE / 32];
+    bool nan_here = false;
+#pragma unroll
+    for (int i = 0; i < kFrontMaxE / 32; ++i) {
+      const int e = lane + 32 * i;
+      float v = 0.f;
+      if (e < E) v = __ldg(row + e);
+      nan_here |= e < E && v != v;
+      key[i] = e < E ? front_key(v) : 0u;
+    }
+    int mye = 0;
+    float myv = 0.f;
+    if (__any_sync(0xFFFFFFFFu, nan_here)) {
+      if (lane < k) {
+        idx[t * k + lane] = lane;
+        wts[t * k + lane] = 1.0f / static_cast<float>(k);
+        s_idx[t * k + lane] = lane;
+      }
+      if (lane == 0) set_status(status, K3MOE_DEV_NONFINITE);
+    } else {
+      for (int j = 0; j < k; ++j) {
+        uint32_t bk = 0u;
+        int bi = 0;
+#pragma unroll
+        for (int i = 0; i < kFrontMaxE / 32; ++i)
+          if (key[i] > bk) {  // strict: the lowest index among equal keys
+            bk = key[i];
+            bi = i;
+          }
+        int be = bk ? lane + 32 * bi : 0x7FFFFFFF;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          const uint32_t ok = __shfl_xor_sync(0xFFFFFFFFu, bk, off);
+          const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, off);
+          if (ok > bk || (ok == bk && oe < be)) {
+            bk = ok;
+            be = oe;
+          }
+        }
+        if (lane == j) mye = be;
+#pragma unroll
+        for (int i = 0; i < kFrontMaxE / 32; ++i)
+          if (lane + 32 * i == be) key[i] = 0u;
+      }
+      if (lane < k) myv = __ldg(row + mye);
+      const bool active = lane < k;
+      const float m = __shfl_sync(0xFFFFFFFFu, myv, 0);
+      float wj;
+      if (m == -INFINITY) {
+        wj = 1.0f / static_cast<float>(k);
+      } else if (m == INFINITY) {
+        const int ninf = __popc(__ballot_sync(0xFFFFFFFFu, active && myv == INFINITY));
+        wj = (myv == INFINITY) ? 1.0f / static_cast<float>(ninf) : 0.0f;
+      } else {
+        const double ex = active ? exp(static_cast<double>(myv) - static_cast<double>(m)) : 0.0;
+        double sum = ex;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
+        wj = static_cast<float>(ex / sum);
+      }
+      if (active) {
+        idx[t * k + lane] = mye;
+        wts[t * k + lane] = wj;
+        s_idx[t * k + lane] = mye;
+      }
+    }
+  }
+  __syncthreads();
+  // ---- bucket
+  for (int a = tid; a < A; a += 1024) atomicAdd(&s_cnt[s_idx[a]], 1);
+  __syncthreads();
+  int total;
+  const int c = tid < E ? s_cnt[tid] : 0;
+  const int ex_off = front_scan(c, buf, &total);
+  if (tid < E) s_off[tid] = ex_off;
+  if (tid == 0) s_off[E] = total;
+  __syncthreads();
+  for (int e = tid; e < E; e += 1024) counts[e] = s_cnt[e];
+  for (int e = tid; e <= E; e += 1024) offsets[e] = s_off[e];
+  for (int a = tid; a < A; a += 1024) {
+    const int e = s_idx[a];
+    int r = 0;
+    for (int b = 0; b < a; ++b) r += s_idx[b] == e;
+    const int p = s_off[e] + r;
+    perm[p] = a;
+    inv[a] = p;
+  }
+  // ---- prep: active slots in expert order, zeroed maxima of h, x rows to prescaled f16
+  int nact;
+  const int act = tid < E && s_cnt[tid] > 0;
+  const int sl = front_scan(act, buf, &nact);
+  if (act) {
+    const bool pr = expert_present(w, tid);
+    if (!pr && w.w13_codes[tid] && w.w13_scales[tid] && w.w2_codes[tid] && w.w2_scales[tid])
+      set_status(status, K3MOE_DEV_BOUNDS);  // non-NULL but misaligned: treated as absent
+    slots[sl] = make_int4(tid, s_off[tid], s_cnt[tid], pr ? 1 : 0);
+  }
+  if (tid == 0) meta[0] = nact;
+  for (int p = tid; p < A; p += 1024) hmax[p] = 0;
+  for (int t = 0; t < T; ++t) {
+    const uint16_t *xr = x + static_cast<size_t>(t) * H;
+    float mx = 0.f;
+    for (int c2 = tid; c2 < H; c2 += 1024) mx = fmaxf(mx, fabsf(bf16_bits_to_f32(xr[c2])));
+    const int p = prescale_exp(front_max(mx, red));
+    if (tid == 0) xexp[t] = p;
+    row_to_f16_piece_major(xr, H, scale_pow2(1.0f, -p), x16 + static_cast<size_t>(t) * (H / 8));
+  }
+}
+
+bool layer_front_fits(const k3moe_shape &s) {
+  return s.T <= kFrontMaxT && s.E <= kFrontMaxE && s.T * s.k <= kFrontMaxA;
+}
+
+// route + bucket + GEMV prep in one block, then the GEMV kernels and the combine.
+int launch_layer_gemv_fast(const k3moe_shape &s, const float *logits, const uint16_t *x, const k3moe_weights &w,
+                           int32_t *idx, float *wts, int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv,
+                           float *Y, uint16_t *out, float *out_f32, void *ws, int32_t *status, cudaStream_t st) {
+  if (s.T == 0) return 0;
+  const GemvBufs b = gemv_bufs(s, ws);
+  if (launch_pdl(layer_front_kernel, dim3(1), dim3(1024), 0, st, logits, x, w, s.T, s.H, s.E, s.k, idx, wts, counts,
+                 offsets, perm, inv, b.slots, b.meta, b.xexp, b.x16, b.hmax, status) != cudaSuccess)
+    return -1;
+  RowsParams P;
+  P.w = w;
+  P.H = s.H;
+  P.I = s.I;
+  P.k = s.k;
+  P.A = s.T * s.k;
+  P.perm = perm;
+  P.slots = b.slots;
+  P.meta = b.meta;
+  P.aexp = b.xexp;
+  P.act = b.x16;
+  P.hrow = b.hrow;
+  P.hmax = b.hmax;
+  P.Y = Y;
+  P.status = status;
+  if (launch_rows(P, sm_count(), st, P.A, b.h16, b.hexp)) return -1;
+  return launch_combine(s, Y, wts, inv, nullptr, out, out_f32, st);
+}
+
 int launch_ffn_gemv(const k3moe_shape &s, const uint16_t *x, const k3moe_weights &w,
                     const int32_t *offsets, const int32_t *perm, float *Y, void *ws,
                     int32_t *status, cudaStream_t st) {

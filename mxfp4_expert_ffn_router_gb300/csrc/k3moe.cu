@@ -101,10 +101,19 @@ size_t k3moe_workspace_h_offset(k3moe_shape s, int mode) {
   return static_cast<size_t>(-1);
 }
 
+// The layer call runs bucket and expert FFN one after the other: one workspace
+// serves both.
+static size_t layer_workspace(const k3moe_shape &s, int resolved) {
+  if (resolved < 0) return 0;
+  const size_t b = k3moe::bucket_workspace(s), f = ffn_workspace(s, resolved);
+  return b > f ? b : f;
+}
+
 size_t k3moe_workspace_bytes(k3moe_shape s, int op, int mode) {
   if (abi_check_shape(s) != K3MOE_OK) return 0;
   if (op == K3MOE_OP_BUCKET) return k3moe::bucket_workspace(s);
   if (op == K3MOE_OP_EXPERT_FFN) return ffn_workspace(s, resolve_ffn_mode(s, mode));
+  if (op == K3MOE_OP_LAYER) return layer_workspace(s, resolve_ffn_mode(s, mode));
   return 0;
 }
 
@@ -215,6 +224,36 @@ int k3moe_cache_fetch(k3moe_shape s, int slots, void *arena, size_t arena_bytes,
   return abi_launched(k3moe::launch_cache_fetch(s, slots, arena, *host_w, counts, count_base, count_n,
                                                 reinterpret_cast<unsigned long long *>(stats), dev_status,
                                                 reinterpret_cast<k3moe_stream>(stream)));
+}
+
+int k3moe_layer(k3moe_shape s, const float *logits, const uint16_t *x, const k3moe_weights *w, int32_t *idx,
+                float *wts, int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv, float *Y, uint16_t *out,
+                float *out_f32, int mode, void *ws, size_t ws_bytes, int32_t *dev_status, k3moe_stream_t stream) {
+  int rc = abi_check_shape(s);
+  if (rc) return rc;
+  if (mode < K3MOE_FFN_AUTO || mode > K3MOE_FFN_W4A4) return K3MOE_ERR_ARG;
+  const int resolved = resolve_ffn_mode(s, mode);
+  if (resolved < 0) return K3MOE_ERR_UNSUPPORTED;
+  if (s.T == 0) return K3MOE_OK;
+  if (!logits || !x || !w || !idx || !wts || !counts || !offsets || !perm || !inv || !Y || !out) return K3MOE_ERR_ARG;
+  if (!w->w13_codes || !w->w13_scales || !w->w2_codes || !w->w2_scales) return K3MOE_ERR_ARG;
+  if (!aligned16(x) || !aligned16(Y) || !aligned16(out) || (out_f32 && !aligned16(out_f32))) return K3MOE_ERR_ALIGN;
+  const size_t need = layer_workspace(s, resolved);
+  if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u)) return K3MOE_ERR_WORKSPACE;
+  if ((rc = abi_check_arch())) return rc;
+  const cudaStream_t st = reinterpret_cast<k3moe_stream>(stream);
+  if (resolved == K3MOE_FFN_GEMV && k3moe::layer_front_fits(s))
+    return abi_launched(k3moe::launch_layer_gemv_fast(s, logits, x, *w, idx, wts, counts, offsets, perm, inv, Y, out,
+                                                      out_f32, ws, dev_status, st));
+  if (k3moe::launch_route(s, logits, idx, wts, dev_status, st)) return abi_launched(-1);
+  if (k3moe::launch_bucket(s, idx, counts, offsets, perm, inv, ws, dev_status, st)) return abi_launched(-1);
+  int lrc;
+  if (resolved == K3MOE_FFN_GEMM || resolved == K3MOE_FFN_W4A4)
+    lrc = k3moe::launch_ffn_gemm(s, x, *w, offsets, perm, Y, ws, dev_status, st, resolved == K3MOE_FFN_W4A4);
+  else
+    lrc = k3moe::launch_ffn_gemv(s, x, *w, offsets, perm, Y, ws, dev_status, st);
+  if (lrc) return abi_launched(-1);
+  return abi_launched(k3moe::launch_combine(s, Y, wts, inv, nullptr, out, out_f32, st));
 }
 
 int k3moe_quantize_mxfp4(int64_t n, const uint16_t *x, uint8_t *codes, uint8_t *scales, k3moe_stream_t stream) {

@@ -62,6 +62,10 @@ int launch_gemv_prep(const k3moe_shape &s, const uint16_t *x, const k3moe_weight
                      const GemvBufs &b, int32_t *status, cudaStream_t st);
 int launch_gemv_h16(const k3moe_shape &s, const GemvBufs &b, cudaStream_t st);
 int sm_count();
+bool layer_front_fits(const k3moe_shape &s);
+int launch_layer_gemv_fast(const k3moe_shape &s, const float *logits, const uint16_t *x, const k3moe_weights &w,
+                           int32_t *idx, float *wts, int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv,
+                           float *Y, uint16_t *out, float *out_f32, void *ws, int32_t *status, cudaStream_t st);
 size_t ffn_gemm_workspace(const k3moe_shape &s);
 size_t ffn_gemm_h_offset(const k3moe_shape &s);
 bool ffn_gemm_supported(const k3moe_shape &s);

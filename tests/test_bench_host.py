@@ -120,3 +120,10 @@ def test_extra_workloads_cover_the_configs_and_modes(bench):
     for n in ("batch8", "spec2", "spec4", "spec12", "spec16"):
         modes = {bench.mode_name(gen.CONFIGS[n], m) for nn, m in bench.LEGS if nn == n}
         assert modes == {"gemv", "gemm_w4a16"}
+
+
+def test_layer_kernel_count(bench):
+    assert bench.layer_kernel_count(gen.CONFIGS["decode"], 0) == 5     # single-block front + 3 FFN + combine
+    assert bench.layer_kernel_count(gen.CONFIGS["spec16"], 0) == 5
+    assert bench.layer_kernel_count(gen.CONFIGS["prefill"], 0) == 1 + 3 + 6 + 1
+    assert bench.layer_kernel_count(gen.CONFIGS["batch8"], 3) == 1 + 1 + 6 + 1
