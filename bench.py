@@ -366,7 +366,7 @@ def layer_kernel_count(s, mode):
     and GEMV prep) + gate/up + h16 + down + combine for small GEMV batches, else
     route + bucket (1 or 3) + the expert FFN's kernels + combine."""
     A = s.T * s.k
-    if resolved_mode(s, mode) == 1 and s.T <= 32 and s.E <= 1024 and A <= 512:
+    if resolved_mode(s, mode) == 1 and s.T <= 4 and s.E <= 1024 and A <= 128:
         return 5
     return 1 + (1 if A <= 4096 else 3) + ffn_kernel_count(s, mode) + 1
 
@@ -679,13 +679,13 @@ def run_stack_leg(a, dev, ws, budgets_gb=(8, 32, 64, 128), layers=92, physical=2
     t0 = time.perf_counter()
     store = HostExpertStore(s.H, s.I, s.E, physical, layers, fill, device=dev)
     setup_s = time.perf_counter() - t0
-    n_in = 16
-    inputs = []
-    for i in range(n_in):
-        seed = 500 + i
-        lg = gen.normal_f32(seed, gen.stream(gen.KIND_LOGITS), s.E, 2.0).reshape(1, s.E)
-        x = gen.make_x(s, seed=seed)
-        inputs.append((torch.from_numpy(lg).to(dev), torch.from_numpy(x.view(np.int16)).to(dev)))
+    # distinct inputs for every (token, layer): no routing repeats across tokens
+    n_in = (warm_tokens + timed_tokens) * layers
+    lg_all = gen.normal_f32(500, gen.stream(gen.KIND_LOGITS), n_in * s.E, 2.0).reshape(n_in, 1, s.E)
+    x_all = gen.normal_bf16_bits(500, gen.stream(gen.KIND_X), n_in * s.H).reshape(n_in, 1, s.H)
+    lg_d = torch.from_numpy(lg_all).to(dev)
+    x_d = torch.from_numpy(x_all.view(np.int16)).to(dev)
+    inputs = [(lg_d[i], x_d[i]) for i in range(n_in)]
     out = torch.empty((1, s.H), dtype=torch.bfloat16, device=dev)
     be = expert_bytes(s)
     res = {"layers": layers, "physical_layers_in_host_memory": physical,
@@ -703,7 +703,7 @@ def run_stack_leg(a, dev, ws, budgets_gb=(8, 32, 64, 128), layers=92, physical=2
                 before = stack.counters()
             ev0.record(stream)
             for l in range(layers):
-                lg, x = inputs[(tkn * layers + l) % n_in]
+                lg, x = inputs[tkn * layers + l]
                 stack.layer(l, lg, x, out, stream=stream)
             ev1.record(stream)
             ev1.synchronize()

@@ -301,7 +301,7 @@ int k3moe_cache_fetch(k3moe_shape s, int slots, void *arena, size_t arena_bytes,
  * perm, inv, Y) is written as those calls write it.  The workspace, of
  * k3moe_workspace_bytes(s, K3MOE_OP_LAYER, mode) bytes (256-byte aligned),
  * serves the bucketing and the expert FFN in turn.  When the FFN runs the GEMV
- * kernels and the batch is small (T <= 32, E <= 1024, T*k <= 512) the route,
+ * kernels and the batch is small (T <= 4, E <= 1024, T*k <= 128) the route,
  * the bucketing and the FFN's preparation run as one single-block kernel: a
  * decode step is then five launches instead of seven.  Errors: the union of the
  * four calls'. */

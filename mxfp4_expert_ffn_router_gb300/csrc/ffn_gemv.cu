@@ -682,16 +682,17 @@ int sm_count() {
 // (T <= 32 tokens, E <= 1024 experts, A = T k <= 512), writing exactly what the
 // route, bucket and prep kernels write (same selection order, same weights bit
 // for bit, same stable bucket order, same slots and prescaled activations).
-//  * route: warp t takes token t; lane l holds the order-preserving keys of
-//    experts l, l + 32, ...; k rounds of a warp arg-max over (key desc, index
-//    asc) give the picks in output order; the weights are route_kernel's
-//    (double exp over the picks, xor-butterfly sum over the 32 lanes);
+//  * route, token by token over the whole block: thread e holds expert e's
+//    order-preserving key; a 32-step bit search with one counting barrier per
+//    step finds the k-th largest key, ties at it go in index order, the k picks
+//    are ordered by (key desc, index asc) and weighted with route_kernel's
+//    arithmetic (double exp over the picks, xor-butterfly sum over a warp);
 //  * bucket: shared-memory counts, a block scan for the offsets, and each
 //    assignment's rank among the earlier assignments of its expert;
 //  * prep: active slots in expert order (block scan), x rows to prescaled f16.
 namespace {
 
-constexpr int kFrontMaxT = 32, kFrontMaxE = 1024, kFrontMaxA = 512;
+constexpr int kFrontMaxT = 4, kFrontMaxE = 1024, kFrontMaxA = 128;
 
 __device__ __forceinline__ uint32_t front_key(float v) {  // -0 and +0 share a key; 0 = no expert
   uint32_t u = __float_as_uint(v);
@@ -757,78 +758,80 @@ __global__ void __launch_bounds__(1024)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int A = T * k;
   for (int e = tid; e < E; e += 1024) s_cnt[e] = 0;
-  // ---- route: warp t, token t
-  if (warp < T) {
-    const int t = warp;
-    const float *row = logits + static_cast<size_t>(t) * E;
-    uint32_t key[kFrontMaxE / 32];
-    bool nan_here = false;
-#pragma unroll
-    for (int i = 0; i < kFrontMaxE / 32; ++i) {
-      const int e = lane + 32 * i;
-      float v = 0.f;
-      if (e < E) v = __ldg(row + e);
-      nan_here |= e < E && v != v;
-      key[i] = e < E ? front_key(v) : 0u;
+  // ---- route, token by token with the whole block (one key per thread)
+  __shared__ int s_n, s_wc[32];
+  __shared__ uint32_t s_key[32];
+  __shared__ int s_e[32], s_oe[32];
+  __shared__ float s_v[32], s_ov[32];
+  for (int t = 0; t < T; ++t) {
+    const float v = tid < E ? __ldg(logits + static_cast<size_t>(t) * E + tid) : 0.f;
+    const uint32_t key = tid < E ? front_key(v) : 0u;
+    if (tid == 0) s_n = 0;
+    if (__syncthreads_or(tid < E && v != v)) {  // a NaN row: experts 0..k-1, weights 1/k
+      if (tid < k) {
+        idx[t * k + tid] = tid;
+        wts[t * k + tid] = 1.0f / static_cast<float>(k);
+        s_idx[t * k + tid] = tid;
+      }
+      if (tid == 0) set_status(status, K3MOE_DEV_NONFINITE);
+      __syncthreads();
+      continue;
     }
-    int mye = 0;
-    float myv = 0.f;
-    if (__any_sync(0xFFFFFFFFu, nan_here)) {
-      if (lane < k) {
-        idx[t * k + lane] = lane;
-        wts[t * k + lane] = 1.0f / static_cast<float>(k);
-        s_idx[t * k + lane] = lane;
-      }
-      if (lane == 0) set_status(status, K3MOE_DEV_NONFINITE);
-    } else {
-      for (int j = 0; j < k; ++j) {
-        uint32_t bk = 0u;
-        int bi = 0;
-#pragma unroll
-        for (int i = 0; i < kFrontMaxE / 32; ++i)
-          if (key[i] > bk) {  // strict: the lowest index among equal keys
-            bk = key[i];
-            bi = i;
-          }
-        int be = bk ? lane + 32 * bi : 0x7FFFFFFF;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-          const uint32_t ok = __shfl_xor_sync(0xFFFFFFFFu, bk, off);
-          const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, off);
-          if (ok > bk || (ok == bk && oe < be)) {
-            bk = ok;
-            be = oe;
-          }
-        }
-        if (lane == j) mye = be;
-#pragma unroll
-        for (int i = 0; i < kFrontMaxE / 32; ++i)
-          if (lane + 32 * i == be) key[i] = 0u;
-      }
-      if (lane < k) myv = __ldg(row + mye);
+    // tau = the k-th largest key: the largest value with count(key >= tau) >= k
+    uint32_t tau = 0u;
+    for (int bit = 31; bit >= 0; --bit) {
+      const uint32_t cand = tau | (1u << bit);
+      if (__syncthreads_count(key >= cand) >= k) tau = cand;
+    }
+    const int need = k - __syncthreads_count(key > tau);  // keys equal to tau to take, lowest indices first
+    const bool tie = key == tau && key != 0u;
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, tie);
+    if (lane == 0) s_wc[warp] = __popc(m);
+    __syncthreads();
+    int before = 0;
+    for (int i = 0; i < warp; ++i) before += s_wc[i];
+    const int rank = before + __popc(m & ((1u << lane) - 1u));
+    if (key > tau || (tie && rank < need)) {
+      const int slot = atomicAdd(&s_n, 1);
+      s_key[slot] = key;
+      s_e[slot] = tid;
+      s_v[slot] = v;
+    }
+    __syncthreads();
+    if (tid < k) {  // the k picks ordered by (key desc, index asc)
+      const uint32_t mk = s_key[tid];
+      const int me = s_e[tid];
+      int r = 0;
+      for (int j = 0; j < k; ++j) r += (s_key[j] > mk) || (s_key[j] == mk && s_e[j] < me);
+      s_oe[r] = me;
+      s_ov[r] = s_v[tid];
+    }
+    __syncthreads();
+    if (warp == 0) {  // weights over the k picks (route_kernel's arithmetic)
       const bool active = lane < k;
-      const float m = __shfl_sync(0xFFFFFFFFu, myv, 0);
+      const float myv = active ? s_ov[lane] : 0.f;
+      const float mx = s_ov[0];
       float wj;
-      if (m == -INFINITY) {
+      if (mx == -INFINITY) {
         wj = 1.0f / static_cast<float>(k);
-      } else if (m == INFINITY) {
+      } else if (mx == INFINITY) {
         const int ninf = __popc(__ballot_sync(0xFFFFFFFFu, active && myv == INFINITY));
         wj = (myv == INFINITY) ? 1.0f / static_cast<float>(ninf) : 0.0f;
       } else {
-        const double ex = active ? exp(static_cast<double>(myv) - static_cast<double>(m)) : 0.0;
+        const double ex = active ? exp(static_cast<double>(myv) - static_cast<double>(mx)) : 0.0;
         double sum = ex;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
         wj = static_cast<float>(ex / sum);
       }
       if (active) {
-        idx[t * k + lane] = mye;
+        idx[t * k + lane] = s_oe[lane];
         wts[t * k + lane] = wj;
-        s_idx[t * k + lane] = mye;
+        s_idx[t * k + lane] = s_oe[lane];
       }
     }
+    __syncthreads();
   }
-  __syncthreads();
   // ---- bucket
   for (int a = tid; a < A; a += 1024) atomicAdd(&s_cnt[s_idx[a]], 1);
   __syncthreads();

@@ -124,6 +124,7 @@ def test_extra_workloads_cover_the_configs_and_modes(bench):
 
 def test_layer_kernel_count(bench):
     assert bench.layer_kernel_count(gen.CONFIGS["decode"], 0) == 5     # single-block front + 3 FFN + combine
-    assert bench.layer_kernel_count(gen.CONFIGS["spec16"], 0) == 5
+    assert bench.layer_kernel_count(gen.CONFIGS["spec4"], 0) == 5
+    assert bench.layer_kernel_count(gen.CONFIGS["spec12"], 0) == 1 + 1 + 4 + 1
     assert bench.layer_kernel_count(gen.CONFIGS["prefill"], 0) == 1 + 3 + 6 + 1
     assert bench.layer_kernel_count(gen.CONFIGS["batch8"], 3) == 1 + 1 + 6 + 1
