@@ -688,7 +688,19 @@ def run_stack_leg(a, dev, ws, budgets_gb=(8, 32, 64, 128), layers=92, physical=2
     inputs = [(lg_d[i], x_d[i]) for i in range(n_in)]
     out = torch.empty((1, s.H), dtype=torch.bfloat16, device=dev)
     be = expert_bytes(s)
-    res = {"layers": layers, "physical_layers_in_host_memory": physical,
+    # reference for the arena fill: the copy engines' host -> HBM rate on 2 GB of the store
+    src = store.arrays[0].view(-1)[: 2 << 30]
+    dst = torch.empty(src.numel(), dtype=torch.uint8, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dst.copy_(src, non_blocking=True)
+    e0.record()
+    for _ in range(3):
+        dst.copy_(src, non_blocking=True)
+    e1.record()
+    e1.synchronize()
+    dma_gbs = 3 * src.numel() / (e0.elapsed_time(e1) / 1e3) / 1e9
+    del dst
+    res = {"layers": layers, "physical_layers_in_host_memory": physical, "host_to_hbm_dma_gbs": dma_gbs,
            "host_store_gb": store.bytes / 1e9, "host_store_setup_s": setup_s,
            "expert_bytes": be, "requests_per_token": layers * s.k, "budgets": {}}
     stream = torch.cuda.current_stream()

@@ -230,6 +230,10 @@ struct RowsParams {
   int32_t *status;
 };
 
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
 __device__ __forceinline__ const uint8_t *ldg_ptr(const uint8_t *const *arr, int e) {
   return reinterpret_cast<const uint8_t *>(__ldg(reinterpret_cast<const unsigned long long *>(arr) + e));
 }
@@ -479,6 +483,37 @@ __device__ __forceinline__ void compute_half(const uint4 (&cw)[R][NH], const uin
   }
 }
 
+// L2 prefetch of an item's code rows (and, for gate/up, its scale rows): one
+// 128-byte line per lane and instruction, fire and forget -- no registers wait
+// on it.  Gate/up (2 rows of 512 NJ bytes): lanes 0 .. 4 NJ - 1 take the lines
+// of both rows, the lanes above take the scale lines.  Down (R rows): lane l
+// takes line l % (4 NJ) of row l / (4 NJ).
+template <int KIND, int R, int NJ>
+__device__ __forceinline__ void prefetch_item(const RowsParams &P, long long item, int per_slot, int lane) {
+  const int4 sl = __ldg(P.slots + static_cast<int>(item / per_slot));
+  if (!sl.w) return;
+  const int rb = static_cast<int>(item % per_slot);
+  constexpr int kLines = 4 * NJ;  // 128-byte lines per code row
+  if (KIND == 0) {
+    const uint8_t *cb = ldg_ptr(P.w.w13_codes, sl.x);
+    if (lane < kLines) {
+      prefetch_l2(cb + static_cast<size_t>(rb) * (512 * NJ) + 128 * lane);
+      prefetch_l2(cb + static_cast<size_t>(P.I + rb) * (512 * NJ) + 128 * lane);
+    } else if (lane < kLines + 2) {
+      const uint8_t *sb = ldg_ptr(P.w.w13_scales, sl.x);
+      const int row = lane == kLines ? rb : P.I + rb;
+      prefetch_l2(sb + static_cast<size_t>(row) * (32 * NJ));
+    }
+  } else {
+    const uint8_t *cb = ldg_ptr(P.w.w2_codes, sl.x);
+    const int r = lane / kLines, line = lane % kLines;
+    if (r < R) {
+      const int row = min(rb * R + r, P.H - 1);
+      prefetch_l2(cb + static_cast<size_t>(row) * (512 * NJ) + 128 * line);
+    }
+  }
+}
+
 template <int KIND, int R, int NJ>
 __global__ void __launch_bounds__(kGvWarps * 32, 2) gemv_rows_pipe_kernel(RowsParams P) {
   pdl_wait();
@@ -499,11 +534,14 @@ __global__ void __launch_bounds__(kGvWarps * 32, 2) gemv_rows_pipe_kernel(RowsPa
     load_half<R, 0, HA>(cur, ca, sa);
     if (HB > 0) load_half<R, HA, HB>(cur, cb, sb);
   }
+  if (item + stride < nitems) prefetch_item<KIND, R, NJ>(P, item + stride, per_slot, lane);
   for (;;) {
     const long long nitem = item + stride;
     const bool has_next = nitem < nitems;
     ItemRows<R> nxt;
     if (has_next) item_rows_at<KIND, R, NJ>(P, nitem, per_slot, nxt);
+    // the item after next goes to L2 now; its register loads come one item later
+    if (nitem + stride < nitems) prefetch_item<KIND, R, NJ>(P, nitem + stride, per_slot, lane);
     const bool pf = has_next && nxt.sl.w;
     for (int t = 0; t < cur.sl.z; ++t) {
       const int p = cur.sl.y + t;
