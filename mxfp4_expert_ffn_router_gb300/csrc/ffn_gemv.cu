@@ -230,10 +230,6 @@ struct RowsParams {
   int32_t *status;
 };
 
-__device__ __forceinline__ void prefetch_l2(const void *p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
-}
-
 __device__ __forceinline__ const uint8_t *ldg_ptr(const uint8_t *const *arr, int e) {
   return reinterpret_cast<const uint8_t *>(__ldg(reinterpret_cast<const unsigned long long *>(arr) + e));
 }
@@ -483,37 +479,6 @@ __device__ __forceinline__ void compute_half(const uint4 (&cw)[R][NH], const uin
   }
 }
 
-// L2 prefetch of an item's code rows (and, for gate/up, its scale rows): one
-// 128-byte line per lane and instruction, fire and forget -- no registers wait
-// on it.  Gate/up (2 rows of 512 NJ bytes): lanes 0 .. 4 NJ - 1 take the lines
-// of both rows, the lanes above take the scale lines.  Down (R rows): lane l
-// takes line l % (4 NJ) of row l / (4 NJ).
-template <int KIND, int R, int NJ>
-__device__ __forceinline__ void prefetch_item(const RowsParams &P, long long item, int per_slot, int lane) {
-  const int4 sl = __ldg(P.slots + static_cast<int>(item / per_slot));
-  if (!sl.w) return;
-  const int rb = static_cast<int>(item % per_slot);
-  constexpr int kLines = 4 * NJ;  // 128-byte lines per code row
-  if (KIND == 0) {
-    const uint8_t *cb = ldg_ptr(P.w.w13_codes, sl.x);
-    if (lane < kLines) {
-      prefetch_l2(cb + static_cast<size_t>(rb) * (512 * NJ) + 128 * lane);
-      prefetch_l2(cb + static_cast<size_t>(P.I + rb) * (512 * NJ) + 128 * lane);
-    } else if (lane < kLines + 2) {
-      const uint8_t *sb = ldg_ptr(P.w.w13_scales, sl.x);
-      const int row = lane == kLines ? rb : P.I + rb;
-      prefetch_l2(sb + static_cast<size_t>(row) * (32 * NJ));
-    }
-  } else {
-    const uint8_t *cb = ldg_ptr(P.w.w2_codes, sl.x);
-    const int r = lane / kLines, line = lane % kLines;
-    if (r < R) {
-      const int row = min(rb * R + r, P.H - 1);
-      prefetch_l2(cb + static_cast<size_t>(row) * (512 * NJ) + 128 * line);
-    }
-  }
-}
-
 template <int KIND, int R, int NJ>
 __global__ void __launch_bounds__(kGvWarps * 32, 2) gemv_rows_pipe_kernel(RowsParams P) {
   pdl_wait();
@@ -534,14 +499,11 @@ __global__ void __launch_bounds__(kGvWarps * 32, 2) gemv_rows_pipe_kernel(RowsPa
     load_half<R, 0, HA>(cur, ca, sa);
     if (HB > 0) load_half<R, HA, HB>(cur, cb, sb);
   }
-  if (item + stride < nitems) prefetch_item<KIND, R, NJ>(P, item + stride, per_slot, lane);
   for (;;) {
     const long long nitem = item + stride;
     const bool has_next = nitem < nitems;
     ItemRows<R> nxt;
     if (has_next) item_rows_at<KIND, R, NJ>(P, nitem, per_slot, nxt);
-    // the item after next goes to L2 now; its register loads come one item later
-    if (nitem + stride < nitems) prefetch_item<KIND, R, NJ>(P, nitem + stride, per_slot, lane);
     const bool pf = has_next && nxt.sl.w;
     for (int t = 0; t < cur.sl.z; ++t) {
       const int p = cur.sl.y + t;
@@ -720,14 +682,18 @@ int sm_count() {
 // (T <= 32 tokens, E <= 1024 experts, A = T k <= 512), writing exactly what the
 // route, bucket and prep kernels write (same selection order, same weights bit
 // for bit, same stable bucket order, same slots and prescaled activations).
-//  * route, token by token over the whole block: thread e holds expert e's
-//    order-preserving key; a 32-step bit search with one counting barrier per
-//    step finds the k-th largest key, ties at it go in index order, the k picks
-//    are ordered by (key desc, index asc) and weighted with route_kernel's
-//    arithmetic (double exp over the picks, xor-butterfly sum over a warp);
-//  * bucket: shared-memory counts, a block scan for the offsets, and each
-//    assignment's rank among the earlier assignments of its expert;
-//  * prep: active slots in expert order (block scan), x rows to prescaled f16.
+//  * route: warp t takes token t with warp-level operations only: lane l holds
+//    the order-preserving keys of experts l, l + 32, ...; a 32-step bit search
+//    with one warp reduction per step finds the k-th largest key, ties at it go
+//    in index order, the k picks are ordered by (key desc, index asc) and
+//    weighted with route_kernel's arithmetic (double exp over the picks,
+//    xor-butterfly sum); meanwhile warps 4..31 take the max |x| of row slices;
+//  * bucket, by counting over the A <= 128 assignments: assignment a's place is
+//    #{a' : (idx[a'], a') < (idx[a], a)}, which sorts the experts; offsets and
+//    counts come from binary searches in the sorted experts;
+//  * prep: the first position of each expert writes its active slot (the number
+//    of distinct experts before it), then x rows to prescaled f16.
+// Two block barriers in all.
 namespace {
 
 constexpr int kFrontMaxT = 4, kFrontMaxE = 1024, kFrontMaxA = 128;
@@ -736,45 +702,6 @@ __device__ __forceinline__ uint32_t front_key(float v) {  // -0 and +0 share a k
   uint32_t u = __float_as_uint(v);
   if (u == 0x80000000u) u = 0u;
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// Exclusive scan over a 1024-thread block; *total gets the sum.
-__device__ __forceinline__ int front_scan(int v, int *buf, int *total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int inc = v;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int o = __shfl_up_sync(0xFFFFFFFFu, inc, off);
-    if (lane >= off) inc += o;
-  }
-  __syncthreads();
-  if (lane == 31) buf[warp] = inc;
-  __syncthreads();
-  if (warp == 0) {
-    const int wv = buf[lane];
-    int wi = wv;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(0xFFFFFFFFu, wi, off);
-      if (lane >= off) wi += o;
-    }
-    buf[lane] = wi - wv;
-    if (lane == 31) buf[32] = wi;
-  }
-  __syncthreads();
-  *total = buf[32];
-  return buf[warp] + inc - v;
-}
-
-__device__ __forceinline__ float front_max(float mx, float *red) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
-  __syncthreads();
-  float r = red[0];
-  for (int i = 1; i < 32; ++i) r = fmaxf(r, red[i]);
-  return r;
 }
 
 }  // namespace
@@ -789,66 +716,82 @@ __global__ void __launch_bounds__(1024)
   pdl_wait();
   pdl_trigger();
   __shared__ int s_idx[kFrontMaxA];
-  __shared__ int s_cnt[kFrontMaxE];
-  __shared__ int s_off[kFrontMaxE + 1];
-  __shared__ int buf[33];
-  __shared__ float red[32];
+  __shared__ int s_sorted[kFrontMaxA];
+  __shared__ int s_xexp[kFrontMaxT];
+  __shared__ float s_xpart[32];
+  __shared__ uint32_t s_key[kFrontMaxT][32];
+  __shared__ int s_e[kFrontMaxT][32], s_oe[kFrontMaxT][32];
+  __shared__ float s_v[kFrontMaxT][32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int A = T * k;
-  for (int e = tid; e < E; e += 1024) s_cnt[e] = 0;
-  // ---- route, token by token with the whole block (one key per thread)
-  __shared__ int s_n, s_wc[32];
-  __shared__ uint32_t s_key[32];
-  __shared__ int s_e[32], s_oe[32];
-  __shared__ float s_v[32], s_ov[32];
-  for (int t = 0; t < T; ++t) {
-    const float v = tid < E ? __ldg(logits + static_cast<size_t>(t) * E + tid) : 0.f;
-    const uint32_t key = tid < E ? front_key(v) : 0u;
-    if (tid == 0) s_n = 0;
-    if (__syncthreads_or(tid < E && v != v)) {  // a NaN row: experts 0..k-1, weights 1/k
-      if (tid < k) {
-        idx[t * k + tid] = tid;
-        wts[t * k + tid] = 1.0f / static_cast<float>(k);
-        s_idx[t * k + tid] = tid;
+  // ---- phase A: warp t < T routes token t; warps 4..31 find the max |x| of row slices
+  if (warp < T) {
+    const int t = warp;
+    const float *row = logits + static_cast<size_t>(t) * E;
+    uint32_t key[kFrontMaxE / 32];
+    bool nan_here = false;
+#pragma unroll
+    for (int i = 0; i < kFrontMaxE / 32; ++i) {
+      const int e = lane + 32 * i;
+      float v = 0.f;
+      if (e < E) v = __ldg(row + e);
+      nan_here |= e < E && v != v;
+      key[i] = e < E ? front_key(v) : 0u;  // 0: no expert (every real key is larger)
+    }
+    if (__any_sync(0xFFFFFFFFu, nan_here)) {  // a NaN row: experts 0..k-1, weights 1/k
+      if (lane < k) {
+        idx[t * k + lane] = lane;
+        wts[t * k + lane] = 1.0f / static_cast<float>(k);
+        s_idx[t * k + lane] = lane;
       }
-      if (tid == 0) set_status(status, K3MOE_DEV_NONFINITE);
-      __syncthreads();
-      continue;
-    }
-    // tau = the k-th largest key: the largest value with count(key >= tau) >= k
-    uint32_t tau = 0u;
-    for (int bit = 31; bit >= 0; --bit) {
-      const uint32_t cand = tau | (1u << bit);
-      if (__syncthreads_count(key >= cand) >= k) tau = cand;
-    }
-    const int need = k - __syncthreads_count(key > tau);  // keys equal to tau to take, lowest indices first
-    const bool tie = key == tau && key != 0u;
-    const unsigned m = __ballot_sync(0xFFFFFFFFu, tie);
-    if (lane == 0) s_wc[warp] = __popc(m);
-    __syncthreads();
-    int before = 0;
-    for (int i = 0; i < warp; ++i) before += s_wc[i];
-    const int rank = before + __popc(m & ((1u << lane) - 1u));
-    if (key > tau || (tie && rank < need)) {
-      const int slot = atomicAdd(&s_n, 1);
-      s_key[slot] = key;
-      s_e[slot] = tid;
-      s_v[slot] = v;
-    }
-    __syncthreads();
-    if (tid < k) {  // the k picks ordered by (key desc, index asc)
-      const uint32_t mk = s_key[tid];
-      const int me = s_e[tid];
-      int r = 0;
-      for (int j = 0; j < k; ++j) r += (s_key[j] > mk) || (s_key[j] == mk && s_e[j] < me);
-      s_oe[r] = me;
-      s_ov[r] = s_v[tid];
-    }
-    __syncthreads();
-    if (warp == 0) {  // weights over the k picks (route_kernel's arithmetic)
+      if (lane == 0) set_status(status, K3MOE_DEV_NONFINITE);
+    } else {
+      // tau = the k-th largest key: the largest value with count(key >= tau) >= k
+      uint32_t tau = 0u;
+      for (int bit = 31; bit >= 0; --bit) {
+        const uint32_t cand = tau | (1u << bit);
+        int c0 = 0, c1 = 0;
+#pragma unroll
+        for (int i = 0; i < kFrontMaxE / 32; i += 2) {
+          c0 += key[i] >= cand;
+          c1 += key[i + 1] >= cand;
+        }
+        if (static_cast<int>(__reduce_add_sync(0xFFFFFFFFu, static_cast<unsigned>(c0 + c1))) >= k) tau = cand;
+      }
+      int cgt = 0;
+#pragma unroll
+      for (int i = 0; i < kFrontMaxE / 32; ++i) cgt += key[i] > tau;
+      const int need = k - static_cast<int>(__reduce_add_sync(0xFFFFFFFFu, static_cast<unsigned>(cgt)));
+      // the picks in index order (i major, lane minor): keys above tau, and the first `need` ties
+      int ties = 0, nsel = 0;
+#pragma unroll
+      for (int i = 0; i < kFrontMaxE / 32; ++i) {
+        const bool tie = key[i] == tau && key[i] != 0u;
+        const unsigned mt = __ballot_sync(0xFFFFFFFFu, tie);
+        const bool sel = key[i] > tau || (tie && ties + __popc(mt & ((1u << lane) - 1u)) < need);
+        ties += __popc(mt);
+        const unsigned ms = __ballot_sync(0xFFFFFFFFu, sel);
+        if (sel) {
+          const int slot = nsel + __popc(ms & ((1u << lane) - 1u));
+          s_key[t][slot] = key[i];
+          s_e[t][slot] = lane + 32 * i;
+        }
+        nsel += __popc(ms);
+      }
+      __syncwarp();
+      // order by (key desc, index asc); weights with route_kernel's arithmetic
+      if (lane < k) {
+        const uint32_t mk = s_key[t][lane];
+        const int me = s_e[t][lane];
+        int r = 0;
+        for (int j = 0; j < k; ++j) r += (s_key[t][j] > mk) || (s_key[t][j] == mk && s_e[t][j] < me);
+        s_oe[t][r] = me;
+        s_v[t][r] = __ldg(row + me);
+      }
+      __syncwarp();
       const bool active = lane < k;
-      const float myv = active ? s_ov[lane] : 0.f;
-      const float mx = s_ov[0];
+      const float myv = active ? s_v[t][lane] : 0.f;
+      const float mx = s_v[t][0];
       float wj;
       if (mx == -INFINITY) {
         wj = 1.0f / static_cast<float>(k);
@@ -863,52 +806,88 @@ __global__ void __launch_bounds__(1024)
         wj = static_cast<float>(ex / sum);
       }
       if (active) {
-        idx[t * k + lane] = s_oe[lane];
+        idx[t * k + lane] = s_oe[t][lane];
         wts[t * k + lane] = wj;
-        s_idx[t * k + lane] = s_oe[lane];
+        s_idx[t * k + lane] = s_oe[t][lane];
       }
     }
-    __syncthreads();
+  } else if (warp >= kFrontMaxT) {
+    // warps 4..31: partial max |x| of a slice of one token's row (16-byte loads)
+    const int nw = 32 - kFrontMaxT, wpt = nw / T, wr = warp - kFrontMaxT;
+    if (wr < wpt * T) {
+      const int t = wr / wpt, part = wr % wpt;
+      const int n16 = H / 8, per = (n16 + wpt - 1) / wpt;
+      const uint4 *xr = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(t) * H);
+      float mx = 0.f;
+#pragma unroll 4
+      for (int c = part * per + lane; c < min(n16, (part + 1) * per); c += 32) {
+        const uint4 v = __ldg(xr + c);
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+          mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(u[m] << 16)), fabsf(__uint_as_float(u[m] & 0xFFFF0000u))));
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+      if (lane == 0) s_xpart[wr] = mx;
+    }
   }
-  // ---- bucket
-  for (int a = tid; a < A; a += 1024) atomicAdd(&s_cnt[s_idx[a]], 1);
   __syncthreads();
-  int total;
-  const int c = tid < E ? s_cnt[tid] : 0;
-  const int ex_off = front_scan(c, buf, &total);
-  if (tid < E) s_off[tid] = ex_off;
-  if (tid == 0) s_off[E] = total;
-  __syncthreads();
-  for (int e = tid; e < E; e += 1024) counts[e] = s_cnt[e];
-  for (int e = tid; e <= E; e += 1024) offsets[e] = s_off[e];
-  for (int a = tid; a < A; a += 1024) {
-    const int e = s_idx[a];
-    int r = 0;
-    for (int b = 0; b < a; ++b) r += s_idx[b] == e;
-    const int p = s_off[e] + r;
-    perm[p] = a;
-    inv[a] = p;
+  // ---- phase B: each assignment's place in (expert, assignment) order, the x prescale
+  if (tid < A) {
+    const int e = s_idx[tid];
+    int p = 0;
+    for (int a = 0; a < A; ++a) p += s_idx[a] < e || (s_idx[a] == e && a < tid);
+    perm[p] = tid;
+    inv[tid] = p;
+    s_sorted[p] = e;
   }
-  // ---- prep: active slots in expert order, zeroed maxima of h, x rows to prescaled f16
-  int nact;
-  const int act = tid < E && s_cnt[tid] > 0;
-  const int sl = front_scan(act, buf, &nact);
-  if (act) {
-    const bool pr = expert_present(w, tid);
-    if (!pr && w.w13_codes[tid] && w.w13_scales[tid] && w.w2_codes[tid] && w.w2_scales[tid])
-      set_status(status, K3MOE_DEV_BOUNDS);  // non-NULL but misaligned: treated as absent
-    slots[sl] = make_int4(tid, s_off[tid], s_cnt[tid], pr ? 1 : 0);
-  }
-  if (tid == 0) meta[0] = nact;
-  for (int p = tid; p < A; p += 1024) hmax[p] = 0;
-  for (int t = 0; t < T; ++t) {
-    const uint16_t *xr = x + static_cast<size_t>(t) * H;
+  if (tid < T) {
+    const int wpt = (32 - kFrontMaxT) / T;
     float mx = 0.f;
-    for (int c2 = tid; c2 < H; c2 += 1024) mx = fmaxf(mx, fabsf(bf16_bits_to_f32(xr[c2])));
-    const int p = prescale_exp(front_max(mx, red));
-    if (tid == 0) xexp[t] = p;
-    row_to_f16_piece_major(xr, H, scale_pow2(1.0f, -p), x16 + static_cast<size_t>(t) * (H / 8));
+    for (int i = 0; i < wpt; ++i) mx = fmaxf(mx, s_xpart[tid * wpt + i]);
+    const int p = prescale_exp(mx);
+    s_xexp[tid] = p;
+    xexp[tid] = p;
   }
+  for (int p = tid; p < A; p += 1024) hmax[p] = 0;
+  __syncthreads();
+  // ---- phase C: offsets and counts by binary search in the sorted experts,
+  //      active slots (first position of each expert), x rows to prescaled f16
+  for (int e = tid; e <= E; e += 1024) {
+    int lo = 0, hi = A;  // first position with expert >= e
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (s_sorted[mid] < e) lo = mid + 1; else hi = mid;
+    }
+    offsets[e] = lo;
+    if (e < E) {
+      int lo2 = lo, hi2 = A;  // first position with expert > e
+      while (lo2 < hi2) {
+        const int mid = (lo2 + hi2) >> 1;
+        if (s_sorted[mid] <= e) lo2 = mid + 1; else hi2 = mid;
+      }
+      counts[e] = lo2 - lo;
+    }
+  }
+  if (tid < A && (tid == 0 || s_sorted[tid] != s_sorted[tid - 1])) {
+    const int e = s_sorted[tid];
+    int slot = 0, end = tid + 1;
+    for (int p = 1; p <= tid; ++p) slot += s_sorted[p] != s_sorted[p - 1];
+    while (end < A && s_sorted[end] == e) ++end;
+    const bool pr = expert_present(w, e);
+    if (!pr && w.w13_codes[e] && w.w13_scales[e] && w.w2_codes[e] && w.w2_scales[e])
+      set_status(status, K3MOE_DEV_BOUNDS);  // non-NULL but misaligned: treated as absent
+    slots[slot] = make_int4(e, tid, end - tid, pr ? 1 : 0);
+  }
+  if (tid == 0) {
+    int n = A > 0 ? 1 : 0;
+    for (int p = 1; p < A; ++p) n += s_sorted[p] != s_sorted[p - 1];
+    meta[0] = n;
+  }
+  for (int t = 0; t < T; ++t)
+    row_to_f16_piece_major(x + static_cast<size_t>(t) * H, H, scale_pow2(1.0f, -s_xexp[t]),
+                           x16 + static_cast<size_t>(t) * (H / 8));
 }
 
 bool layer_front_fits(const k3moe_shape &s) {
