@@ -202,9 +202,12 @@ def measured_peaks():
         return None
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(files=None) -> str:
+    """Hash of the CUDA sources (all of csrc/, or the listed file names in it)."""
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "mxfp4_expert_ffn_router_gb300", "csrc", "*"))):
+    csrc = os.path.join(ROOT, "mxfp4_expert_ffn_router_gb300", "csrc")
+    paths = sorted(glob.glob(os.path.join(csrc, "*"))) if files is None else [os.path.join(csrc, f) for f in sorted(files)]
+    for f in paths:
         h.update(open(f, "rb").read())
     return h.hexdigest()[:16]
 
@@ -218,7 +221,13 @@ def recorded_traffic(config: str):
     except Exception:
         return None
     ent = d.get(config)
-    if not ent or ent.get("source_hash") != kernel_source_hash():
+    if not ent:
+        return None
+    try:
+        now = kernel_source_hash(ent.get("source_files"))
+    except OSError:
+        return None
+    if ent.get("source_hash") != now:
         return None
     return ent.get("dram_bytes_per_call")
 

@@ -94,26 +94,6 @@ __device__ __forceinline__ uint32_t idesc_f16(int M, int N) {
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
-// 32 lanes x 32 bit, 16 consecutive columns per thread, registers -> tensor
-// memory, without waiting for completion.
-__device__ __forceinline__ void tc_st16_async(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15, %16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
-}
-// Wait for this thread's tensor-memory stores; the registers a pending store
-// reads are named so that they stay live and unmodified until here.
-__device__ __forceinline__ void tc_wait_st_keep(uint32_t (&r)[16]) {
-  asm volatile("tcgen05.wait::st.sync.aligned;"
-               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
-                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
-               :
-               : "memory");
-}
-
 // A operand from tensor memory (M lanes x K/2 columns of f16 pairs), B from shared memory.
 __device__ __forceinline__ void tc_mma_f16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
                                               uint32_t accumulate) {
@@ -526,12 +506,6 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     // weight stages); the next window's scales are loaded one group ahead
     uint4 scv = make_uint4(0, 0, 0, 0);
     if (svec) scv = *reinterpret_cast<const uint4 *>(srow);
-    // The tensor-memory store of step ks completes while step ks + 1 is read and
-    // converted: its completion (wait::st, fence, arrivals) is taken just before
-    // step ks + 1 is stored.  Two register buffers by step parity; the wait names
-    // the pending buffer so that it stays live and unmodified until then.
-    uint32_t obuf[2][16];
-    int pend_s = -1, pend_ws = -1;  // stage awaiting its arrival, weight stage released with it
     for (int kb = 0; kb < ksteps; kb += 8) {
       uint4 scn = make_uint4(0, 0, 0, 0);
       if (svec && kb + 8 < ksteps) scn = *reinterpret_cast<const uint4 *>(srow + 2 * (kb + 8));
@@ -554,7 +528,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         const uint32_t mulbits = f16_pow2_bits(sbyte - smax);
         const uint32_t mul2 = mulbits | (mulbits << 16);
         const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-        uint32_t(&o)[16] = obuf[j & 1];  // 32 f16 = columns 16*hf .. 16*hf+15 of the stage
+        uint32_t o[16];  // 32 f16 = columns 16*hf .. 16*hf+15 of the stage (two K values per column)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t h[4];
@@ -567,31 +541,16 @@ __global__ void __launch_bounds__(kThreadsG, 1)
             o[4 * c + m] = *reinterpret_cast<const uint32_t *>(&prod);
           }
         }
-        if (pend_s >= 0) {
-          tc_wait_st_keep(obuf[(j & 1) ^ 1]);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) {
-            mb_arrive(&full_bar[pend_s]);
-            if (pend_ws >= 0) mb_arrive(&wempty_bar[pend_ws]);
-          }
+        tc_st16(a_lane + kTileN + s * kAcols + 16 * hf, o);  // waits for the warp's stores
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mb_arrive(&full_bar[s]);
+          // the weight stage is free once this warp has read its last K step
+          if ((j % kWSteps) == kWSteps - 1 || ks == ksteps - 1) mb_arrive(&wempty_bar[ws]);
         }
-        tc_st16_async(a_lane + kTileN + s * kAcols + 16 * hf, o);
-        pend_s = s;
-        // the weight stage is free once this warp has read its last K step
-        pend_ws = ((j % kWSteps) == kWSteps - 1 || ks == ksteps - 1) ? ws : -1;
       }
       scv = scn;
-    }
-    if (pend_s >= 0) {
-      tc_wait_st_keep(obuf[0]);  // both buffers: the pending one's parity is a run-time value here
-      tc_wait_st_keep(obuf[1]);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mb_arrive(&full_bar[pend_s]);
-        if (pend_ws >= 0) mb_arrive(&wempty_bar[pend_ws]);
-      }
     }
   } else if (warp == kTmaWarp) {
     // ---------------------------------------------------- TMA: weight codes + activation tiles

@@ -72,7 +72,7 @@ def test_routed_experts_matches_the_oracle_rule(bench):
 def test_traffic_record_follows_the_sources(bench, tmp_path, monkeypatch):
     rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
     # the committed record is reported only while it is keyed by the current sources
-    if rec["decode"]["source_hash"] == bench.kernel_source_hash():
+    if rec["decode"]["source_hash"] == bench.kernel_source_hash(rec["decode"].get("source_files")):
         assert bench.recorded_traffic("decode") == rec["decode"]["dram_bytes_per_call"]
     else:
         assert bench.recorded_traffic("decode") is None
