@@ -58,6 +58,8 @@ def parse():
                    help="override E (small cases for profiling; 0 = the workload's own)")
     p.add_argument("--tokens", type=int, default=0,
                    help="override T (small cases for profiling; 0 = the workload's own)")
+    p.add_argument("--no-graphs", dest="graphs", action="store_false",
+                   help="time each step as a k3moe_layer call instead of the replay of its captured CUDA graph")
     p.add_argument("--legs", default="all", choices=["all", "none"],
                    help="also time the other workloads (batch8, speculative-verify batches, prefill, "
                         "skewed, probe) into the line's workloads object")
@@ -417,6 +419,8 @@ def workload_config(a, s, name=None):
                         f"MXFP4 experts resident",
             "tokens": s.T, "hidden": s.H, "intermediate": s.I, "experts": s.E, "top_k": s.k,
             "l2": f"{getattr(a, 'l2_mode', 'L2 flushed between steps')}; inputs rotate over {a.sets} sets",
+            "launch": ("each timed step replays a CUDA graph holding one captured k3moe_layer call"
+                       if getattr(a, "graphs", False) else "each timed step is one k3moe_layer call"),
             "parallelism": f"replicas x{a.gpus}"}
 
 
@@ -528,9 +532,26 @@ class LayerBench:
         if ev is not None:
             ev[3].record(stream)
 
+    def capture(self):
+        """One CUDA graph per input set holding that set's k3moe_layer call (its
+        kernels keep their programmatic-launch edges in the graph), so that a timed
+        step is one graph launch on the host instead of a ctypes call and five
+        kernel launches: the host cannot fall behind the GPU."""
+        import torch
+        k3, s = self.k3, self.s
+        self.graphs = []
+        for j in range(self.nsets):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                k3.k3moe_layer(s, self.logits_d[j], self.x_d[j], self.W, self.idx, self.w, self.cnt, self.offsets,
+                               self.perm, self.inv, self.Y, self.out, None, self.mode, self.wsl, self.st)
+            self.graphs.append(g)
+        torch.cuda.synchronize()
+
     def run(self, steps, warmup, clocks=None, barrier=None):
-        """Warm-up, then K timed steps (events around each step only), then the same
-        K steps again with the expert FFN call bracketed (phase split)."""
+        """Warm-up, then K timed steps (events around each step only; each step a
+        graph replay when the graphs were captured), then the same K steps again as
+        separate calls with the expert FFN call bracketed (phase split)."""
         import torch
         for i in range(warmup):
             if self.do_flush:
@@ -539,6 +560,12 @@ class LayerBench:
         torch.cuda.synchronize()
         if int(self.st.item()) != 0:
             raise RuntimeError(f"{self.name}: device status {int(self.st.item())} during warm-up")
+        self.graphs = None
+        if getattr(self.a, "graphs", False):
+            self.capture()
+            for i in range(warmup):
+                self.graphs[i % self.nsets].replay()
+            torch.cuda.synchronize()
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
         pevs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
         if barrier:
@@ -549,7 +576,13 @@ class LayerBench:
         for i in range(steps):
             if self.do_flush:
                 self.flush.fill_((i + 1) & 0xFF)
-            self.layer(warmup + i, evs[i])
+            if self.graphs is not None:
+                ev = evs[i]
+                ev[0].record(self.stream)
+                self.graphs[(warmup + i) % self.nsets].replay()
+                ev[3].record(self.stream)
+            else:
+                self.layer(warmup + i, evs[i])
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
         for i in range(steps):

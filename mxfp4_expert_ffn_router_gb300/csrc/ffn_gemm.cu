@@ -754,6 +754,7 @@ struct SfChunk {
 // Bounded wait that also gives up as soon as another role has given up (`abort`
 // in shared memory); a timeout raises the flag.  Returns true when the phase completed.
 __device__ __forceinline__ bool mb_wait_or_abort(uint64_t *b, uint32_t parity, volatile int *abort) {
+  if (mb_test(b, parity)) return true;
   for (long long i = 0; i < kSpinG; ++i) {
     if (mb_try(b, parity)) return true;
     if (*abort) return false;
