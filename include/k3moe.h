@@ -107,8 +107,8 @@ typedef struct {
                               register-pipelined GEMV kernels                           */
 #define K3MOE_FFN_GEMM 3   /* grouped GEMMs on the tcgen05 tensor cores (weights dequantised
                               exactly to bf16, fp32 accumulators in tensor memory) for
-                              token chunks; needs H and 2I multiples of 128 and I a
-                              multiple of 64 (else K3MOE_ERR_UNSUPPORTED).              */
+                              token chunks; needs H and I multiples of 128
+                              (else K3MOE_ERR_UNSUPPORTED).                             */
 #define K3MOE_FFN_W4A4 4   /* the GEMM mode with MXFP4 activations: x and h are quantised to
                               MXFP4 per 32-block (k3moe_quantize_mxfp4's rule) before the
                               products, which are then exact; same shape rules as GEMM.

@@ -26,16 +26,18 @@
 // two CTAs per SM:
 //  * warp 8 (TMA): per weight stage (256 K values) two 2-D boxes of weight
 //    codes, 64 rows x 128 bytes each, 128B-swizzled, through the expert's tensor
-//    map (built on the device by gemm_sched_kernel); per K step of 64 one
-//    128-row box of the activation tile;
+//    map (built on the device by gemm_sched_kernel); per K step of 128 two
+//    128-row boxes of 64 values of the activation tile;
 //  * warps 0-7 (dequantisation): thread = one weight row (tensor-memory lane)
-//    and one K half; reads 16 code bytes from shared memory, converts e2m1 pairs
-//    to f16, multiplies by 2^(s - s_ref) and stores the 128 x 64 A stage to
-//    tensor memory with tcgen05.st; one mbarrier arrival per warp and stage;
+//    and one K half; reads 2 x 16 code bytes from shared memory, converts e2m1
+//    pairs to f16, multiplies by 2^(s - s_ref) and stores the 128 x 128 A stage
+//    to tensor memory with tcgen05.st; one mbarrier arrival per warp and stage;
 //  * warp 9 (MMA): owns tensor memory, issues tcgen05.mma kind::f16 with A from
-//    tensor memory and B (activations) from shared memory, M=128, K=16 each,
-//    and commits every stage back to the producers.
-// Four A/activation stages and two weight stages.  The epilogue (warps 0-7)
+//    tensor memory and B (activations) from shared memory, M=128, K=16 each
+//    (8 per stage), and commits every stage back to the producers.
+// A K step of 128 rather than 64 halves the waits, arrivals and commits per MMA:
+// on the issuing thread one satisfied wait plus one commit cost about as much as
+// two MMAs.  Two A/activation stages and two weight stages.  The epilogue (warps 0-7)
 // reads the accumulator with tcgen05.ld and writes h (bf16, the fixed rounding
 // point) or Y (fp32) rows through shared memory.
 #include <cuda.h>
@@ -59,9 +61,11 @@ constexpr int kMmaWarp = kDqWarps + 1;          // tensor-memory owner, MMA issu
 constexpr int kThreadsG = (kDqWarps + 2) * 32;  // 320
 constexpr int kTileM = 128;     // weight rows per tile
 constexpr int kTileN = 128;     // tokens per tile (max)
-constexpr int kTileK = 64;      // K per stage: one 128-byte swizzle atom of 16-bit values
-constexpr int kStagesG = 4;
-constexpr int kStageB = kTileN * kTileK * 2;  // 16 KiB of shared memory per stage (activation tile)
+constexpr int kTileK = 128;     // K per stage: two 128-byte swizzle atoms of 16-bit values
+constexpr int kBoxK = 64;       // K of one activation box (one 128-byte swizzle atom)
+constexpr int kStagesG = 2;
+constexpr int kStageB = kTileN * kTileK * 2;  // 32 KiB of shared memory per stage (activation tile)
+constexpr int kBoxB = kTileN * kBoxK * 2;     // 16 KiB: one box of the stage
 constexpr int kAcols = kTileK / 2;             // tensor-memory columns of one A stage (f16 pairs)
 constexpr int kTmemCols = 256;                 // accumulator (kTileN columns) + kStagesG A stages
 // weight codes reach shared memory by 2-D TMA boxes of 128 code bytes (256 K
@@ -101,6 +105,16 @@ __device__ __forceinline__ void tc_mma_f16_ta(uint32_t tmem_d, uint32_t tmem_a, 
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
       "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// 32 lanes x 32 bit, 16 consecutive columns per thread, registers -> tensor memory;
+// completion is awaited by a later tc_st16 (tcgen05.wait::st covers every earlier store).
+__device__ __forceinline__ void tc_st16_issue(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
 // 32 lanes x 32 bit, 16 consecutive columns per thread, registers -> tensor memory.
@@ -502,52 +516,59 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     smax = sref_s[r];
     const uint32_t a_lane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
     const uint8_t *wsm = gsm + kStagesG * kStageB + r * (kWK / 2);
-    // K steps in groups of 8 (a 16-byte window of the row's scale bytes, two
-    // weight stages); the next window's scales are loaded one group ahead
+    // K steps in groups of 4 (a 16-byte window of the row's scale bytes: 4 blocks
+    // of 32 values per step, two weight stages); the next window's scales are
+    // loaded one group ahead
     uint4 scv = make_uint4(0, 0, 0, 0);
     if (svec) scv = *reinterpret_cast<const uint4 *>(srow);
-    for (int kb = 0; kb < ksteps; kb += 8) {
+    for (int kb = 0; kb < ksteps; kb += 4) {
       uint4 scn = make_uint4(0, 0, 0, 0);
-      if (svec && kb + 8 < ksteps) scn = *reinterpret_cast<const uint4 *>(srow + 2 * (kb + 8));
+      if (svec && kb + 4 < ksteps) scn = *reinterpret_cast<const uint4 *>(srow + 4 * (kb + 4));
       const uint32_t sw[4] = {scv.x, scv.y, scv.z, scv.w};
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < 4; ++j) {
         const int ks = kb + j;
         if (ks >= ksteps) break;
         const int wst = ks / kWSteps, ws = wst % kWStages;
-        if ((j % kWSteps) == 0 && !mb_wait(&wfull_bar[ws], static_cast<uint32_t>(wst / kWStages) & 1u)) timeout = true;
-        int sbyte = 0;
-        if (svec) sbyte = static_cast<int>((sw[j >> 1] >> (16 * (j & 1) + 8 * hf)) & 0xFFu);
-        else if (present) sbyte = srow[2 * ks + hf];
+        if ((ks % kWSteps) == 0 && !mb_wait(&wfull_bar[ws], static_cast<uint32_t>(wst / kWStages) & 1u)) timeout = true;
         const int s = ks % kStagesG;
         const uint32_t lap = static_cast<uint32_t>(ks / kStagesG);
         if (!mb_wait(&empty_bar[s], (lap & 1u) ^ 1u)) timeout = true;
-        uint4 cw = make_uint4(0, 0, 0, 0);
-        if (present)
-          cw = *reinterpret_cast<const uint4 *>(wsm + ws * kWStageB + ((((j % kWSteps) * 2 + hf) ^ (r & 7)) << 4));
-        const uint32_t mulbits = f16_pow2_bits(sbyte - smax);
-        const uint32_t mul2 = mulbits | (mulbits << 16);
-        const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-        uint32_t o[16];  // 32 f16 = columns 16*hf .. 16*hf+15 of the stage (two K values per column)
+        // this thread's two blocks of the step: 4 ks + 2 hf + cc
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t h[4];
-          e2m1x8_to_f16x2(words[c], h);
+        for (int cc = 0; cc < 2; ++cc) {
+          int sbyte = 0;
+          if (svec) sbyte = static_cast<int>((sw[j] >> (8 * (2 * hf + cc))) & 0xFFu);
+          else if (present) sbyte = srow[4 * ks + 2 * hf + cc];
+          uint4 cw = make_uint4(0, 0, 0, 0);
+          if (present)
+            cw = *reinterpret_cast<const uint4 *>(wsm + ws * kWStageB +
+                                                  (((((ks % kWSteps) * 4) + 2 * hf + cc) ^ (r & 7)) << 4));
+          const uint32_t mulbits = f16_pow2_bits(sbyte - smax);
+          const uint32_t mul2 = mulbits | (mulbits << 16);
+          const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+          uint32_t o[16];  // 32 f16 = columns 32 hf + 16 cc .. + 15 of the stage (two K values per column)
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            const __half2 a = *reinterpret_cast<const __half2 *>(&h[m]);
-            const __half2 b = *reinterpret_cast<const __half2 *>(&mul2);
-            const __half2 prod = __hmul2(a, b);
-            o[4 * c + m] = *reinterpret_cast<const uint32_t *>(&prod);
+          for (int c = 0; c < 4; ++c) {
+            uint32_t h[4];
+            e2m1x8_to_f16x2(words[c], h);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              const __half2 a = *reinterpret_cast<const __half2 *>(&h[m]);
+              const __half2 b = *reinterpret_cast<const __half2 *>(&mul2);
+              const __half2 prod = __hmul2(a, b);
+              o[4 * c + m] = *reinterpret_cast<const uint32_t *>(&prod);
+            }
           }
+          if (cc == 0) tc_st16_issue(a_lane + kTileN + s * kAcols + 32 * hf, o);
+          else tc_st16(a_lane + kTileN + s * kAcols + 32 * hf + 16, o);  // waits for both stores
         }
-        tc_st16(a_lane + kTileN + s * kAcols + 16 * hf, o);  // waits for the warp's stores
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
           mb_arrive(&full_bar[s]);
           // the weight stage is free once this warp has read its last K step
-          if ((j % kWSteps) == kWSteps - 1 || ks == ksteps - 1) mb_arrive(&wempty_bar[ws]);
+          if ((ks % kWSteps) == kWSteps - 1 || ks == ksteps - 1) mb_arrive(&wempty_bar[ws]);
         }
       }
       scv = scn;
@@ -587,6 +608,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         uint8_t *sbuf = gsm + s * kStageB;
         mb_arrive_tx(&full_bar[s], kStageB);
         tma_load_2d(sbuf, &bmap, ks * kTileK, g.p0, &full_bar[s]);
+        tma_load_2d(sbuf + kBoxB, &bmap, ks * kTileK + kBoxK, g.p0, &full_bar[s]);
       }
       __syncwarp();
     }
@@ -602,8 +624,9 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         const uint32_t b0 = su32(gsm + s * kStageB);
         const uint32_t a0 = tmem + kTileN + s * kAcols;
 #pragma unroll
-        for (int kk = 0; kk < kTileK / 16; ++kk)  // K = 16 per MMA: A +8 columns, B +32 bytes in the atom
-          tc_mma_f16_ta(tmem, a0 + kk * 8, smem_desc_sw128(b0 + kk * 32), idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kTileK / 16; ++kk)  // K = 16 per MMA: A +8 columns, B +32 bytes in a box's atom
+          tc_mma_f16_ta(tmem, a0 + kk * 8, smem_desc_sw128(b0 + (kk >> 2) * kBoxB + (kk & 3) * 32), idesc,
+                        (ks > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&empty_bar[s]);
       }
       tc_commit(&acc_bar);
@@ -1163,7 +1186,7 @@ bool make_row_map(CUtensorMap *m, void *base, int rows, int K) {
   if (!fn) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-  const cuuint32_t box[2] = {kTileK, kTileN};
+  const cuuint32_t box[2] = {kBoxK, kTileN};
   const cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,

@@ -40,7 +40,7 @@ def resolved_mode(s, mode):
     if mode != k3.K3MOE_FFN_AUTO:
         return mode
     A = s.T * s.k
-    gemm_ok = (2 * s.I) % 128 == 0 and s.H % 128 == 0 and s.I % 64 == 0
+    gemm_ok = s.H % 128 == 0 and s.I % 128 == 0
     return k3.K3MOE_FFN_GEMM if gemm_ok and 2 * A >= 3 * min(A, s.E) else k3.K3MOE_FFN_GEMV
 
 
