@@ -15,9 +15,9 @@
 //
 // Kernels of one call:
 //   gemv_prep    active-expert slots (block-parallel scan of the offsets),
-//                x -> prescaled f16 (piece-major), zeroed per-row maxima of h
+//                x -> prescaled f16 (piece-major)
 //   gemv_rows<0> item = (active slot u, row pair i): for each token p of u,
-//                h[p][i] = bf16(silu(Wg_i x_p) * (Wu_i x_p)), max|h[p]| by atomicMax
+//                h[p][i] = bf16(silu(Wg_i x_p) * (Wu_i x_p)), plain stores
 //   gemv_h16     h rows -> prescaled f16 (exponent from the row's max |h|)
 //   gemv_rows<1> item = (active slot u, 4 rows of W2): Y[p][rows] = W2 rows . h[p]
 //
@@ -42,7 +42,7 @@ constexpr int kDnRows = 4;    // W2 rows per down item
 
 // Workspace layout (byte offsets, 256-aligned pieces).
 struct GemvWs {
-  size_t slots, meta, xexp, x16, hrow, hmax, h16, hexp, total;
+  size_t slots, meta, xexp, x16, hrow, h16, hexp, total;
 };
 
 __host__ __device__ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -57,7 +57,6 @@ __host__ __device__ inline GemvWs gemv_ws(int T, int H, int I, int E, int k) {
   w.xexp = o;  o = align256(o + sizeof(int32_t) * (T > 0 ? T : 1));
   w.x16 = o;   o = align256(o + sizeof(uint16_t) * static_cast<size_t>(T) * H);
   w.hrow = o;  o = align256(o + sizeof(uint16_t) * A * I);          // h, bf16 (the rounding point)
-  w.hmax = o;  o = align256(o + sizeof(int32_t) * a1);              // max |h| per row, as float bits
   w.h16 = o;   o = align256(o + sizeof(uint16_t) * A * I);          // h, prescaled f16, piece-major
   w.hexp = o;  o = align256(o + sizeof(int32_t) * a1);
   w.total = o;
@@ -125,13 +124,12 @@ __device__ __forceinline__ bool expert_present(const k3moe_weights &w, int e) {
 // ----------------------------------------------------------------------------
 // prep.  Block 0: slots of the active experts in expert order, from a
 // block-parallel scan of the bucket offsets (thread i reads experts
-// [i*m, (i+1)*m), m = ceil(E/256) <= 16), and zeroed per-row maxima of h.
+// [i*m, (i+1)*m), m = ceil(E/256) <= 16).
 // Block 1 + t: x[t] -> prescaled f16.
 __global__ void __launch_bounds__(256)
     gemv_prep_kernel(k3moe_weights w, const uint16_t *__restrict__ x, int T, int H, int E, int A,
                      const int32_t *__restrict__ offsets, int4 *__restrict__ slots, int32_t *__restrict__ meta,
-                     int32_t *__restrict__ xexp, uint4 *__restrict__ x16, int32_t *__restrict__ hmax,
-                     int32_t *status) {
+                     int32_t *__restrict__ xexp, uint4 *__restrict__ x16, int32_t *status) {
   pdl_wait();
   pdl_trigger();
   if (blockIdx.x == 0) {
@@ -184,7 +182,6 @@ __global__ void __launch_bounds__(256)
         }
       }
     }
-    for (int p = tid; p < A; p += 256) hmax[p] = 0;
     if (tid == 0) {
       meta[0] = bad ? 0 : total;
       if (bad) set_status(status, K3MOE_DEV_BOUNDS);
@@ -202,17 +199,33 @@ __global__ void __launch_bounds__(256)
   row_to_f16_piece_major(xr, H, scale_pow2(1.0f, -p), x16 + static_cast<size_t>(t) * (H / 8));
 }
 
-// h row p -> prescaled f16 (piece-major), exponent from the row's max |h|.
+// h row p -> prescaled f16 (piece-major), exponent from the row's max |h| (a row
+// holding a NaN takes exponent 0, as prescale_exp gives for a NaN maximum).  The
+// block finds the maximum itself: the gate/up kernels write h with plain stores
+// and no per-row atomics.
 __global__ void __launch_bounds__(256)
-    gemv_h16_kernel(const uint16_t *__restrict__ hrow, const int32_t *__restrict__ hmax, int I,
-                    uint4 *__restrict__ h16, int32_t *__restrict__ hexp) {
+    gemv_h16_kernel(const uint16_t *__restrict__ hrow, int I, uint4 *__restrict__ h16, int32_t *__restrict__ hexp) {
   pdl_wait();
   pdl_trigger();
   const int p = blockIdx.x;
-  const int e = prescale_exp(__int_as_float(hmax[p]));
+  const uint16_t *row = hrow + static_cast<size_t>(p) * I;
+  __shared__ float red[8];
+  float mx = 0.f;
+  bool nan_here = false;
+  for (int c = threadIdx.x * 8; c < I; c += 256 * 8) {
+    const uint4 v = *reinterpret_cast<const uint4 *>(row + c);
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const float a = fabsf(__uint_as_float(u[m] << 16)), b = fabsf(__uint_as_float(u[m] & 0xFFFF0000u));
+      nan_here |= (a != a) || (b != b);
+      mx = fmaxf(mx, fmaxf(a, b));
+    }
+  }
+  const bool any_nan = __syncthreads_or(nan_here) != 0;
+  const int e = any_nan ? 0 : prescale_exp(block_max_256(mx, red));
   if (threadIdx.x == 0) hexp[p] = e;
-  row_to_f16_piece_major(hrow + static_cast<size_t>(p) * I, I, scale_pow2(1.0f, -e),
-                         h16 + static_cast<size_t>(p) * (I / 8));
+  row_to_f16_piece_major(row, I, scale_pow2(1.0f, -e), h16 + static_cast<size_t>(p) * (I / 8));
 }
 
 // ----------------------------------------------------------------------------
@@ -225,7 +238,6 @@ struct RowsParams {
   const int32_t *aexp;   // activation prescale exponent: per token (gate/up) or per bucket position (down)
   const uint4 *act;      // activations, f16 piece-major: x16 [T][H] (gate/up) or h16 [A][I] (down)
   uint16_t *hrow;        // gate/up output, bf16 [A][I]
-  int32_t *hmax;         // gate/up output, max |h| per row
   float *Y;              // down output, [A][H]
   int32_t *status;
 };
@@ -375,7 +387,6 @@ __global__ void __launch_bounds__(kGvWarps * 32, 2) gemv_rows_kernel(RowsParams 
             }
             const uint16_t hb = f32_to_bf16_rne(hv);
             P.hrow[static_cast<size_t>(p0 + t) * P.I + rb] = hb;
-            atomicMax(P.hmax + p0 + t, static_cast<int>(__float_as_uint(fabsf(bf16_bits_to_f32(hb)))));
           }
         }
       } else {
@@ -542,7 +553,6 @@ __global__ void __launch_bounds__(kGvWarps * 32, 2) gemv_rows_pipe_kernel(RowsPa
           }
           const uint16_t hb = f32_to_bf16_rne(hv);
           P.hrow[static_cast<size_t>(p) * P.I + cur.rb] = hb;
-          atomicMax(P.hmax + p, static_cast<int>(__float_as_uint(fabsf(bf16_bits_to_f32(hb)))));
         }
       } else {
 #pragma unroll
@@ -626,8 +636,8 @@ cudaError_t launch_rows_nt1(const RowsParams &P, int K, int nsm, cudaStream_t st
 // weight codes stay in registers while the warp loops over the expert's tokens.
 int launch_rows(RowsParams P, int nsm, cudaStream_t st, int A, uint4 *h16, int32_t *hexp) {
   if (launch_rows_nt1<0, 2>(P, P.H, nsm, st) != cudaSuccess) return -1;
-  if (launch_pdl(gemv_h16_kernel, dim3(A), dim3(256), 0, st, static_cast<const uint16_t *>(P.hrow),
-                 static_cast<const int32_t *>(P.hmax), P.I, h16, hexp) != cudaSuccess)
+  if (launch_pdl(gemv_h16_kernel, dim3(A), dim3(256), 0, st, static_cast<const uint16_t *>(P.hrow), P.I, h16,
+                 hexp) != cudaSuccess)
     return -1;
   P.aexp = hexp;
   P.act = h16;
@@ -645,7 +655,6 @@ GemvBufs gemv_bufs(const k3moe_shape &s, void *ws) {
   b.xexp = reinterpret_cast<int32_t *>(base + L.xexp);
   b.x16 = reinterpret_cast<uint4 *>(base + L.x16);
   b.hrow = reinterpret_cast<uint16_t *>(base + L.hrow);
-  b.hmax = reinterpret_cast<int32_t *>(base + L.hmax);
   b.h16 = reinterpret_cast<uint4 *>(base + L.h16);
   b.hexp = reinterpret_cast<int32_t *>(base + L.hexp);
   return b;
@@ -654,14 +663,14 @@ GemvBufs gemv_bufs(const k3moe_shape &s, void *ws) {
 int launch_gemv_prep(const k3moe_shape &s, const uint16_t *x, const k3moe_weights &w, const int32_t *offsets,
                      const GemvBufs &b, int32_t *status, cudaStream_t st) {
   return launch_pdl(gemv_prep_kernel, dim3(1 + s.T), dim3(256), 0, st, w, x, s.T, s.H, s.E, s.T * s.k, offsets,
-                    b.slots, b.meta, b.xexp, b.x16, b.hmax, status) == cudaSuccess
+                    b.slots, b.meta, b.xexp, b.x16, status) == cudaSuccess
              ? 0
              : -1;
 }
 
 int launch_gemv_h16(const k3moe_shape &s, const GemvBufs &b, cudaStream_t st) {
-  return launch_pdl(gemv_h16_kernel, dim3(s.T * s.k), dim3(256), 0, st, static_cast<const uint16_t *>(b.hrow),
-                    static_cast<const int32_t *>(b.hmax), s.I, b.h16, b.hexp) == cudaSuccess
+  return launch_pdl(gemv_h16_kernel, dim3(s.T * s.k), dim3(256), 0, st, static_cast<const uint16_t *>(b.hrow), s.I,
+                    b.h16, b.hexp) == cudaSuccess
              ? 0
              : -1;
 }
@@ -711,8 +720,7 @@ __global__ void __launch_bounds__(1024)
                        int H, int E, int k, int32_t *__restrict__ idx, float *__restrict__ wts,
                        int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int32_t *__restrict__ perm,
                        int32_t *__restrict__ inv, int4 *__restrict__ slots, int32_t *__restrict__ meta,
-                       int32_t *__restrict__ xexp, uint4 *__restrict__ x16, int32_t *__restrict__ hmax,
-                       int32_t *status) {
+                       int32_t *__restrict__ xexp, uint4 *__restrict__ x16, int32_t *status) {
   pdl_wait();
   pdl_trigger();
   __shared__ int s_idx[kFrontMaxA];
@@ -850,7 +858,6 @@ __global__ void __launch_bounds__(1024)
     s_xexp[tid] = p;
     xexp[tid] = p;
   }
-  for (int p = tid; p < A; p += 1024) hmax[p] = 0;
   __syncthreads();
   // ---- phase C: offsets and counts by binary search in the sorted experts,
   //      active slots (first position of each expert), x rows to prescaled f16
@@ -901,7 +908,7 @@ int launch_layer_gemv_fast(const k3moe_shape &s, const float *logits, const uint
   if (s.T == 0) return 0;
   const GemvBufs b = gemv_bufs(s, ws);
   if (launch_pdl(layer_front_kernel, dim3(1), dim3(1024), 0, st, logits, x, w, s.T, s.H, s.E, s.k, idx, wts, counts,
-                 offsets, perm, inv, b.slots, b.meta, b.xexp, b.x16, b.hmax, status) != cudaSuccess)
+                 offsets, perm, inv, b.slots, b.meta, b.xexp, b.x16, status) != cudaSuccess)
     return -1;
   RowsParams P;
   P.w = w;
@@ -915,7 +922,6 @@ int launch_layer_gemv_fast(const k3moe_shape &s, const float *logits, const uint
   P.aexp = b.xexp;
   P.act = b.x16;
   P.hrow = b.hrow;
-  P.hmax = b.hmax;
   P.Y = Y;
   P.status = status;
   if (launch_rows(P, sm_count(), st, P.A, b.h16, b.hexp)) return -1;
@@ -940,7 +946,6 @@ int launch_ffn_gemv(const k3moe_shape &s, const uint16_t *x, const k3moe_weights
   P.aexp = b.xexp;
   P.act = b.x16;
   P.hrow = b.hrow;
-  P.hmax = b.hmax;
   P.Y = Y;
   P.status = status;
   return launch_rows(P, sm_count(), st, P.A, b.h16, b.hexp);

@@ -53,7 +53,6 @@ struct GemvBufs {
   int32_t *xexp;    // prescale exponent per token
   uint4 *x16;       // x as prescaled f16, piece-major [T][H/8]
   uint16_t *hrow;   // h, bf16 [A][I] (the rounding point)
-  int32_t *hmax;    // max |h| per bucket position (float bits)
   uint4 *h16;       // h as prescaled f16, piece-major [A][I/8]
   int32_t *hexp;    // prescale exponent per bucket position
 };
