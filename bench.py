@@ -364,7 +364,7 @@ def resolved_mode(s, mode):
         return mode
     A = s.T * s.k
     gemm_ok = s.H % 128 == 0 and s.I % 128 == 0
-    return 3 if gemm_ok and 4 * A >= 5 * min(A, s.E) else 1
+    return 3 if gemm_ok and 5 * A >= 4 * s.E else 1
 
 
 def ffn_kernel_count(s, mode):

@@ -96,8 +96,8 @@ typedef struct {
 
 /* Expert FFN modes.  All compute the same function (bf16 activations, exact
  * MXFP4 weights, fp32 accumulation); they differ in how weights are streamed. */
-#define K3MOE_FFN_AUTO 0   /* the library picks per call: GEMM when 4 A >= 5 min(A, E)
-                              (A = T*k; 1.25 assignments per expert that can be active)
+#define K3MOE_FFN_AUTO 0   /* the library picks per call: GEMM when 5 A >= 4 E
+                              (A = T*k; 0.8 assignments per expert)
                               and the shape allows it, else GEMV                      */
 #define K3MOE_FFN_GEMV 1   /* CUDA-core GEMV kernels, 128-bit register loads (any shape);
                               each routed expert's weights are read once per call     */

@@ -22,19 +22,29 @@
 //    prescale per row (max|v| * 2^-p in [2^14, 2^15)), laid out in bucket order
 //    by two small pre-pass kernels so that a 2-D TMA tile load fetches them.
 //
-// One CTA per tile (active expert, 128 weight rows, <= 128 tokens), 10 warps,
+// One CTA per tile (active expert, 128 weight rows, <= 128 tokens), 11 warps,
 // two CTAs per SM:
-//  * warp 8 (TMA): per weight stage (256 K values) two 2-D boxes of weight
-//    codes, 64 rows x 128 bytes each, 128B-swizzled, through the expert's tensor
-//    map (built on the device by gemm_sched_kernel); per K step of 128 two
-//    128-row boxes of 64 values of the activation tile;
+//  * warp 8 (TMA, activations): per K step of 128 two boxes of 64 values of the
+//    activation tile, as soon as the MMA has released the stage; a box is only
+//    as high as the tile's tokens rounded up to 16 (one tensor map per height),
+//    not 128 rows, which cuts the L2-to-shared-memory traffic of a prefill tile
+//    (about 73 tokens per expert) by about a third;
+//  * warp 9 (TMA, weights): per weight stage (256 K values) two 2-D boxes of
+//    weight codes, 64 rows x 128 bytes each, 128B-swizzled, through the expert's
+//    tensor map (built on the device by gemm_sched_kernel), as soon as the
+//    dequantising warps have released the stage.  The two rings have their own
+//    producers so that an activation load never waits for a weight stage to
+//    drain (with one producer thread every activation tile, and its L2 latency,
+//    joined the chain from one K step to the next);
 //  * warps 0-7 (dequantisation): thread = one weight row (tensor-memory lane)
 //    and one K half; reads 2 x 16 code bytes from shared memory, converts e2m1
 //    pairs to f16, multiplies by 2^(s - s_ref) and stores the 128 x 128 A stage
 //    to tensor memory with tcgen05.st; one mbarrier arrival per warp and stage;
-//  * warp 9 (MMA): owns tensor memory, issues tcgen05.mma kind::f16 with A from
+//  * warp 10 (MMA): owns tensor memory, issues tcgen05.mma kind::f16 with A from
 //    tensor memory and B (activations) from shared memory, M=128, K=16 each
-//    (8 per stage), and commits every stage back to the producers.
+//    (8 per stage, four per asm block: the issuing thread shares its scheduler
+//    with dequantising warps, so each instruction it spends per MMA shows), and
+//    commits every stage back to the producers.
 // A K step of 128 rather than 64 halves the waits, arrivals and commits per MMA:
 // on the issuing thread one satisfied wait plus one commit cost about as much as
 // two MMAs.  Two A/activation stages and two weight stages.  The epilogue (warps 0-7)
@@ -57,8 +67,9 @@ namespace {
 
 constexpr int kDqWarps = 8;                     // dequantisation + epilogue warps
 constexpr int kTmaWarp = kDqWarps;              // activation-tile TMA producer
-constexpr int kMmaWarp = kDqWarps + 1;          // tensor-memory owner, MMA issuer
-constexpr int kThreadsG = (kDqWarps + 2) * 32;  // 320
+constexpr int kWTmaWarp = kDqWarps + 1;         // weight-code TMA producer
+constexpr int kMmaWarp = kDqWarps + 2;          // tensor-memory owner, MMA issuer
+constexpr int kThreadsG = (kDqWarps + 3) * 32;  // 352
 constexpr int kTileM = 128;     // weight rows per tile
 constexpr int kTileN = 128;     // tokens per tile (max)
 constexpr int kTileK = 128;     // K per stage: two 128-byte swizzle atoms of 16-bit values
@@ -98,13 +109,24 @@ __device__ __forceinline__ uint32_t idesc_f16(int M, int N) {
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
-// A operand from tensor memory (M lanes x K/2 columns of f16 pairs), B from shared memory.
-__device__ __forceinline__ void tc_mma_f16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
-                                              uint32_t accumulate) {
+// A operand from tensor memory (M lanes x K/2 columns of f16 pairs), B from shared memory:
+// four MMAs over one 64-value box of the B stage (K = 16 each): A columns a,
+// a + 8, a + 16, a + 24 and B descriptors b, b + 2, b + 4, b + 6 (32 bytes
+// further each, in the descriptor's address field).  The first accumulates
+// when `acc` is nonzero, the other three always.  One asm block keeps the
+// issuing thread to about three instructions per MMA: it shares its scheduler
+// with busy dequantisation warps, so every instruction it issues costs cycles.
+__device__ __forceinline__ void tc_mma4_f16_ta(uint32_t tmem_d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred p, q;\n\t.reg .b32 a1, a2, a3;\n\t.reg .b64 b1, b2, b3;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 q, %3, %3;\n\t"
+      "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\t"
+      "add.u64 b1, %2, 2;\n\tadd.u64 b2, %2, 4;\n\tadd.u64 b3, %2, 6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, q;\n\t}" ::"r"(tmem_d),
+      "r"(a), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
 // 32 lanes x 32 bit, 16 consecutive columns per thread, registers -> tensor memory;
@@ -400,6 +422,12 @@ struct GemmParams {
   int32_t *status;
 };
 
+// Activation-tile maps whose boxes are 16, 32, ..., 128 rows high: a tile loads
+// only its expert's tokens (rounded up to 16), not 128 rows.
+struct RowMaps {
+  CUtensorMap m[kTileN / 16];
+};
+
 // dynamic shared memory: 1024 bytes of alignment slack, the activation stages,
 // then the weight stages (the epilogue transpose buffer [kTileN][kTileM + 1]
 // fp32 reuses them once every stage has been consumed)
@@ -417,7 +445,7 @@ __device__ __forceinline__ int tile_wrow(int kind, int m0, int r, int I) {
 }
 
 __global__ void __launch_bounds__(kThreadsG, 1)
-    ffn_gemm_kernel(const __grid_constant__ CUtensorMap bmap, GemmParams P) {
+    ffn_gemm_kernel(const __grid_constant__ RowMaps bmaps, GemmParams P) {
   extern __shared__ __align__(1024) uint8_t gsm_raw[];
   // the 128B-swizzle atoms need 1024-byte aligned shared addresses: align explicitly
   uint8_t *gsm = gsm_raw + ((1024u - (su32(gsm_raw) & 1023u)) & 1023u);
@@ -492,17 +520,21 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     // 16-byte chunks of the row's scale bytes)
     int smax = 0;
     if (svec) {
-      for (int b = 16 * hf; b < sbytes; b += 32) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(srow + b);
-        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+      // the thread's 16-byte chunks of scale bytes are loaded 8 at a time, all in
+      // flight together (one memory latency per 8 chunks rather than one per chunk),
+      // and reduced bytewise
+      constexpr int kScanChunks = 8;
+      uint32_t m4 = 0;
+      for (int b0 = 16 * hf; b0 < sbytes; b0 += 32 * kScanChunks) {
+        uint4 v[kScanChunks];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          smax = max(smax, static_cast<int>(w4[m] & 0xFFu));
-          smax = max(smax, static_cast<int>((w4[m] >> 8) & 0xFFu));
-          smax = max(smax, static_cast<int>((w4[m] >> 16) & 0xFFu));
-          smax = max(smax, static_cast<int>(w4[m] >> 24));
-        }
+        for (int c = 0; c < kScanChunks; ++c)
+          v[c] = b0 + 32 * c < sbytes ? *reinterpret_cast<const uint4 *>(srow + b0 + 32 * c) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int c = 0; c < kScanChunks; ++c)
+          m4 = __vmaxu4(__vmaxu4(m4, __vmaxu4(v[c].x, v[c].y)), __vmaxu4(v[c].z, v[c].w));
       }
+      smax = static_cast<int>(max(max(m4 & 0xFFu, (m4 >> 8) & 0xFFu), max((m4 >> 16) & 0xFFu, m4 >> 24)));
     } else if (present) {
       for (int b = hf; b < sbytes; b += 2) smax = max(smax, static_cast<int>(srow[b]));
     }
@@ -574,18 +606,32 @@ __global__ void __launch_bounds__(kThreadsG, 1)
       scv = scn;
     }
   } else if (warp == kTmaWarp) {
-    // ---------------------------------------------------- TMA: weight codes + activation tiles
-    const int nws = (ksteps + kWSteps - 1) / kWSteps;
-    uint8_t *wbase = gsm + kStagesG * kStageB;
-    const CUtensorMap *wmap =
-        reinterpret_cast<const CUtensorMap *>(P.maps + static_cast<size_t>(kind * P.E + g.u) * kMapBytes);
-    // the map was written by the previous kernel: order its reads after those writes
-    if (present && lane == 0)
-      asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(wmap) : "memory");
-    const int y0 = tile_wrow(kind, g.m0, 0, P.I), y1 = tile_wrow(kind, g.m0, kWBoxRows, P.I);
-    auto issue_weights = [&](int wst) {
-      const int ws = wst % kWStages;
-      if (lane == 0) {
+    // ---------------------------------------------------- TMA: activation tiles
+    if (lane == 0) {
+      for (int ks = 0; ks < ksteps; ++ks) {
+        const int s = ks % kStagesG;
+        const uint32_t lap = static_cast<uint32_t>(ks / kStagesG);
+        if (!mb_wait(&empty_bar[s], (lap & 1u) ^ 1u)) timeout = true;
+        uint8_t *sbuf = gsm + s * kStageB;
+        const CUtensorMap *bm = &bmaps.m[Npad / 16 - 1];
+        mb_arrive_tx(&full_bar[s], static_cast<uint32_t>(2 * Npad * kBoxK * 2));
+        tma_load_2d(sbuf, bm, ks * kTileK, g.p0, &full_bar[s]);
+        tma_load_2d(sbuf + kBoxB, bm, ks * kTileK + kBoxK, g.p0, &full_bar[s]);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kWTmaWarp) {
+    // ---------------------------------------------------- TMA: weight codes
+    if (lane == 0) {
+      const int nws = (ksteps + kWSteps - 1) / kWSteps;
+      uint8_t *wbase = gsm + kStagesG * kStageB;
+      const CUtensorMap *wmap =
+          reinterpret_cast<const CUtensorMap *>(P.maps + static_cast<size_t>(kind * P.E + g.u) * kMapBytes);
+      // the map was written by the previous kernel: order its reads after those writes
+      if (present) asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(wmap) : "memory");
+      const int y0 = tile_wrow(kind, g.m0, 0, P.I), y1 = tile_wrow(kind, g.m0, kWBoxRows, P.I);
+      for (int wst = 0; wst < nws; ++wst) {
+        const int ws = wst % kWStages;
         if (!mb_wait(&wempty_bar[ws], (static_cast<uint32_t>(wst / kWStages) & 1u) ^ 1u)) timeout = true;
         mb_arrive_tx(&wfull_bar[ws], present ? static_cast<uint32_t>(kWStageB) : 0u);
         if (present) {
@@ -594,24 +640,8 @@ __global__ void __launch_bounds__(kThreadsG, 1)
           tma_load_2d(dst + kWStageB / 2, wmap, wst * (kWK / 2), y1, &wfull_bar[ws]);
         }
       }
-    };
-    for (int wst = 0; wst < kWStages - 1 && wst < nws; ++wst) issue_weights(wst);
-    for (int ks = 0; ks < ksteps; ++ks) {
-      if (ks % kWSteps == 0) {
-        const int wn = ks / kWSteps + kWStages - 1;
-        if (wn < nws) issue_weights(wn);
-      }
-      if (lane == 0) {
-        const int s = ks % kStagesG;
-        const uint32_t lap = static_cast<uint32_t>(ks / kStagesG);
-        if (!mb_wait(&empty_bar[s], (lap & 1u) ^ 1u)) timeout = true;
-        uint8_t *sbuf = gsm + s * kStageB;
-        mb_arrive_tx(&full_bar[s], kStageB);
-        tma_load_2d(sbuf, &bmap, ks * kTileK, g.p0, &full_bar[s]);
-        tma_load_2d(sbuf + kBoxB, &bmap, ks * kTileK + kBoxK, g.p0, &full_bar[s]);
-      }
-      __syncwarp();
     }
+    __syncwarp();
   } else {
     // ---------------------------------------------------- MMA issue
     if (lane == 0) {
@@ -621,12 +651,11 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         const uint32_t lap = static_cast<uint32_t>(ks / kStagesG);
         if (!mb_wait(&full_bar[s], lap & 1u)) timeout = true;
         tc_fence_after();
-        const uint32_t b0 = su32(gsm + s * kStageB);
+        const uint64_t bd = smem_desc_sw128(su32(gsm + s * kStageB));
         const uint32_t a0 = tmem + kTileN + s * kAcols;
 #pragma unroll
-        for (int kk = 0; kk < kTileK / 16; ++kk)  // K = 16 per MMA: A +8 columns, B +32 bytes in a box's atom
-          tc_mma_f16_ta(tmem, a0 + kk * 8, smem_desc_sw128(b0 + (kk >> 2) * kBoxB + (kk & 3) * 32), idesc,
-                        (ks > 0 || kk > 0) ? 1u : 0u);
+        for (int bx = 0; bx < kTileK / kBoxK; ++bx)  // per box 4 MMAs of K = 16: A +8 columns, B +32 bytes
+          tc_mma4_f16_ta(tmem, a0 + bx * 32, bd + bx * (kBoxB >> 4), idesc, (ks > 0 || bx > 0) ? 1u : 0u);
         tc_commit(&empty_bar[s]);
       }
       tc_commit(&acc_bar);
@@ -786,6 +815,7 @@ __device__ __forceinline__ bool mb_wait_or_abort(uint64_t *b, uint32_t parity, v
   *abort = 1;
   return false;
 }
+
 
 }  // namespace
 
@@ -1179,19 +1209,47 @@ int launch_gemm_mxf4(const k3moe_shape &s, const uint16_t *x, const int32_t *per
 
 }  // namespace
 
-// 2-D map over rows x K of 16-bit values: box = 64 (K) x 128 rows, 128B swizzle,
+namespace {
+// 2-D map over rows x K of 16-bit values: box = 64 (K) x box_rows, 128B swizzle,
 // rows past the end read as zero.
-bool make_row_map(CUtensorMap *m, void *base, int rows, int K) {
+bool make_row_map_box(CUtensorMap *m, void *base, int rows, int K, int box_rows) {
   EncodeTiledFn fn = encode_tiled();
   if (!fn) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-  const cuuint32_t box[2] = {kBoxK, kTileN};
+  const cuuint32_t box[2] = {kBoxK, static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+// The maps of every box height over one buffer; the last encoding per buffer
+// role (x or h) is kept per thread, since the workspace is normally reused.
+bool make_row_maps(RowMaps *out, int role, void *base, int rows, int K) {
+  struct Entry {
+    void *base = nullptr;
+    int rows = -1, K = -1;
+    RowMaps maps;
+  };
+  thread_local Entry cache[2];
+  Entry &c = cache[role];
+  if (c.base != base || c.rows != rows || c.K != K) {
+    c.base = nullptr;
+    for (int i = 0; i < kTileN / 16; ++i)
+      if (!make_row_map_box(&c.maps.m[i], base, rows, K, 16 * (i + 1))) return false;
+    c.base = base;
+    c.rows = rows;
+    c.K = K;
+  }
+  *out = c.maps;
+  return true;
+}
+}  // namespace
+
+// 2-D map over rows x K of 16-bit values: box = 64 (K) x 128 rows, 128B swizzle,
+// rows past the end read as zero.
+bool make_row_map(CUtensorMap *m, void *base, int rows, int K) { return make_row_map_box(m, base, rows, K, kTileN); }
 
 size_t ffn_gemm_workspace(const k3moe_shape &s) { return gemm_ws(s.T, s.H, s.I, s.E, s.k).total; }
 size_t ffn_gemm_h_offset(const k3moe_shape &s) { return gemm_ws(s.T, s.H, s.I, s.E, s.k).hrow; }
@@ -1222,8 +1280,7 @@ int launch_ffn_gemm(const k3moe_shape &s, const uint16_t *x, const k3moe_weights
   uint16_t *h16 = reinterpret_cast<uint16_t *>(base + L.h16);
   int32_t *hexp = reinterpret_cast<int32_t *>(base + L.hexp);
   uint8_t *maps = reinterpret_cast<uint8_t *>(base + L.maps);
-  CUtensorMap xmap, hmap, t13, t2;
-  if (!make_row_map(&xmap, xg, A, s.H) || !make_row_map(&hmap, h16, A, s.I)) return -1;
+  CUtensorMap t13, t2;
   if (!make_code_map(&t13, maps, 2 * s.I, s.H / 2) || !make_code_map(&t2, maps, s.H, s.I / 2)) return -1;
   if (launch_pdl(gemm_prep_kernel, dim3(1), dim3(32), 0, st, offsets, s.E, A, mt_gu, mt_dn, active, meta, sp0,
                  scnt, pgu, pdn, status) != cudaSuccess)
@@ -1255,6 +1312,8 @@ int launch_ffn_gemm(const k3moe_shape &s, const uint16_t *x, const k3moe_weights
   if (launch_pdl(rows_to_f16, dim3(A), dim3(256), 0, st, x, perm, s.k, A, s.H, xg, xexp, status) !=
       cudaSuccess)
     return -1;
+  RowMaps xmaps, hmaps;
+  if (!make_row_maps(&xmaps, 0, xg, A, s.H) || !make_row_maps(&hmaps, 1, h16, A, s.I)) return -1;
   static bool attr = false;
   if (!attr) {
     if (cudaFuncSetAttribute(ffn_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem) !=
@@ -1275,7 +1334,7 @@ int launch_ffn_gemm(const k3moe_shape &s, const uint16_t *x, const k3moe_weights
   P.tab = tab_gu;
   P.bexp = xexp;
   if (launch_pdl(ffn_gemm_kernel, dim3(static_cast<unsigned>(ntile_max * mt_gu)), dim3(kThreadsG), kGemmSmem, st,
-                 xmap, P) != cudaSuccess)
+                 xmaps, P) != cudaSuccess)
     return -1;
   if (launch_pdl(rows_to_f16, dim3(A), dim3(256), 0, st, static_cast<const uint16_t *>(hrow),
                  static_cast<const int32_t *>(nullptr), 1, A, s.I, h16, hexp, status) != cudaSuccess)
@@ -1284,7 +1343,7 @@ int launch_ffn_gemm(const k3moe_shape &s, const uint16_t *x, const k3moe_weights
   P.tab = tab_dn;
   P.bexp = hexp;
   if (launch_pdl(ffn_gemm_kernel, dim3(static_cast<unsigned>(ntile_max * mt_dn)), dim3(kThreadsG), kGemmSmem, st,
-                 hmap, P) != cudaSuccess)
+                 hmaps, P) != cudaSuccess)
     return -1;
   return 0;
 }

@@ -70,14 +70,13 @@ extern "C" {
 static int resolve_ffn_mode(const k3moe_shape &s, int mode) {
   switch (mode) {
     case K3MOE_FFN_AUTO: {
-      // tensor cores once the assignments average 1.25 tokens or more per expert
-      // that can be active (measured at H = 7168, I = 2048, E = 896, k = 16 with
-      // independent routing: the GEMM overtakes the GEMV kernels between T = 64
-      // and T = 80); otherwise the GEMV kernels, which stream each routed
-      // expert's weights once for its tokens
+      // tensor cores once the assignments reach 0.8 per expert (measured at
+      // H = 7168, I = 2048, E = 896, k = 16 with independent routing: the GEMM
+      // overtakes the GEMV kernels between T = 32 and T = 48); otherwise the
+      // GEMV kernels, which stream each routed expert's weights once for its
+      // tokens but spend CUDA-core instructions on every token
       const long long A = static_cast<long long>(s.T) * s.k;
-      const long long experts = A < s.E ? A : s.E;
-      if (k3moe::ffn_gemm_supported(s) && 4 * A >= 5 * experts) return K3MOE_FFN_GEMM;
+      if (k3moe::ffn_gemm_supported(s) && 5 * A >= 4 * static_cast<long long>(s.E)) return K3MOE_FFN_GEMM;
       return K3MOE_FFN_GEMV;
     }
     case K3MOE_FFN_GEMV: return K3MOE_FFN_GEMV;

@@ -41,7 +41,7 @@ def resolved_mode(s, mode):
         return mode
     A = s.T * s.k
     gemm_ok = s.H % 128 == 0 and s.I % 128 == 0
-    return k3.K3MOE_FFN_GEMM if gemm_ok and 4 * A >= 5 * min(A, s.E) else k3.K3MOE_FFN_GEMV
+    return k3.K3MOE_FFN_GEMM if gemm_ok and 5 * A >= 4 * s.E else k3.K3MOE_FFN_GEMV
 
 
 def gamma(s, mode) -> float:

@@ -149,11 +149,11 @@ def _bench_module():
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("T,E,k,gemm", [
-    (1, 896, 16, False), (8, 896, 16, False), (64, 896, 16, False),   # < 1.25 assignments per possible expert
-    (80, 896, 16, True), (128, 896, 16, True), (300, 5, 1, True),     # >= 1.25: the tensor-core GEMM
+    (1, 896, 16, False), (8, 896, 16, False), (44, 896, 16, False),   # < 0.8 assignments per expert
+    (45, 896, 16, True), (128, 896, 16, True), (300, 5, 1, True),     # >= 0.8: the tensor-core GEMM
 ])
 def test_auto_mode_resolution(L, T, E, k, gemm):
-    """AUTO resolves to the GEMM exactly when 4 A >= 5 min(A, E) (the measured
+    """AUTO resolves to the GEMM exactly when 5 A >= 4 E (the measured
     crossover at H = 7168, I = 2048), seen through the workspace it asks for, and
     bench.py's mirror of the rule (which labels and counts the kernels) agrees."""
     import gen

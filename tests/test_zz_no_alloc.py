@@ -62,8 +62,8 @@ def test_noalloc_matches_workspace_entry_point_twice(T, H, I, E, k, mode):
 
 
 def test_noalloc_auto_is_gemv_where_the_workspace_entry_point_picks_the_gemm():
-    """T=8, E=48, k=16: k3moe_expert_ffn's AUTO takes the tensor-core GEMM (4A >= 5
-    min(A, E)); the allocation-free entry point's AUTO takes the GEMV kernels: its
+    """T=8, E=48, k=16: k3moe_expert_ffn's AUTO takes the tensor-core GEMM (5A >=
+    4E); the allocation-free entry point's AUTO takes the GEMV kernels: its
     output is bitwise the workspace entry point's GEMV output (the two modes are
     each checked against the oracle by the parity tests); GEMM and W4A4 are
     refused."""
