@@ -205,8 +205,10 @@ __global__ void __launch_bounds__(256)
 // and no per-row atomics.
 __global__ void __launch_bounds__(256)
     gemv_h16_kernel(const uint16_t *__restrict__ hrow, int I, uint4 *__restrict__ h16, int32_t *__restrict__ hexp) {
-  pdl_wait();
+  // dependents first: the down projection may then start on the SMs the gate/up
+  // kernel frees and prefetch its first weight rows while this kernel waits
   pdl_trigger();
+  pdl_wait();
   const int p = blockIdx.x;
   const uint16_t *row = hrow + static_cast<size_t>(p) * I;
   __shared__ float red[8];
@@ -231,7 +233,7 @@ __global__ void __launch_bounds__(256)
 // ----------------------------------------------------------------------------
 struct RowsParams {
   k3moe_weights w;
-  int H, I, k, A;
+  int H, I, k, A, E;
   const int32_t *perm;
   const int4 *slots;
   const int32_t *meta;
@@ -490,17 +492,50 @@ __device__ __forceinline__ void compute_half(const uint4 (&cw)[R][NH], const uin
   }
 }
 
+__device__ __forceinline__ void prefetch_line_l2(const void *p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
+// Down projection only: the weight rows of the warp's first two items into L2
+// before the kernel waits for its predecessor.  The slot table comes from a kernel
+// that completed before this one was launched and is read through L2 (bounds
+// checked all the same); the weights are not written by the predecessor.  It is a
+// hint: the rows are loaded again after the wait.
+template <int R, int NJ>
+__device__ __forceinline__ void prefetch_first_items(const RowsParams &P, int per_slot, long long item,
+                                                     long long stride) {
+  const int lane = threadIdx.x & 31;
+  const int nsl = min(__ldcg(P.meta), min(P.A, P.E));
+  const long long nit = static_cast<long long>(max(nsl, 0)) * per_slot;
+  for (int q = 0; q < 2; ++q, item += stride) {
+    if (item >= nit) return;
+    const int4 sl = __ldcg(P.slots + static_cast<int>(item / per_slot));
+    if (!sl.w || sl.x < 0 || sl.x >= P.E) continue;
+    const uint8_t *cb = ldg_ptr(P.w.w2_codes, sl.x), *sb = ldg_ptr(P.w.w2_scales, sl.x);
+    if (!cb || !sb) continue;
+    const int rb = static_cast<int>(item % per_slot);
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int row = min(rb * R + r, P.H - 1);
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) prefetch_line_l2(cb + static_cast<size_t>(row) * (512 * NJ) + 16 * lane + 512 * j);
+      if (lane == 0) prefetch_line_l2(sb + static_cast<size_t>(row) * (32 * NJ));
+    }
+  }
+}
+
 template <int KIND, int R, int NJ>
 __global__ void __launch_bounds__(kGvWarps * 32, 2) gemv_rows_pipe_kernel(RowsParams P) {
-  pdl_wait();
-  pdl_trigger();
   constexpr int HA = (NJ + 1) / 2, HB = NJ - HA;
   constexpr int NCH = 32 * NJ;  // chunks per row
   const int lane = threadIdx.x & 31;
   const int per_slot = KIND == 0 ? P.I : (P.H + R - 1) / R;
-  const long long nitems = static_cast<long long>(P.meta[0]) * per_slot;
   const long long stride = static_cast<long long>(gridDim.x) * kGvWarps;
   long long item = static_cast<long long>(blockIdx.x) * kGvWarps + (threadIdx.x >> 5);
+  if (KIND == 1) prefetch_first_items<R, NJ>(P, per_slot, item, stride);
+  pdl_wait();
+  pdl_trigger();
+  const long long nitems = static_cast<long long>(P.meta[0]) * per_slot;
   if (item >= nitems) return;
   ItemRows<R> cur;
   item_rows_at<KIND, R, NJ>(P, item, per_slot, cur);
@@ -688,13 +723,15 @@ int sm_count() {
 
 // ----------------------------------------------------------------------------
 // Decode front in one block: route, bucket and the GEMV prep of a small batch
-// (T <= 32 tokens, E <= 1024 experts, A = T k <= 512), writing exactly what the
+// (T <= 4 tokens, E <= 1024 experts, A = T k <= 128), writing exactly what the
 // route, bucket and prep kernels write (same selection order, same weights bit
 // for bit, same stable bucket order, same slots and prescaled activations).
 //  * route: warp t takes token t with warp-level operations only: lane l holds
-//    the order-preserving keys of experts l, l + 32, ...; a 32-step bit search
-//    with one warp reduction per step finds the k-th largest key, ties at it go
-//    in index order, the k picks are ordered by (key desc, index asc) and
+//    the order-preserving keys of experts l, l + 32, ...; k rounds of a warp
+//    arg-max (two warp reductions each: the largest key, then the smallest
+//    index holding it) give the picks in (key desc, index asc) order; in place
+//    of a 32-step bit search for the k-th key, a tie pass and a rank pass, this
+//    took about 2 us off the decode step,
 //    weighted with route_kernel's arithmetic (double exp over the picks,
 //    xor-butterfly sum); meanwhile warps 4..31 take the max |x| of row slices;
 //  * bucket, by counting over the A <= 128 assignments: assignment a's place is
@@ -727,8 +764,7 @@ __global__ void __launch_bounds__(1024)
   __shared__ int s_sorted[kFrontMaxA];
   __shared__ int s_xexp[kFrontMaxT];
   __shared__ float s_xpart[32];
-  __shared__ uint32_t s_key[kFrontMaxT][32];
-  __shared__ int s_e[kFrontMaxT][32], s_oe[kFrontMaxT][32];
+  __shared__ int s_oe[kFrontMaxT][32];
   __shared__ float s_v[kFrontMaxT][32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int A = T * k;
@@ -754,47 +790,44 @@ __global__ void __launch_bounds__(1024)
       }
       if (lane == 0) set_status(status, K3MOE_DEV_NONFINITE);
     } else {
-      // tau = the k-th largest key: the largest value with count(key >= tau) >= k
-      uint32_t tau = 0u;
-      for (int bit = 31; bit >= 0; --bit) {
-        const uint32_t cand = tau | (1u << bit);
-        int c0 = 0, c1 = 0;
+      // the k picks in (key desc, index asc) order, one per round of a warp-wide
+      // arg-max: the largest key by one warp reduction, then the smallest index
+      // holding it by another; the winning lane drops that key and finds its
+      // next best.  A lane's best is its largest key at its smallest i (index
+      // lane + 32 i), and every expert e < E has a key above 0 (k <= E).
+      uint32_t kb = 0u;
+      int ib = kFrontMaxE / 32;
 #pragma unroll
-        for (int i = 0; i < kFrontMaxE / 32; i += 2) {
-          c0 += key[i] >= cand;
-          c1 += key[i + 1] >= cand;
+      for (int i = 0; i < kFrontMaxE / 32; ++i)
+        if (key[i] > kb) {
+          kb = key[i];
+          ib = i;
         }
-        if (static_cast<int>(__reduce_add_sync(0xFFFFFFFFu, static_cast<unsigned>(c0 + c1))) >= k) tau = cand;
-      }
-      int cgt = 0;
+      int pick = 0;
+      for (int j = 0; j < k; ++j) {
+        const uint32_t bk = __reduce_max_sync(0xFFFFFFFFu, kb);
+        const unsigned cand =
+            (kb == bk && ib < kFrontMaxE / 32) ? static_cast<unsigned>(lane + 32 * ib) : 0xFFFFFFFFu;
+        const unsigned be = __reduce_min_sync(0xFFFFFFFFu, cand);
+        if (lane == j) pick = static_cast<int>(be);
+        if (static_cast<int>(be & 31u) == lane) {
+          const int rm = static_cast<int>(be >> 5);
+          kb = 0u;
+          ib = kFrontMaxE / 32;
 #pragma unroll
-      for (int i = 0; i < kFrontMaxE / 32; ++i) cgt += key[i] > tau;
-      const int need = k - static_cast<int>(__reduce_add_sync(0xFFFFFFFFu, static_cast<unsigned>(cgt)));
-      // the picks in index order (i major, lane minor): keys above tau, and the first `need` ties
-      int ties = 0, nsel = 0;
-#pragma unroll
-      for (int i = 0; i < kFrontMaxE / 32; ++i) {
-        const bool tie = key[i] == tau && key[i] != 0u;
-        const unsigned mt = __ballot_sync(0xFFFFFFFFu, tie);
-        const bool sel = key[i] > tau || (tie && ties + __popc(mt & ((1u << lane) - 1u)) < need);
-        ties += __popc(mt);
-        const unsigned ms = __ballot_sync(0xFFFFFFFFu, sel);
-        if (sel) {
-          const int slot = nsel + __popc(ms & ((1u << lane) - 1u));
-          s_key[t][slot] = key[i];
-          s_e[t][slot] = lane + 32 * i;
+          for (int i = 0; i < kFrontMaxE / 32; ++i) {
+            if (i == rm) key[i] = 0u;
+            if (key[i] > kb) {
+              kb = key[i];
+              ib = i;
+            }
+          }
         }
-        nsel += __popc(ms);
       }
-      __syncwarp();
-      // order by (key desc, index asc); weights with route_kernel's arithmetic
+      // weights with route_kernel's arithmetic
       if (lane < k) {
-        const uint32_t mk = s_key[t][lane];
-        const int me = s_e[t][lane];
-        int r = 0;
-        for (int j = 0; j < k; ++j) r += (s_key[t][j] > mk) || (s_key[t][j] == mk && s_e[t][j] < me);
-        s_oe[t][r] = me;
-        s_v[t][r] = __ldg(row + me);
+        s_oe[t][lane] = pick;
+        s_v[t][lane] = __ldg(row + pick);
       }
       __syncwarp();
       const bool active = lane < k;
@@ -916,6 +949,7 @@ int launch_layer_gemv_fast(const k3moe_shape &s, const float *logits, const uint
   P.I = s.I;
   P.k = s.k;
   P.A = s.T * s.k;
+  P.E = s.E;
   P.perm = perm;
   P.slots = b.slots;
   P.meta = b.meta;
@@ -940,6 +974,7 @@ int launch_ffn_gemv(const k3moe_shape &s, const uint16_t *x, const k3moe_weights
   P.I = s.I;
   P.k = s.k;
   P.A = s.T * s.k;
+  P.E = s.E;
   P.perm = perm;
   P.slots = b.slots;
   P.meta = b.meta;
