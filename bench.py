@@ -60,6 +60,9 @@ def parse():
                    help="override T (small cases for profiling; 0 = the workload's own)")
     p.add_argument("--no-graphs", dest="graphs", action="store_false",
                    help="time each step as a k3moe_layer call instead of the replay of its captured CUDA graph")
+    p.add_argument("--calls-per-graph", type=int, default=8,
+                   help="consecutive k3moe_layer calls (one per step, each on its own input set) per captured "
+                        "graph, as a model's layers follow each other; 1 = one graph per step")
     p.add_argument("--legs", default="all", choices=["all", "none"],
                    help="also time the other workloads (batch8, speculative-verify batches, prefill, "
                         "skewed, probe) into the line's workloads object")
@@ -413,14 +416,24 @@ def tensor_figures(s, mode, ffn_s):
             "frac": tf / (bf16 * ratio), "fp4_dense_frac": tf / (bf16 * 6.0)}
 
 
+def launch_note(a, calls_per_graph=None):
+    if not getattr(a, "graphs", False):
+        return "each timed step is one k3moe_layer call"
+    g = calls_per_graph if calls_per_graph is not None else max(1, getattr(a, "calls_per_graph", 1))
+    if g <= 1:
+        return "each timed step replays a CUDA graph holding one captured k3moe_layer call"
+    return (f"each timed step is one k3moe_layer call on its own input set; the calls are replayed from CUDA "
+            f"graphs holding {g} consecutive calls each (their kernels keep programmatic-launch edges, also "
+            f"from one call to the next), timed per graph and divided evenly among its calls")
+
+
 def workload_config(a, s, name=None):
     name = name or a.config
     return {"workload": f"{name}: T={s.T} tokens, H={s.H}, I={s.I}, E={s.E}, top-{s.k}, "
                         f"MXFP4 experts resident",
             "tokens": s.T, "hidden": s.H, "intermediate": s.I, "experts": s.E, "top_k": s.k,
             "l2": f"{getattr(a, 'l2_mode', 'L2 flushed between steps')}; inputs rotate over {a.sets} sets",
-            "launch": ("each timed step replays a CUDA graph holding one captured k3moe_layer call"
-                       if getattr(a, "graphs", False) else "each timed step is one k3moe_layer call"),
+            "launch": launch_note(a, getattr(a, "calls_per_graph_used", None)),
             "parallelism": f"replicas x{a.gpus}"}
 
 
@@ -539,13 +552,29 @@ class LayerBench:
         kernel launches: the host cannot fall behind the GPU."""
         import torch
         k3, s = self.k3, self.s
+
+        def call(j):
+            k3.k3moe_layer(s, self.logits_d[j], self.x_d[j], self.W, self.idx, self.w, self.cnt, self.offsets,
+                           self.perm, self.inv, self.Y, self.out, None, self.mode, self.wsl, self.st)
+
         self.graphs = []
         for j in range(self.nsets):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                k3.k3moe_layer(s, self.logits_d[j], self.x_d[j], self.W, self.idx, self.w, self.cnt, self.offsets,
-                               self.perm, self.inv, self.Y, self.out, None, self.mode, self.wsl, self.st)
+                call(j)
             self.graphs.append(g)
+        # graphs of G consecutive calls (sets b G .. b G + G - 1), when the sets divide into them and no L2
+        # flush has to run between steps
+        G = max(1, getattr(self.a, "calls_per_graph", 1))
+        self.G = G if G > 1 and self.nsets % G == 0 and not self.do_flush else 1
+        self.ggraphs = []
+        if self.G > 1:
+            for b in range(self.nsets // self.G):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    for j in range(b * self.G, (b + 1) * self.G):
+                        call(j)
+                self.ggraphs.append(g)
         torch.cuda.synchronize()
 
     def run(self, steps, warmup, clocks=None, barrier=None):
@@ -561,10 +590,13 @@ class LayerBench:
         if int(self.st.item()) != 0:
             raise RuntimeError(f"{self.name}: device status {int(self.st.item())} during warm-up")
         self.graphs = None
+        self.G = 1
         if getattr(self.a, "graphs", False):
             self.capture()
             for i in range(warmup):
                 self.graphs[i % self.nsets].replay()
+            for g in self.ggraphs:
+                g.replay()
             torch.cuda.synchronize()
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
         pevs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
@@ -573,16 +605,25 @@ class LayerBench:
         torch.cuda.synchronize()
         t0 = time.time()
         t_wall = time.perf_counter()
-        for i in range(steps):
+        spans = []  # (first step, steps) per timed launch
+        i = 0
+        while i < steps:
             if self.do_flush:
                 self.flush.fill_((i + 1) & 0xFF)
+            j = (warmup + i) % self.nsets
+            n = self.G if (self.graphs is not None and self.G > 1 and j % self.G == 0 and i + self.G <= steps) else 1
             if self.graphs is not None:
                 ev = evs[i]
                 ev[0].record(self.stream)
-                self.graphs[(warmup + i) % self.nsets].replay()
+                if n > 1:
+                    self.ggraphs[j // self.G].replay()
+                else:
+                    self.graphs[j].replay()
                 ev[3].record(self.stream)
             else:
                 self.layer(warmup + i, evs[i])
+            spans.append((i, n))
+            i += n
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
         for i in range(steps):
@@ -595,7 +636,10 @@ class LayerBench:
             barrier()
         if int(self.st.item()) != 0:
             raise RuntimeError(f"{self.name}: device status {int(self.st.item())} in the timed steps")
-        self.step_ms = np.array([e[0].elapsed_time(e[3]) for e in evs])
+        self.step_ms = np.zeros(steps)
+        for i0, n in spans:
+            self.step_ms[i0:i0 + n] = evs[i0][0].elapsed_time(evs[i0][3]) / n
+        self.calls_per_graph = self.G
         self.rb_ms = np.array([e[0].elapsed_time(e[1]) for e in pevs])
         self.ffn_ms = np.array([e[1].elapsed_time(e[2]) for e in pevs])
         self.comb_ms = np.array([e[2].elapsed_time(e[3]) for e in pevs])
@@ -816,6 +860,7 @@ def run_gpu(a):
     clocks.start()
     time.sleep(0.3)
     lb.run(a.steps, a.warmup, barrier=barrier)
+    a.calls_per_graph_used = getattr(lb, "calls_per_graph", 1)
     clocks.t0, clocks.t1 = lb.t0, lb.t1
     tot_ms = slowest_rank_ms(float(lb.step_ms.sum()), ws, dev)
     value = whole_job_rate(s.T * a.steps, tot_ms, ws)

@@ -120,6 +120,13 @@ __device__ __forceinline__ bool expert_present(const k3moe_weights &w, int e) {
   const uint8_t *a = w.w13_codes[e], *b = w.w13_scales[e], *c = w.w2_codes[e], *d = w.w2_scales[e];
   return a && b && c && d && ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(c)) & 15u) == 0;
 }
+// Of an expert's four pointers (w13 codes and scales, w2 codes and scales):
+// 1 present (as expert_present); 2 all given but the codes misaligned (absent,
+// and reported); 0 absent.
+__device__ __forceinline__ int expert_flags(const uint8_t *a, const uint8_t *b, const uint8_t *c, const uint8_t *d) {
+  if (!(a && b && c && d)) return 0;
+  return ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(c)) & 15u) == 0 ? 1 : 2;
+}
 
 // ----------------------------------------------------------------------------
 // prep.  Block 0: slots of the active experts in expert order, from a
@@ -729,9 +736,11 @@ int sm_count() {
 //  * route: warp t takes token t with warp-level operations only: lane l holds
 //    the order-preserving keys of experts l, l + 32, ...; k rounds of a warp
 //    arg-max (two warp reductions each: the largest key, then the smallest
-//    index holding it) give the picks in (key desc, index asc) order; in place
-//    of a 32-step bit search for the k-th key, a tie pass and a rank pass, this
-//    took about 2 us off the decode step,
+//    index holding it) give the picks in (key desc, index asc) order (in place
+//    of a 32-step bit search for the k-th key, a tie pass and a rank pass), and
+//    the picked experts' four weight pointers are loaded right away and used
+//    after the softmax (in the bucketing phase they cost the decode step about
+//    4 us: the pointer arrays are cold after each step's weight stream),
 //    weighted with route_kernel's arithmetic (double exp over the picks,
 //    xor-butterfly sum); meanwhile warps 4..31 take the max |x| of row slices;
 //  * bucket, by counting over the A <= 128 assignments: assignment a's place is
@@ -762,6 +771,7 @@ __global__ void __launch_bounds__(1024)
   pdl_trigger();
   __shared__ int s_idx[kFrontMaxA];
   __shared__ int s_sorted[kFrontMaxA];
+  __shared__ int s_pres[kFrontMaxA], s_pres_sorted[kFrontMaxA];  // expert_flags per assignment / bucket position
   __shared__ int s_xexp[kFrontMaxT];
   __shared__ float s_xpart[32];
   __shared__ int s_oe[kFrontMaxT][32];
@@ -787,6 +797,7 @@ __global__ void __launch_bounds__(1024)
         idx[t * k + lane] = lane;
         wts[t * k + lane] = 1.0f / static_cast<float>(k);
         s_idx[t * k + lane] = lane;
+        s_pres[t * k + lane] = expert_flags(w.w13_codes[lane], w.w13_scales[lane], w.w2_codes[lane], w.w2_scales[lane]);
       }
       if (lane == 0) set_status(status, K3MOE_DEV_NONFINITE);
     } else {
@@ -794,7 +805,8 @@ __global__ void __launch_bounds__(1024)
       // arg-max: the largest key by one warp reduction, then the smallest index
       // holding it by another; the winning lane drops that key and finds its
       // next best.  A lane's best is its largest key at its smallest i (index
-      // lane + 32 i), and every expert e < E has a key above 0 (k <= E).
+      // lane + 32 i), and every expert e < E has a key above 0 (k <= E).  (Caching
+      // each lane's best two measured no faster than this rescan.)
       uint32_t kb = 0u;
       int ib = kFrontMaxE / 32;
 #pragma unroll
@@ -824,6 +836,15 @@ __global__ void __launch_bounds__(1024)
           }
         }
       }
+      // the picked experts' weight pointers are loaded now and used after the
+      // weights, so that their latency overlaps the softmax
+      const uint8_t *pa = nullptr, *pb = nullptr, *pc = nullptr, *pd = nullptr;
+      if (lane < k) {
+        pa = w.w13_codes[pick];
+        pb = w.w13_scales[pick];
+        pc = w.w2_codes[pick];
+        pd = w.w2_scales[pick];
+      }
       // weights with route_kernel's arithmetic
       if (lane < k) {
         s_oe[t][lane] = pick;
@@ -850,6 +871,7 @@ __global__ void __launch_bounds__(1024)
         idx[t * k + lane] = s_oe[t][lane];
         wts[t * k + lane] = wj;
         s_idx[t * k + lane] = s_oe[t][lane];
+        s_pres[t * k + lane] = expert_flags(pa, pb, pc, pd);
       }
     }
   } else if (warp >= kFrontMaxT) {
@@ -882,6 +904,7 @@ __global__ void __launch_bounds__(1024)
     perm[p] = tid;
     inv[tid] = p;
     s_sorted[p] = e;
+    s_pres_sorted[p] = s_pres[tid];
   }
   if (tid < T) {
     const int wpt = (32 - kFrontMaxT) / T;
@@ -915,9 +938,9 @@ __global__ void __launch_bounds__(1024)
     int slot = 0, end = tid + 1;
     for (int p = 1; p <= tid; ++p) slot += s_sorted[p] != s_sorted[p - 1];
     while (end < A && s_sorted[end] == e) ++end;
-    const bool pr = expert_present(w, e);
-    if (!pr && w.w13_codes[e] && w.w13_scales[e] && w.w2_codes[e] && w.w2_scales[e])
-      set_status(status, K3MOE_DEV_BOUNDS);  // non-NULL but misaligned: treated as absent
+    const int fl = s_pres_sorted[tid];
+    const bool pr = (fl & 1) != 0;
+    if (fl == 2) set_status(status, K3MOE_DEV_BOUNDS);  // non-NULL but misaligned: treated as absent
     slots[slot] = make_int4(e, tid, end - tid, pr ? 1 : 0);
   }
   if (tid == 0) {
