@@ -754,13 +754,26 @@ __device__ __forceinline__ uint32_t idesc_mxf4(int M, int N, int sf_id) {
          (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) | (static_cast<uint32_t>(sf_id) << 29);
 }
 
-__device__ __forceinline__ void tc_mma_mxf4(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                            uint32_t tmem_sfa, uint32_t tmem_sfb, uint32_t accumulate) {
+// The four MMAs of one stage (K = 64 each, 256 K values): operand descriptors a
+// and b advance 32 bytes (2 in the address field) per MMA; MMAs 0 and 2 take the
+// scale-factor id 0 (idesc0), 1 and 3 id 2 (idesc2); MMAs 0 and 1 read the scale
+// words at sfa / sfb, 2 and 3 the next word (+4 columns).  The first accumulates
+// when `acc` is nonzero.  One asm block keeps the issuing thread to a few
+// instructions per MMA.
+__device__ __forceinline__ void tc_mma4_mxf4(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc0,
+                                             uint32_t idesc2, uint32_t sfa, uint32_t sfb, uint32_t acc) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+      "{\n\t.reg .pred p, q;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t.reg .b32 sa1, sb1;\n\t"
+      "setp.ne.b32 p, %7, 0;\n\tsetp.eq.b32 q, %3, %3;\n\t"
+      "add.u64 a1, %1, 2;\n\tadd.u64 a2, %1, 4;\n\tadd.u64 a3, %1, 6;\n\t"
+      "add.u64 b1, %2, 2;\n\tadd.u64 b2, %2, 4;\n\tadd.u64 b3, %2, 6;\n\t"
+      "add.u32 sa1, %5, 4;\n\tadd.u32 sb1, %6, 4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], a1, b1, %4, [%5], [%6], q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], a2, b2, %3, [sa1], [sb1], q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], a3, b3, %4, [sa1], [sb1], q;\n\t}" ::"r"(
           tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(tmem_sfa), "r"(tmem_sfb), "r"(accumulate)
+      "l"(a), "l"(b), "r"(idesc0), "r"(idesc2), "r"(sfa), "r"(sfb), "r"(acc)
       : "memory");
 }
 
@@ -833,7 +846,7 @@ struct Mx4Params {
 };
 
 __global__ void __launch_bounds__(kMxThreads, 2)
-    ffn_gemm_mxf4_kernel(const __grid_constant__ CUtensorMap amap, Mx4Params P) {
+    ffn_gemm_mxf4_kernel(const __grid_constant__ RowMaps amaps, Mx4Params P) {
   extern __shared__ __align__(1024) uint8_t msm_raw[];
   uint8_t *msm = msm_raw + ((1024u - (su32(msm_raw) & 1023u)) & 1023u);
   __shared__ uint64_t full[kMxStages], empty[kMxStages], sf_full[2], sf_empty[2], acc_bar;
@@ -976,7 +989,7 @@ __global__ void __launch_bounds__(kMxThreads, 2)
           break;
         }
         uint8_t *st = msm + s * kMxStageB;
-        mb_arrive_tx(&full[s], static_cast<uint32_t>((present ? 2 : 1) * kMxAtomB));
+        mb_arrive_tx(&full[s], static_cast<uint32_t>((present ? kMxAtomB : 0) + Npad * 128));
         if (present) {  // weight codes: K offset in bytes (128 per stage), two boxes of 64 rows
           tma_load_2d(st, wmap, a * 128, y0, &full[s]);
           tma_load_2d(st + kMxAtomB / 2, wmap, a * 128, y1, &full[s]);
@@ -985,7 +998,7 @@ __global__ void __launch_bounds__(kMxThreads, 2)
             tma_prefetch_2d(wmap, (a + kMxAhead) * 128, y1);
           }
         }
-        tma_load_2d(st + kMxAtomB, &amap, a * 128, g.p0, &full[s]);
+        tma_load_2d(st + kMxAtomB, &amaps.m[Npad / 16 - 1], a * 128, g.p0, &full[s]);
       }
     }
   } else {
@@ -1005,16 +1018,12 @@ __global__ void __launch_bounds__(kMxThreads, 2)
         tc_fence_after();
         const uint32_t wa = su32(msm + s * kMxStageB);
         const uint32_t sf = tmem + kMxColSf + slot * kMxSfChunkCols;
-#pragma unroll
-        for (int j = 0; j < kMxSteps; ++j) {
-          // both operands advance 32 bytes (64 values) per step; the step's two
-          // 32-value blocks are blocks 8 t + 2 j, 8 t + 2 j + 1 of the chunk:
-          // scale word 2 t + j / 2, byte pair 2 (j % 2)
-          const uint32_t word = static_cast<uint32_t>(2 * t + (j >> 1));
-          tc_mma_mxf4(tmem, smem_desc_sw128(wa + 32 * j), smem_desc_sw128(wa + kMxAtomB + 32 * j),
-                      idesc_mxf4(kTileM, Npad, 2 * (j & 1)), sf + 4 * word, sf + 16 + 4 * word,
-                      (a > 0 || j > 0) ? 1u : 0u);
-        }
+        // both operands advance 32 bytes (64 values) per MMA; MMA j's two 32-value
+        // blocks are blocks 8 t + 2 j, 8 t + 2 j + 1 of the chunk: scale word
+        // 2 t + j / 2, byte pair 2 (j % 2)
+        static_assert(kMxSteps == 4, "one stage = four MMAs of K = 64");
+        tc_mma4_mxf4(tmem, smem_desc_sw128(wa), smem_desc_sw128(wa + kMxAtomB), idesc_mxf4(kTileM, Npad, 0),
+                     idesc_mxf4(kTileM, Npad, 2), sf + 8 * t, sf + 16 + 8 * t, a > 0 ? 1u : 0u);
         tc_commit(&empty[s]);
         if (t == kMxCh - 1 || a == nst - 1) tc_commit(&sf_empty[slot]);
       }
@@ -1161,55 +1170,18 @@ bool make_code_map(CUtensorMap *m, void *base, int rows, int kbytes) {
 
 // 2-D map over activation bytes (rows x row_bytes): box = 128 bytes x 128 rows,
 // 128B swizzle; rows past the end read as zero.
-bool make_byte_map(CUtensorMap *m, void *base, int rows, int row_bytes) {
+bool make_byte_map(CUtensorMap *m, void *base, int rows, int row_bytes, int box_rows = kTileN) {
   EncodeTiledFn fn = encode_tiled();
   if (!fn) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
-  const cuuint32_t box[2] = {128, kTileN};
+  const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The W4A4 GEMM (both projections): MXFP4 activations of x -> gate/up -> MXFP4
-// activations of h -> down.
-int launch_gemm_mxf4(const k3moe_shape &s, const uint16_t *x, const int32_t *perm, int A, long long ntile_max,
-                     int mt_gu, int mt_dn, Mx4Params P, const int4 *tab_dn, uint8_t *xq, uint8_t *xsc, uint8_t *hq,
-                     uint8_t *hsc, int32_t *status, cudaStream_t st) {
-  CUtensorMap xmap, hmap;
-  if (!make_byte_map(&xmap, xq, A, s.H / 2) || !make_byte_map(&hmap, hq, A, s.I / 2)) return -1;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(ffn_gemm_mxf4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxDynSmem) !=
-        cudaSuccess)
-      return -1;
-    attr = true;
-  }
-  if (launch_pdl(gemm_rows_to_mxfp4_kernel, dim3(A), dim3(256), 0, st, x, perm, s.k, A, s.H, xq, xsc, status) !=
-      cudaSuccess)
-    return -1;
-  P.kind = 0;
-  P.ascale = xsc;
-  if (launch_pdl(ffn_gemm_mxf4_kernel, dim3(static_cast<unsigned>(ntile_max * mt_gu)), dim3(kMxThreads), kMxDynSmem,
-                 st, xmap, P) != cudaSuccess)
-    return -1;
-  if (launch_pdl(gemm_rows_to_mxfp4_kernel, dim3(A), dim3(256), 0, st, static_cast<const uint16_t *>(P.hrow),
-                 static_cast<const int32_t *>(nullptr), 1, A, s.I, hq, hsc, status) != cudaSuccess)
-    return -1;
-  P.kind = 1;
-  P.tab = tab_dn;
-  P.ascale = hsc;
-  if (launch_pdl(ffn_gemm_mxf4_kernel, dim3(static_cast<unsigned>(ntile_max * mt_dn)), dim3(kMxThreads), kMxDynSmem,
-                 st, hmap, P) != cudaSuccess)
-    return -1;
-  return 0;
-}
-
-}  // namespace
-
-namespace {
 // 2-D map over rows x K of 16-bit values: box = 64 (K) x box_rows, 128B swizzle,
 // rows past the end read as zero.
 bool make_row_map_box(CUtensorMap *m, void *base, int rows, int K, int box_rows) {
@@ -1224,20 +1196,24 @@ bool make_row_map_box(CUtensorMap *m, void *base, int rows, int K, int box_rows)
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The maps of every box height over one buffer; the last encoding per buffer
-// role (x or h) is kept per thread, since the workspace is normally reused.
+// The maps of every box height over one buffer: 16-bit rows of K values (roles 0
+// and 1: x and h for the W4A16 GEMM) or rows of K bytes of MXFP4 codes (roles 2
+// and 3: x and h for the W4A4 GEMM).  The last encoding per role is kept per
+// thread, since the workspace is normally reused.
 bool make_row_maps(RowMaps *out, int role, void *base, int rows, int K) {
   struct Entry {
     void *base = nullptr;
     int rows = -1, K = -1;
     RowMaps maps;
   };
-  thread_local Entry cache[2];
+  thread_local Entry cache[4];
   Entry &c = cache[role];
   if (c.base != base || c.rows != rows || c.K != K) {
     c.base = nullptr;
     for (int i = 0; i < kTileN / 16; ++i)
-      if (!make_row_map_box(&c.maps.m[i], base, rows, K, 16 * (i + 1))) return false;
+      if (!(role < 2 ? make_row_map_box(&c.maps.m[i], base, rows, K, 16 * (i + 1))
+                     : make_byte_map(&c.maps.m[i], base, rows, K, 16 * (i + 1))))
+        return false;
     c.base = base;
     c.rows = rows;
     c.K = K;
@@ -1245,7 +1221,43 @@ bool make_row_maps(RowMaps *out, int role, void *base, int rows, int K) {
   *out = c.maps;
   return true;
 }
+
+// The W4A4 GEMM (both projections): MXFP4 activations of x -> gate/up -> MXFP4
+// activations of h -> down.
+int launch_gemm_mxf4(const k3moe_shape &s, const uint16_t *x, const int32_t *perm, int A, long long ntile_max,
+                     int mt_gu, int mt_dn, Mx4Params P, const int4 *tab_dn, uint8_t *xq, uint8_t *xsc, uint8_t *hq,
+                     uint8_t *hsc, int32_t *status, cudaStream_t st) {
+  RowMaps xmaps, hmaps;
+  if (!make_row_maps(&xmaps, 2, xq, A, s.H / 2) || !make_row_maps(&hmaps, 3, hq, A, s.I / 2)) return -1;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(ffn_gemm_mxf4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxDynSmem) !=
+        cudaSuccess)
+      return -1;
+    attr = true;
+  }
+  if (launch_pdl(gemm_rows_to_mxfp4_kernel, dim3(A), dim3(256), 0, st, x, perm, s.k, A, s.H, xq, xsc, status) !=
+      cudaSuccess)
+    return -1;
+  P.kind = 0;
+  P.ascale = xsc;
+  if (launch_pdl(ffn_gemm_mxf4_kernel, dim3(static_cast<unsigned>(ntile_max * mt_gu)), dim3(kMxThreads), kMxDynSmem,
+                 st, xmaps, P) != cudaSuccess)
+    return -1;
+  if (launch_pdl(gemm_rows_to_mxfp4_kernel, dim3(A), dim3(256), 0, st, static_cast<const uint16_t *>(P.hrow),
+                 static_cast<const int32_t *>(nullptr), 1, A, s.I, hq, hsc, status) != cudaSuccess)
+    return -1;
+  P.kind = 1;
+  P.tab = tab_dn;
+  P.ascale = hsc;
+  if (launch_pdl(ffn_gemm_mxf4_kernel, dim3(static_cast<unsigned>(ntile_max * mt_dn)), dim3(kMxThreads), kMxDynSmem,
+                 st, hmaps, P) != cudaSuccess)
+    return -1;
+  return 0;
+}
+
 }  // namespace
+
 
 // 2-D map over rows x K of 16-bit values: box = 64 (K) x 128 rows, 128B swizzle,
 // rows past the end read as zero.
