@@ -320,6 +320,16 @@ int k3moe_layer(k3moe_shape s, const float *logits, const uint16_t *x, const k3m
 int k3moe_combine_residual(k3moe_shape s, const float *Y, const float *w, const int32_t *inv, const uint16_t *residual,
                            uint16_t *out, float *out_f32, k3moe_stream_t stream);
 
+/* Self-test of the bounded waits (a test hook, not part of the path): one
+ * thread waits, with the iteration bound every mbarrier wait in the tensor-core
+ * kernels uses, on a phase that nothing completes, so the wait runs out: the
+ * kernel ORs K3MOE_DEV_TIMEOUT into *dev_status and writes the wait's duration
+ * in nanoseconds to *dev_elapsed_ns (both device pointers), then returns; the
+ * context stays usable.  No copy or tensor-core operation is in flight in the
+ * waiting CTA.  Errors: NULL pointer -> K3MOE_ERR_ARG; not sm_103 ->
+ * K3MOE_ERR_ARCH; launch failure -> K3MOE_ERR_LAUNCH. */
+int k3moe_selftest_bounded_wait(int32_t *dev_status, unsigned long long *dev_elapsed_ns, k3moe_stream_t stream);
+
 /* Human-readable name of a k3moe_status value. */
 const char *k3moe_status_string(int code);
 

@@ -99,6 +99,8 @@ def lib():
             L.k3moe_layer.restype = i32
             L.k3moe_layer.argtypes = [Shape, vp, vp, ctypes.POINTER(_WeightsC), vp, vp, vp, vp, vp, vp, vp, vp, vp, i32,
                                       vp, sz, vp, vp]
+            L.k3moe_selftest_bounded_wait.restype = i32
+            L.k3moe_selftest_bounded_wait.argtypes = [vp, vp, vp]
             L.k3moe_status_string.restype = ctypes.c_char_p
             L.k3moe_status_string.argtypes = [i32]
             L.k3moe_last_cuda_error.restype = ctypes.c_char_p
@@ -275,6 +277,14 @@ def k3moe_quantize_mxfp4(x, codes, scales, stream=None):
     rc = lib().k3moe_quantize_mxfp4(n, _ptr(x, _BF16, "x"), _ptr(codes, torch.uint8, "codes"),
                                     _ptr(scales, torch.uint8, "scales"), _stream(stream))
     _check("k3moe_quantize_mxfp4", rc)
+
+
+def k3moe_selftest_bounded_wait(dev_status, dev_elapsed_ns, stream=None):
+    """A bounded mbarrier wait that nothing completes: ORs K3MOE_DEV_TIMEOUT into
+    dev_status (int32) and writes the wait's duration in ns to dev_elapsed_ns (int64)."""
+    _check("k3moe_selftest_bounded_wait",
+           lib().k3moe_selftest_bounded_wait(_ptr(dev_status, torch.int32, "dev_status"),
+                                             _ptr(dev_elapsed_ns, torch.int64, "dev_elapsed_ns"), _stream(stream)))
 
 
 def k3moe_combine(shape, Y, w, inv, out, out_f32=None, stream=None):

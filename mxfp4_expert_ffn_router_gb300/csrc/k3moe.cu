@@ -6,7 +6,9 @@
 #include <mutex>
 
 #include "../../include/k3moe.h"
+#include "k3moe_dev.cuh"
 #include "k3moe_launch.h"
+#include "tc_sm103.cuh"
 
 namespace {
 
@@ -293,6 +295,40 @@ int k3moe_combine_residual(k3moe_shape s, const float *Y, const float *w, const 
 }
 
 const char *k3moe_last_cuda_error(void) { return t_last_cuda_error; }
+
+}  // extern "C"
+
+namespace {
+// One thread waits, with the bound every tensor-core kernel's waits use, on an
+// mbarrier phase that nothing completes (no copy or MMA is in flight into the
+// CTA), then reports K3MOE_DEV_TIMEOUT and how long the wait took.
+__global__ void selftest_bounded_wait_kernel(int32_t *status, unsigned long long *elapsed_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    k3moe::mb_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long t0, t1;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    const bool done = k3moe::mb_wait(&bar, 0);
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
+    if (!done) k3moe::set_status(status, K3MOE_DEV_TIMEOUT);
+    *elapsed_ns = t1 - t0;
+  }
+}
+}  // namespace
+
+extern "C" {
+
+int k3moe_selftest_bounded_wait(int32_t *dev_status, unsigned long long *dev_elapsed_ns, k3moe_stream_t stream) {
+  if (!dev_status || !dev_elapsed_ns) return K3MOE_ERR_ARG;
+  const int rc = abi_check_arch();
+  if (rc) return rc;
+  selftest_bounded_wait_kernel<<<1, 32, 0, reinterpret_cast<k3moe_stream>(stream)>>>(dev_status, dev_elapsed_ns);
+  return abi_launched(0);
+}
 
 const char *k3moe_status_string(int code) {
   switch (code) {

@@ -7,8 +7,12 @@
 
 namespace k3moe {
 
-// Iterations of a bounded mbarrier wait before it gives up (a few hundred ms).
-constexpr long long kSpinTc = 1LL << 22;
+// Iterations of a bounded mbarrier wait before it gives up: about a second on a
+// GB300 (an iteration, a try_wait and a short sleep, measured at about 3.8 us by
+// k3moe_selftest_bounded_wait), where every wait of these kernels normally ends
+// within microseconds.  A count of iterations rather than a clock, so that a CTA
+// that is not scheduled for a while does not run it down.
+constexpr long long kSpinTc = 1LL << 18;
 
 __device__ __forceinline__ uint32_t su32(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
