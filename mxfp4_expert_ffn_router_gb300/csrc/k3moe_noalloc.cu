@@ -72,7 +72,7 @@ extern "C" int k3moe_expert_ffn_noalloc(k3moe_shape s, const uint16_t *x, const 
   void *ws = nullptr;
   if ((rc = scratch_for_current_device(&ws))) return rc;
   // Nothing in the scratch has to start at zero: the first kernel of each call
-  // (the prep kernel) writes every counter, table and maximum the call reads.
+  // (the prep kernel) writes every count and table the call reads.
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   return k3moe::abi_launched(k3moe::launch_ffn_gemv(s, x, *w, offsets, perm, Y, ws, dev_status, st));
 }
