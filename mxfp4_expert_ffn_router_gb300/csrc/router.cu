@@ -14,12 +14,15 @@
 //    reduces with an xor butterfly (every lane ends with the same bits).  The
 //    longest chain of roundings is ceil(H / 256) - 1 + 3 + 5.
 //  * router_gemm_kernel (token chunks): tcgen05.mma kind::f16 with both bf16
-//    operands in shared memory, M = 128 experts, N = 128 tokens, K = 16 per
-//    MMA; TMA loads 128-row x 64-value boxes of wr and x (128-byte swizzle) into
-//    a 4-stage ring; the accumulator lives in tensor memory and the epilogue
-//    warps write it to logits with one coalesced 128-byte store per token and
-//    warp.  Warps 0-3 epilogue (tensor-memory lane quadrant = warp), warp 4 TMA,
-//    warp 5 tensor-memory owner and MMA issuer.
+//    operands in shared memory, M = 128 experts, N = 256 tokens, K = 16 per
+//    MMA (four per asm block); TMA loads a 128-row x 64-value box of wr and two
+//    of x (128-byte swizzle) per stage into a 4-stage ring; the accumulator lives
+//    in tensor memory and the epilogue warps write it to logits with one
+//    coalesced 128-byte store per token and warp.  Warps 0-3 epilogue
+//    (tensor-memory lane quadrant = warp), warp 4 TMA, warp 5 tensor-memory owner
+//    and MMA issuer.  256 tokens per tile rather than 128 let each wr box serve
+//    twice the tokens: the fills from L2 to shared memory, not the tensor core,
+//    bound a tile.
 #include <cuda.h>
 
 #include "k3moe_dev.cuh"
@@ -101,15 +104,15 @@ __global__ void __launch_bounds__(kRgWarps * 32)
 namespace {
 
 constexpr int kRmM = 128;   // experts per tile (MMA M, tensor-memory lanes)
-constexpr int kRmN = 128;   // tokens per tile (MMA N, accumulator columns)
+constexpr int kRmN = 256;   // tokens per tile (MMA N, accumulator columns)
 constexpr int kRmK = 64;    // K per stage: one 128-byte swizzle atom of bf16
 constexpr int kRmStages = 4;
-constexpr int kRmTileB = 128 * kRmK * 2;    // 16 KiB: one operand box
-constexpr int kRmStageB = 2 * kRmTileB;     // wr box + x box
+constexpr int kRmTileB = 128 * kRmK * 2;    // 16 KiB: one 128-row operand box
+constexpr int kRmStageB = 3 * kRmTileB;     // wr box + two x boxes (256 token rows, contiguous)
 constexpr int kRmSmem = 1024 + kRmStages * kRmStageB;
 constexpr int kRmThreads = 6 * 32;
 constexpr int kRmTmaWarp = 4, kRmMmaWarp = 5;
-constexpr int kRmTmemCols = 128;
+constexpr int kRmTmemCols = kRmN;
 
 // Instruction descriptor, kind::f16 with bf16 A and B, fp32 D, both K-major.
 __device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
@@ -120,12 +123,20 @@ __device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
          | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16
 }
 
-__device__ __forceinline__ void tc_mma_bf16_ss(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                               uint32_t accumulate) {
+// The four MMAs of a stage (K = 16 each): both descriptors advance 32 bytes (2 in
+// the address field) per MMA; the first accumulates when `acc` is nonzero.
+__device__ __forceinline__ void tc_mma4_bf16_ss(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                                uint32_t acc) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred p, q;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 q, %3, %3;\n\t"
+      "add.u64 a1, %1, 2;\n\tadd.u64 a2, %1, 4;\n\tadd.u64 a3, %1, 6;\n\t"
+      "add.u64 b1, %2, 2;\n\tadd.u64 b2, %2, 4;\n\tadd.u64 b3, %2, 6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, q;\n\t}" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
 
@@ -177,6 +188,7 @@ __global__ void __launch_bounds__(kRmThreads, 1)
         mb_arrive_tx(&full_bar[s], kRmStageB);
         tma_load_2d(a, &amap, ks * kRmK, e0, &full_bar[s]);
         tma_load_2d(a + kRmTileB, &bmap, ks * kRmK, t0, &full_bar[s]);
+        tma_load_2d(a + 2 * kRmTileB, &bmap, ks * kRmK, t0 + 128, &full_bar[s]);
         issued = ks + 1;
       }
       // drain: every issued copy has landed before this CTA can leave
@@ -195,10 +207,10 @@ __global__ void __launch_bounds__(kRmThreads, 1)
         }
         tc_fence_after();
         const uint32_t a0 = su32(rsm + s * kRmStageB), b0 = a0 + kRmTileB;
-#pragma unroll
-        for (int kk = 0; kk < kRmK / 16; ++kk)  // K = 16 per MMA: +32 bytes inside the swizzle atom
-          tc_mma_bf16_ss(tmem, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32), idesc,
-                         (ks > 0 || kk > 0) ? 1u : 0u);
+        // K = 16 per MMA: +32 bytes inside the swizzle atom; the 256 token rows of B
+        // are the two x boxes, contiguous (8-row atoms of 1024 bytes throughout)
+        static_assert(kRmK == 64, "one stage = four MMAs");
+        tc_mma4_bf16_ss(tmem, smem_desc_sw128(a0), smem_desc_sw128(b0), idesc, ks > 0 ? 1u : 0u);
         tc_commit(&empty_bar[s]);
         done = ks + 1;
       }
