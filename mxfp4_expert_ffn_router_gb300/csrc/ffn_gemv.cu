@@ -249,7 +249,54 @@ struct RowsParams {
   uint16_t *hrow;        // gate/up output, bf16 [A][I]
   float *Y;              // down output, [A][H]
   int32_t *status;
+  // gate/up of the decode layer only (NULL otherwise): the routing weights of the
+  // rw_T tokens, computed by the grid's last rw_T warps once their items are done
+  const float *rw_logits;  // [rw_T][E]
+  const int32_t *rw_idx;   // [rw_T][k], the picks of the layer's front
+  float *rw_w;             // [rw_T][k]
+  int rw_T;
 };
+
+// Routing weights of token t = (warps in the grid - 1 - this warp), the same
+// arithmetic as route_kernel (exp in double of each pick's logit minus the
+// largest, xor-butterfly sum, one division, then float; a largest logit of +inf
+// splits the weight among the +inf picks, one of -inf gives 1/k), or 1/k for a
+// row holding a NaN, whose picks are experts 0..k-1.  Only the combine reads
+// them, so they need not hold up the front of the layer.  The warp is converged.
+__device__ __forceinline__ void route_weights_tail(const RowsParams &P) {
+  const long long gw = static_cast<long long>(blockIdx.x) * kGvWarps + (threadIdx.x >> 5);
+  const long long t = static_cast<long long>(gridDim.x) * kGvWarps - 1 - gw;
+  if (t >= P.rw_T) return;
+  const int lane = threadIdx.x & 31, k = P.k, E = P.E;
+  const float *row = P.rw_logits + t * E;
+  bool nan_here = false;
+  for (int e = lane; e < E; e += 32) {
+    const float v = __ldg(row + e);
+    nan_here |= v != v;
+  }
+  const bool active = lane < k;
+  float wj;
+  if (__any_sync(0xFFFFFFFFu, nan_here)) {
+    wj = 1.0f / static_cast<float>(k);
+  } else {
+    const int pick = active ? min(max(P.rw_idx[t * k + lane], 0), E - 1) : 0;
+    const float myv = active ? __ldg(row + pick) : 0.f;
+    const float mx = __shfl_sync(0xFFFFFFFFu, myv, 0);  // the first pick holds the largest logit
+    if (mx == -INFINITY) {
+      wj = 1.0f / static_cast<float>(k);
+    } else if (mx == INFINITY) {
+      const int ninf = __popc(__ballot_sync(0xFFFFFFFFu, active && myv == INFINITY));
+      wj = (myv == INFINITY) ? 1.0f / static_cast<float>(ninf) : 0.0f;
+    } else {
+      const double ex = active ? exp(static_cast<double>(myv) - static_cast<double>(mx)) : 0.0;
+      double sum = ex;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
+      wj = static_cast<float>(ex / sum);
+    }
+  }
+  if (active) P.rw_w[t * k + lane] = wj;
+}
 
 __device__ __forceinline__ const uint8_t *ldg_ptr(const uint8_t *const *arr, int e) {
   return reinterpret_cast<const uint8_t *>(__ldg(reinterpret_cast<const unsigned long long *>(arr) + e));
@@ -408,6 +455,7 @@ __global__ void __launch_bounds__(kGvWarps * 32, 2) gemv_rows_kernel(RowsParams 
       }
     }
   }
+  if (KIND == 0 && P.rw_logits) route_weights_tail(P);
 }
 
 // ----------------------------------------------------------------------------
@@ -531,18 +579,13 @@ __device__ __forceinline__ void prefetch_first_items(const RowsParams &P, int pe
   }
 }
 
+// The warp's items item, item + stride, ... below nitems.
 template <int KIND, int R, int NJ>
-__global__ void __launch_bounds__(kGvWarps * 32, 2) gemv_rows_pipe_kernel(RowsParams P) {
+__device__ __forceinline__ void rows_pipe_items(const RowsParams &P, long long item, long long stride, int per_slot,
+                                                long long nitems) {
   constexpr int HA = (NJ + 1) / 2, HB = NJ - HA;
   constexpr int NCH = 32 * NJ;  // chunks per row
   const int lane = threadIdx.x & 31;
-  const int per_slot = KIND == 0 ? P.I : (P.H + R - 1) / R;
-  const long long stride = static_cast<long long>(gridDim.x) * kGvWarps;
-  long long item = static_cast<long long>(blockIdx.x) * kGvWarps + (threadIdx.x >> 5);
-  if (KIND == 1) prefetch_first_items<R, NJ>(P, per_slot, item, stride);
-  pdl_wait();
-  pdl_trigger();
-  const long long nitems = static_cast<long long>(P.meta[0]) * per_slot;
   if (item >= nitems) return;
   ItemRows<R> cur;
   item_rows_at<KIND, R, NJ>(P, item, per_slot, cur);
@@ -607,6 +650,18 @@ __global__ void __launch_bounds__(kGvWarps * 32, 2) gemv_rows_pipe_kernel(RowsPa
     item = nitem;
     cur = nxt;
   }
+}
+
+template <int KIND, int R, int NJ>
+__global__ void __launch_bounds__(kGvWarps * 32, 2) gemv_rows_pipe_kernel(RowsParams P) {
+  const int per_slot = KIND == 0 ? P.I : (P.H + R - 1) / R;
+  const long long stride = static_cast<long long>(gridDim.x) * kGvWarps;
+  const long long item = static_cast<long long>(blockIdx.x) * kGvWarps + (threadIdx.x >> 5);
+  if (KIND == 1) prefetch_first_items<R, NJ>(P, per_slot, item, stride);
+  pdl_wait();
+  pdl_trigger();
+  rows_pipe_items<KIND, R, NJ>(P, item, stride, per_slot, static_cast<long long>(P.meta[0]) * per_slot);
+  if (KIND == 0 && P.rw_logits) route_weights_tail(P);
 }
 
 // ----------------------------------------------------------------------------
@@ -730,28 +785,34 @@ int sm_count() {
 
 // ----------------------------------------------------------------------------
 // Decode front in one block: route, bucket and the GEMV prep of a small batch
-// (T <= 4 tokens, E <= 1024 experts, A = T k <= 128), writing exactly what the
-// route, bucket and prep kernels write (same selection order, same weights bit
-// for bit, same stable bucket order, same slots and prescaled activations).
+// (T <= 4 tokens, E <= 1024 experts, A = T k <= 128), writing what the route,
+// bucket and prep kernels write (same selection order, same stable bucket order,
+// same slots and prescaled activations) but the routing weights, which the
+// gate/up kernel's last warps compute once their items are done
+// (route_weights_tail): only the combine reads them.
+//  * before the block waits for its predecessor it hints its inputs into L2:
+//    the logits and x rows and the four per-expert pointer arrays, which are cold
+//    after a step's weight stream (a prefetch returns nothing to the block, so it
+//    cannot let the block see a value that the predecessor has yet to write);
 //  * route: warp t takes token t with warp-level operations only: lane l holds
 //    the order-preserving keys of experts l, l + 32, ...; k rounds of a warp
 //    arg-max (two warp reductions each: the largest key, then the smallest
-//    index holding it) give the picks in (key desc, index asc) order (in place
-//    of a 32-step bit search for the k-th key, a tie pass and a rank pass), and
-//    the picked experts' four weight pointers are loaded right away and used
-//    after the softmax (in the bucketing phase they cost the decode step about
-//    4 us: the pointer arrays are cold after each step's weight stream),
-//    weighted with route_kernel's arithmetic (double exp over the picks,
-//    xor-butterfly sum); meanwhile warps 4..31 take the max |x| of row slices;
+//    index holding it) give the picks in (key desc, index asc) order, the
+//    winning lane finding its next best by a pairwise tree over its keys;
+//    meanwhile warps 4..31 take the presence flags of every expert (from its
+//    four weight pointers) and the max |x| of row slices;
 //  * bucket, by counting over the A <= 128 assignments: assignment a's place is
-//    #{a' : (idx[a'], a') < (idx[a], a)}, which sorts the experts; offsets and
-//    counts come from binary searches in the sorted experts;
+//    #{a' : (idx[a'], a') < (idx[a], a)}, which sorts the experts; meanwhile
+//    warps 4..31 write the x rows as prescaled f16; offsets and counts come
+//    from binary searches in the sorted experts;
 //  * prep: the first position of each expert writes its active slot (the number
-//    of distinct experts before it), then x rows to prescaled f16.
+//    of distinct experts before it).
 // Two block barriers in all.
 namespace {
 
 constexpr int kFrontMaxT = 4, kFrontMaxE = 1024, kFrontMaxA = 128;
+constexpr int kFrontKeys = kFrontMaxE / 32;            // keys per lane
+constexpr int kFrontAux = 1024 - 32 * kFrontMaxT;      // threads of warps 4..31
 
 __device__ __forceinline__ uint32_t front_key(float v) {  // -0 and +0 share a key; 0 = no expert
   uint32_t u = __float_as_uint(v);
@@ -759,123 +820,123 @@ __device__ __forceinline__ uint32_t front_key(float v) {  // -0 and +0 share a k
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// The largest of a lane's keys and the lowest slot holding it, by a pairwise
+// tree whose ties keep the left (lower) slot: five levels instead of a chain of
+// 32 dependent compares.
+__device__ __forceinline__ void lane_best(const uint32_t (&key)[kFrontKeys], uint32_t &kb, int &ib) {
+  uint32_t v[kFrontKeys / 2];
+  int ix[kFrontKeys / 2];
+#pragma unroll
+  for (int i = 0; i < kFrontKeys / 2; ++i) {
+    const bool r = key[2 * i + 1] > key[2 * i];
+    v[i] = r ? key[2 * i + 1] : key[2 * i];
+    ix[i] = r ? 2 * i + 1 : 2 * i;
+  }
+#pragma unroll
+  for (int n = kFrontKeys / 4; n >= 1; n >>= 1) {
+#pragma unroll
+    for (int i = 0; i < n; ++i) {  // in place: node i reads 2i and 2i + 1, both >= i
+      const bool r = v[2 * i + 1] > v[2 * i];
+      v[i] = r ? v[2 * i + 1] : v[2 * i];
+      ix[i] = r ? ix[2 * i + 1] : ix[2 * i];
+    }
+  }
+  kb = v[0];
+  ib = ix[0];
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(1024)
     layer_front_kernel(const float *__restrict__ logits, const uint16_t *__restrict__ x, k3moe_weights w, int T,
-                       int H, int E, int k, int32_t *__restrict__ idx, float *__restrict__ wts,
-                       int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int32_t *__restrict__ perm,
-                       int32_t *__restrict__ inv, int4 *__restrict__ slots, int32_t *__restrict__ meta,
-                       int32_t *__restrict__ xexp, uint4 *__restrict__ x16, int32_t *status) {
+                       int H, int E, int k, int32_t *__restrict__ idx, int32_t *__restrict__ counts,
+                       int32_t *__restrict__ offsets, int32_t *__restrict__ perm, int32_t *__restrict__ inv,
+                       int4 *__restrict__ slots, int32_t *__restrict__ meta, int32_t *__restrict__ xexp,
+                       uint4 *__restrict__ x16, int32_t *status) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  {  // L2 hints, one 128-byte line per thread and pass
+    const long long bl = 4LL * T * E, bx = 2LL * T * H, bp = 8LL * E;
+    const long long nl = (bl + 127) / 128, nx = (bx + 127) / 128, np = (bp + 127) / 128;
+    for (long long i = tid; i < nl + nx + 4 * np; i += 1024) {
+      const char *p;
+      if (i < nl) {
+        p = reinterpret_cast<const char *>(logits) + min(128 * i, bl - 1);
+      } else if (i < nl + nx) {
+        p = reinterpret_cast<const char *>(x) + min(128 * (i - nl), bx - 1);
+      } else {
+        const long long j = i - nl - nx, a = j / np, o = j - a * np;
+        const void *arr = a == 0 ? static_cast<const void *>(w.w13_codes)
+                          : a == 1 ? static_cast<const void *>(w.w13_scales)
+                          : a == 2 ? static_cast<const void *>(w.w2_codes)
+                                   : static_cast<const void *>(w.w2_scales);
+        p = reinterpret_cast<const char *>(arr) + min(128 * o, bp - 1);
+      }
+      prefetch_line_l2(p);
+    }
+  }
   pdl_wait();
   pdl_trigger();
   __shared__ int s_idx[kFrontMaxA];
   __shared__ int s_sorted[kFrontMaxA];
-  __shared__ int s_pres[kFrontMaxA], s_pres_sorted[kFrontMaxA];  // expert_flags per assignment / bucket position
-  __shared__ int s_xexp[kFrontMaxT];
+  __shared__ int s_pres_sorted[kFrontMaxA];  // expert_flags per bucket position
+  __shared__ unsigned char s_flag[kFrontMaxE];  // expert_flags per expert
   __shared__ float s_xpart[32];
-  __shared__ int s_oe[kFrontMaxT][32];
-  __shared__ float s_v[kFrontMaxT][32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int A = T * k;
-  // ---- phase A: warp t < T routes token t; warps 4..31 find the max |x| of row slices
+  // ---- phase A: warp t < T routes token t; warps 4..31 take the experts' flags
+  //      and the max |x| of row slices
   if (warp < T) {
     const int t = warp;
     const float *row = logits + static_cast<size_t>(t) * E;
-    uint32_t key[kFrontMaxE / 32];
+    uint32_t key[kFrontKeys];
     bool nan_here = false;
 #pragma unroll
-    for (int i = 0; i < kFrontMaxE / 32; ++i) {
+    for (int i = 0; i < kFrontKeys; ++i) {
       const int e = lane + 32 * i;
       float v = 0.f;
       if (e < E) v = __ldg(row + e);
       nan_here |= e < E && v != v;
       key[i] = e < E ? front_key(v) : 0u;  // 0: no expert (every real key is larger)
     }
-    if (__any_sync(0xFFFFFFFFu, nan_here)) {  // a NaN row: experts 0..k-1, weights 1/k
+    if (__any_sync(0xFFFFFFFFu, nan_here)) {  // a NaN row: experts 0..k-1 (weights 1/k)
       if (lane < k) {
         idx[t * k + lane] = lane;
-        wts[t * k + lane] = 1.0f / static_cast<float>(k);
         s_idx[t * k + lane] = lane;
-        s_pres[t * k + lane] = expert_flags(w.w13_codes[lane], w.w13_scales[lane], w.w2_codes[lane], w.w2_scales[lane]);
       }
       if (lane == 0) set_status(status, K3MOE_DEV_NONFINITE);
     } else {
       // the k picks in (key desc, index asc) order, one per round of a warp-wide
       // arg-max: the largest key by one warp reduction, then the smallest index
       // holding it by another; the winning lane drops that key and finds its
-      // next best.  A lane's best is its largest key at its smallest i (index
-      // lane + 32 i), and every expert e < E has a key above 0 (k <= E).  (Caching
-      // each lane's best two measured no faster than this rescan.)
-      uint32_t kb = 0u;
-      int ib = kFrontMaxE / 32;
-#pragma unroll
-      for (int i = 0; i < kFrontMaxE / 32; ++i)
-        if (key[i] > kb) {
-          kb = key[i];
-          ib = i;
-        }
+      // next best.  A lane's best is its largest key at its lowest slot i (index
+      // lane + 32 i); every expert e < E has a key above 0 (k <= E), so a lane
+      // whose keys are all 0 never matches the round's largest key.
+      uint32_t kb;
+      int ib;
+      lane_best(key, kb, ib);
       int pick = 0;
       for (int j = 0; j < k; ++j) {
         const uint32_t bk = __reduce_max_sync(0xFFFFFFFFu, kb);
-        const unsigned cand =
-            (kb == bk && ib < kFrontMaxE / 32) ? static_cast<unsigned>(lane + 32 * ib) : 0xFFFFFFFFu;
+        const unsigned cand = kb == bk ? static_cast<unsigned>(lane + 32 * ib) : 0xFFFFFFFFu;
         const unsigned be = __reduce_min_sync(0xFFFFFFFFu, cand);
         if (lane == j) pick = static_cast<int>(be);
         if (static_cast<int>(be & 31u) == lane) {
           const int rm = static_cast<int>(be >> 5);
-          kb = 0u;
-          ib = kFrontMaxE / 32;
 #pragma unroll
-          for (int i = 0; i < kFrontMaxE / 32; ++i) {
+          for (int i = 0; i < kFrontKeys; ++i)
             if (i == rm) key[i] = 0u;
-            if (key[i] > kb) {
-              kb = key[i];
-              ib = i;
-            }
-          }
+          lane_best(key, kb, ib);
         }
       }
-      // the picked experts' weight pointers are loaded now and used after the
-      // weights, so that their latency overlaps the softmax
-      const uint8_t *pa = nullptr, *pb = nullptr, *pc = nullptr, *pd = nullptr;
       if (lane < k) {
-        pa = w.w13_codes[pick];
-        pb = w.w13_scales[pick];
-        pc = w.w2_codes[pick];
-        pd = w.w2_scales[pick];
-      }
-      // weights with route_kernel's arithmetic
-      if (lane < k) {
-        s_oe[t][lane] = pick;
-        s_v[t][lane] = __ldg(row + pick);
-      }
-      __syncwarp();
-      const bool active = lane < k;
-      const float myv = active ? s_v[t][lane] : 0.f;
-      const float mx = s_v[t][0];
-      float wj;
-      if (mx == -INFINITY) {
-        wj = 1.0f / static_cast<float>(k);
-      } else if (mx == INFINITY) {
-        const int ninf = __popc(__ballot_sync(0xFFFFFFFFu, active && myv == INFINITY));
-        wj = (myv == INFINITY) ? 1.0f / static_cast<float>(ninf) : 0.0f;
-      } else {
-        const double ex = active ? exp(static_cast<double>(myv) - static_cast<double>(mx)) : 0.0;
-        double sum = ex;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
-        wj = static_cast<float>(ex / sum);
-      }
-      if (active) {
-        idx[t * k + lane] = s_oe[t][lane];
-        wts[t * k + lane] = wj;
-        s_idx[t * k + lane] = s_oe[t][lane];
-        s_pres[t * k + lane] = expert_flags(pa, pb, pc, pd);
+        idx[t * k + lane] = pick;
+        s_idx[t * k + lane] = pick;
       }
     }
   } else if (warp >= kFrontMaxT) {
-    // warps 4..31: partial max |x| of a slice of one token's row (16-byte loads)
+    for (int e = tid - 32 * kFrontMaxT; e < E; e += kFrontAux)
+      s_flag[e] = static_cast<unsigned char>(expert_flags(ldg_ptr(w.w13_codes, e), ldg_ptr(w.w13_scales, e),
+                                                          ldg_ptr(w.w2_codes, e), ldg_ptr(w.w2_scales, e)));
+    // partial max |x| of a slice of one token's row (16-byte loads)
     const int nw = 32 - kFrontMaxT, wpt = nw / T, wr = warp - kFrontMaxT;
     if (wr < wpt * T) {
       const int t = wr / wpt, part = wr % wpt;
@@ -896,7 +957,8 @@ __global__ void __launch_bounds__(1024)
     }
   }
   __syncthreads();
-  // ---- phase B: each assignment's place in (expert, assignment) order, the x prescale
+  // ---- phase B: each assignment's place in (expert, assignment) order (warps
+  //      0..3, as A <= 128); warps 4..31 write x as prescaled f16 (piece-major)
   if (tid < A) {
     const int e = s_idx[tid];
     int p = 0;
@@ -904,19 +966,29 @@ __global__ void __launch_bounds__(1024)
     perm[p] = tid;
     inv[tid] = p;
     s_sorted[p] = e;
-    s_pres_sorted[p] = s_pres[tid];
+    s_pres_sorted[p] = s_flag[e];
   }
-  if (tid < T) {
-    const int wpt = (32 - kFrontMaxT) / T;
-    float mx = 0.f;
-    for (int i = 0; i < wpt; ++i) mx = fmaxf(mx, s_xpart[tid * wpt + i]);
-    const int p = prescale_exp(mx);
-    s_xexp[tid] = p;
-    xexp[tid] = p;
+  if (warp >= kFrontMaxT) {
+    const int wpt = (32 - kFrontMaxT) / T, n8 = H / 8, nch = H / 32;
+    for (int i = tid - 32 * kFrontMaxT; i < T * n8; i += kFrontAux) {
+      const int t = i / n8, piece = i - t * n8;  // piece = c * 4 + q (source order)
+      float mx = 0.f;
+      for (int j = 0; j < wpt; ++j) mx = fmaxf(mx, s_xpart[t * wpt + j]);
+      const int pe = prescale_exp(mx);
+      if (piece == 0) xexp[t] = pe;
+      const float sc = scale_pow2(1.0f, -pe);
+      const uint4 v = __ldg(reinterpret_cast<const uint4 *>(x + static_cast<size_t>(t) * H) + piece);
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+        o[m] = pack_f16x2_scaled(__uint_as_float(u[m] << 16), __uint_as_float(u[m] & 0xFFFF0000u), sc);
+      x16[static_cast<size_t>(t) * n8 + (piece & 3) * nch + (piece >> 2)] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
   }
   __syncthreads();
   // ---- phase C: offsets and counts by binary search in the sorted experts,
-  //      active slots (first position of each expert), x rows to prescaled f16
+  //      active slots (first position of each expert)
   for (int e = tid; e <= E; e += 1024) {
     int lo = 0, hi = A;  // first position with expert >= e
     while (lo < hi) {
@@ -948,22 +1020,20 @@ __global__ void __launch_bounds__(1024)
     for (int p = 1; p < A; ++p) n += s_sorted[p] != s_sorted[p - 1];
     meta[0] = n;
   }
-  for (int t = 0; t < T; ++t)
-    row_to_f16_piece_major(x + static_cast<size_t>(t) * H, H, scale_pow2(1.0f, -s_xexp[t]),
-                           x16 + static_cast<size_t>(t) * (H / 8));
 }
 
 bool layer_front_fits(const k3moe_shape &s) {
   return s.T <= kFrontMaxT && s.E <= kFrontMaxE && s.T * s.k <= kFrontMaxA;
 }
 
-// route + bucket + GEMV prep in one block, then the GEMV kernels and the combine.
+// route + bucket + GEMV prep in one block, then the GEMV kernels (the gate/up
+// kernel also writes the routing weights) and the combine.
 int launch_layer_gemv_fast(const k3moe_shape &s, const float *logits, const uint16_t *x, const k3moe_weights &w,
                            int32_t *idx, float *wts, int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv,
                            float *Y, uint16_t *out, float *out_f32, void *ws, int32_t *status, cudaStream_t st) {
   if (s.T == 0) return 0;
   const GemvBufs b = gemv_bufs(s, ws);
-  if (launch_pdl(layer_front_kernel, dim3(1), dim3(1024), 0, st, logits, x, w, s.T, s.H, s.E, s.k, idx, wts, counts,
+  if (launch_pdl(layer_front_kernel, dim3(1), dim3(1024), 0, st, logits, x, w, s.T, s.H, s.E, s.k, idx, counts,
                  offsets, perm, inv, b.slots, b.meta, b.xexp, b.x16, status) != cudaSuccess)
     return -1;
   RowsParams P;
@@ -981,6 +1051,10 @@ int launch_layer_gemv_fast(const k3moe_shape &s, const float *logits, const uint
   P.hrow = b.hrow;
   P.Y = Y;
   P.status = status;
+  P.rw_logits = logits;
+  P.rw_idx = idx;
+  P.rw_w = wts;
+  P.rw_T = s.T;
   if (launch_rows(P, sm_count(), st, P.A, b.h16, b.hexp)) return -1;
   return launch_combine(s, Y, wts, inv, nullptr, out, out_f32, st);
 }
@@ -1006,6 +1080,10 @@ int launch_ffn_gemv(const k3moe_shape &s, const uint16_t *x, const k3moe_weights
   P.hrow = b.hrow;
   P.Y = Y;
   P.status = status;
+  P.rw_logits = nullptr;
+  P.rw_idx = nullptr;
+  P.rw_w = nullptr;
+  P.rw_T = 0;
   return launch_rows(P, sm_count(), st, P.A, b.h16, b.hexp);
 }
 
