@@ -19,7 +19,7 @@
 //   gemv_rows<0> item = (active slot u, row pair i): for each token p of u,
 //                h[p][i] = bf16(silu(Wg_i x_p) * (Wu_i x_p)), plain stores
 //   gemv_h16     h rows -> prescaled f16 (exponent from the row's max |h|)
-//   gemv_rows<1> item = (active slot u, 4 rows of W2): Y[p][rows] = W2 rows . h[p]
+//   gemv_rows<1> item = (active slot u, 4, 7 or 8 rows of W2): Y[p][rows] = W2 rows . h[p]
 //
 // Work is spread over warps, not blocks: warp w of the grid takes items w, w + W,
 // w + 2W, ... (W = warps in the grid).  An item is streamed in steps of B chunks
@@ -38,7 +38,7 @@ namespace k3moe {
 namespace {
 
 constexpr int kGvWarps = 8;   // warps per block
-constexpr int kDnRows = 4;    // W2 rows per down item
+constexpr int kDnRows = 4;    // W2 rows per down item (guarded kernel)
 
 // Workspace layout (byte offsets, 256-aligned pieces).
 struct GemvWs {
@@ -466,15 +466,32 @@ __global__ void __launch_bounds__(kGvWarps * 32, 2) gemv_rows_kernel(RowsParams 
 // warp keeps half an item in flight while it computes, with the registers of one
 // item.  Tokens are taken one at a time; with several tokens on an item the next
 // item's halves load during its last token.
-template <int R>
+// Gate/up (KIND 0) keeps a pointer per row (rows i and I + i).  The down rows of
+// an item are consecutive (the pipelined down kernel runs only when H is a
+// multiple of R, so every row of an item lies below H): one pointer per item, and
+// row r at a fixed stride from it, an immediate offset in the loads.
+template <int KIND, int R>
 struct ItemRows {
-  int4 sl;                    // slot record {expert, first position, tokens, present}
-  int rb;                     // row block of the item
-  const uint8_t *cr[R], *sr[R];  // the lane's first code chunk and scale byte of each row
+  static constexpr int NP = KIND == 1 ? 1 : R;
+  int4 sl;                      // slot record {expert, first position, tokens, present}
+  int rb;                       // row block of the item
+  const uint8_t *cr[NP], *sr[NP];  // the lane's first code chunk and scale byte of each row (or of row 0)
 };
 
 template <int KIND, int R, int NJ>
-__device__ __forceinline__ void item_rows_at(const RowsParams &P, long long item, int per_slot, ItemRows<R> &it) {
+__device__ __forceinline__ const uint8_t *row_codes(const ItemRows<KIND, R> &it, int r) {
+  if constexpr (KIND == 1) return it.cr[0] + r * (512 * NJ);
+  else return it.cr[r];
+}
+template <int KIND, int R, int NJ>
+__device__ __forceinline__ const uint8_t *row_scales(const ItemRows<KIND, R> &it, int r) {
+  if constexpr (KIND == 1) return it.sr[0] + r * (32 * NJ);
+  else return it.sr[r];
+}
+
+template <int KIND, int R, int NJ>
+__device__ __forceinline__ void item_rows_at(const RowsParams &P, long long item, int per_slot,
+                                             ItemRows<KIND, R> &it) {
   const int lane = threadIdx.x & 31;
   constexpr size_t cbytes = 512 * NJ, sbytes = 32 * NJ;  // K/2 and K/32 for K = 1024 * NJ
   it.sl = __ldg(P.slots + static_cast<int>(item / per_slot));
@@ -484,13 +501,17 @@ __device__ __forceinline__ void item_rows_at(const RowsParams &P, long long item
     cb = ldg_ptr(KIND == 0 ? P.w.w13_codes : P.w.w2_codes, it.sl.x);
     sb = ldg_ptr(KIND == 0 ? P.w.w13_scales : P.w.w2_scales, it.sl.x);
   }
+  if constexpr (KIND == 1) {
+    const int row = it.rb * R;
+    it.cr[0] = cb + row * cbytes + 16 * lane;
+    it.sr[0] = sb + row * sbytes + lane;
+  } else {
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
-    int row;
-    if (KIND == 0) row = r == 0 ? it.rb : P.I + it.rb;
-    else row = min(it.rb * R + r, P.H - 1);  // rows past H are computed (duplicates), not stored
-    it.cr[r] = cb + row * cbytes + 16 * lane;
-    it.sr[r] = sb + row * sbytes + lane;
+    for (int r = 0; r < R; ++r) {
+      const int row = r == 0 ? it.rb : P.I + it.rb;
+      it.cr[r] = cb + row * cbytes + 16 * lane;
+      it.sr[r] = sb + row * sbytes + lane;
+    }
   }
 }
 
@@ -508,42 +529,52 @@ __device__ __forceinline__ uint32_t ldg_u8_pf(const void *p) {
   return v;
 }
 
-template <int R, int J0, int NH>
-__device__ __forceinline__ void load_half(const ItemRows<R> &it, uint4 (&cw)[R][NH], uint32_t (&sc)[R][NH]) {
+template <int KIND, int R, int NJ, int J0, int NH>
+__device__ __forceinline__ void load_half(const ItemRows<KIND, R> &it, uint4 (&cw)[R][NH], uint32_t (&sc)[R][NH]) {
 #pragma unroll
   for (int j = 0; j < NH; ++j)
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      cw[r][j] = ldg_code_pf(it.cr[r] + 16 * 32 * (J0 + j));
-      sc[r][j] = ldg_u8_pf(it.sr[r] + 32 * (J0 + j));
+      cw[r][j] = ldg_code_pf(row_codes<KIND, R, NJ>(it, r) + 16 * 32 * (J0 + j));
+      sc[r][j] = ldg_u8_pf(row_scales<KIND, R, NJ>(it, r) + 32 * (J0 + j));
     }
 }
 
 // acc[r] += lane's share of row r . activation over chunks J0 .. J0 + NH - 1.
+// Rows are taken in groups of at most four (the activation words are loaded
+// again for each group), so that only a group's partial sums are live; each
+// row's sums are formed in the same order whatever the grouping.
 template <int R, int J0, int NH, int NCH>
 __device__ __forceinline__ void compute_half(const uint4 (&cw)[R][NH], const uint32_t (&sc)[R][NH],
                                              const uint4 *arow, float (&acc)[R]) {
+  constexpr int RG = R < 4 ? R : 4;
 #pragma unroll
   for (int j = 0; j < NH; ++j) {
-    float d0[R], d1[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) d0[r] = d1[r] = 0.f;
+    for (int g = 0; g < R; g += RG) {
+      float d0[RG], d1[RG];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint4 xv = __ldg(arow + q * NCH + 32 * (J0 + j));
+      for (int r = 0; r < RG; ++r) d0[r] = d1[r] = 0.f;
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        uint32_t wh[4];
-        const uint32_t word = q == 0 ? cw[r][j].x : q == 1 ? cw[r][j].y : q == 2 ? cw[r][j].z : cw[r][j].w;
-        e2m1x8_to_f16x2(word, wh);
-        d0[r] = fma2_f16_f32(wh[0], xv.x, d0[r]);
-        d1[r] = fma2_f16_f32(wh[1], xv.y, d1[r]);
-        d0[r] = fma2_f16_f32(wh[2], xv.z, d0[r]);
-        d1[r] = fma2_f16_f32(wh[3], xv.w, d1[r]);
+      for (int q = 0; q < 4; ++q) {
+        const uint4 xv = __ldg(arow + q * NCH + 32 * (J0 + j));
+#pragma unroll
+        for (int r = 0; r < RG; ++r) {
+          if (g + r >= R) break;  // the last group may be short
+          uint32_t wh[4];
+          const uint4 &c = cw[g + r][j];
+          const uint32_t word = q == 0 ? c.x : q == 1 ? c.y : q == 2 ? c.z : c.w;
+          e2m1x8_to_f16x2(word, wh);
+          d0[r] = fma2_f16_f32(wh[0], xv.x, d0[r]);
+          d1[r] = fma2_f16_f32(wh[1], xv.y, d1[r]);
+          d0[r] = fma2_f16_f32(wh[2], xv.z, d0[r]);
+          d1[r] = fma2_f16_f32(wh[3], xv.w, d1[r]);
+        }
       }
-    }
 #pragma unroll
-    for (int r = 0; r < R; ++r) acc[r] = fmaf(d0[r] + d1[r], e8m0_to_f32(sc[r][j]), acc[r]);
+      for (int r = 0; r < RG; ++r)
+        if (g + r < R) acc[g + r] = fmaf(d0[r] + d1[r], e8m0_to_f32(sc[g + r][j]), acc[g + r]);
+    }
   }
 }
 
@@ -587,18 +618,18 @@ __device__ __forceinline__ void rows_pipe_items(const RowsParams &P, long long i
   constexpr int NCH = 32 * NJ;  // chunks per row
   const int lane = threadIdx.x & 31;
   if (item >= nitems) return;
-  ItemRows<R> cur;
+  ItemRows<KIND, R> cur;
   item_rows_at<KIND, R, NJ>(P, item, per_slot, cur);
   uint4 ca[R][HA], cb[R][HB > 0 ? HB : 1];
   uint32_t sa[R][HA], sb[R][HB > 0 ? HB : 1];
   if (cur.sl.w) {
-    load_half<R, 0, HA>(cur, ca, sa);
-    if (HB > 0) load_half<R, HA, HB>(cur, cb, sb);
+    load_half<KIND, R, NJ, 0, HA>(cur, ca, sa);
+    if (HB > 0) load_half<KIND, R, NJ, HA, HB>(cur, cb, sb);
   }
   for (;;) {
     const long long nitem = item + stride;
     const bool has_next = nitem < nitems;
-    ItemRows<R> nxt;
+    ItemRows<KIND, R> nxt;
     if (has_next) item_rows_at<KIND, R, NJ>(P, nitem, per_slot, nxt);
     const bool pf = has_next && nxt.sl.w;
     for (int t = 0; t < cur.sl.z; ++t) {
@@ -619,10 +650,10 @@ __device__ __forceinline__ void rows_pipe_items(const RowsParams &P, long long i
 #pragma unroll
       for (int r = 0; r < R; ++r) acc[r] = 0.f;
       if (cur.sl.w) compute_half<R, 0, HA, NCH>(ca, sa, arow, acc);
-      if (last && pf) load_half<R, 0, HA>(nxt, ca, sa);  // half A of the next item flies now
+      if (last && pf) load_half<KIND, R, NJ, 0, HA>(nxt, ca, sa);  // half A of the next item flies now
       if (HB > 0) {
         if (cur.sl.w) compute_half<R, HA, HB, NCH>(cb, sb, arow, acc);
-        if (last && pf) load_half<R, HA, HB>(nxt, cb, sb);
+        if (last && pf) load_half<KIND, R, NJ, HA, HB>(nxt, cb, sb);
       }
 #pragma unroll
       for (int r = 0; r < R; ++r)
@@ -693,9 +724,8 @@ cudaError_t launch_rows_kernel(const RowsParams &P, int nsm, cudaStream_t st) {
 }
 
 // One token.  Gate/up (2 rows): exact instances for K/32 = 32 * NJ with NJ in
-// {2, 4, 7}, else the guarded one holding 8 chunks per lane and row (several
-// segments past K = 8192).  Down (4 rows): 2 chunks per lane and row (exact for
-// K = 2048), more would not fit the registers.
+// {2, 4, 7}.  Down (7 or 8 consecutive rows): 2 chunks per lane and row (exact
+// for K = 2048).
 template <int KIND, int R, int NJ>
 cudaError_t launch_rows_pipe(const RowsParams &P, int nsm, cudaStream_t st) {
   static int nb = 0;
@@ -712,13 +742,18 @@ cudaError_t launch_rows_pipe(const RowsParams &P, int nsm, cudaStream_t st) {
 
 // Gate/up (2 rows): pipelined exact instances for K/32 = 32 * NJ with NJ in
 // {2, 4, 7}, else the guarded kernel holding 8 chunks per lane and row (several
-// segments past K = 8192).  Down (4 rows): the pipelined exact instance for
-// K = 2048, else the guarded kernel with 2 chunks per lane and row.
+// segments past K = 8192).  Down: the pipelined exact instance for K = 2048 (7 or
+// 8 rows per item), else the guarded kernel with 4 rows and 2 chunks per lane and
+// row.
 template <int KIND, int R>
 cudaError_t launch_rows_nt1(const RowsParams &P, int K, int nsm, cudaStream_t st) {
   const int nch = K / 32;
   if constexpr (KIND == 1) {
-    if (nch == 64) return launch_rows_pipe<KIND, R, 2>(P, nsm, st);
+    // the pipelined kernel takes 7 rows per item when 7 divides H (H = 7 x 1024 in
+    // the decode shape; 7 rows of codes fit the 128 registers, 8 spill ten words),
+    // else 8 (H is a multiple of 32): every row of an item lies below H
+    if (nch == 64 && P.H % 7 == 0) return launch_rows_pipe<KIND, 7, 2>(P, nsm, st);
+    if (nch == 64 && P.H % 8 == 0) return launch_rows_pipe<KIND, 8, 2>(P, nsm, st);
     return launch_rows_kernel<KIND, R, 1, 2, false>(P, nsm, st);
   } else {
     if (nch == 64) return launch_rows_pipe<KIND, R, 2>(P, nsm, st);
