@@ -63,9 +63,11 @@ def parse():
     p.add_argument("--calls-per-graph", type=int, default=8,
                    help="consecutive k3moe_layer calls (one per step, each on its own input set) per captured "
                         "graph, as a model's layers follow each other; 1 = one graph per step")
-    p.add_argument("--legs", default="all", choices=["all", "none"],
+    p.add_argument("--legs", default="all", choices=["all", "none", "router"],
                    help="also time the other workloads (batch8, speculative-verify batches, prefill, "
-                        "skewed, probe) into the line's workloads object")
+                        "skewed, probe) into the line's workloads object; router: the router entry point "
+                        "alone on the decode, batch8 and prefill tokens (its own 896 x 7168 router matrix, "
+                        "whatever --experts is)")
     p.add_argument("--leg-steps", type=int, default=20, help="timed steps per extra workload (at most --steps)")
     p.add_argument("--leg-cpu-seconds", type=float, default=2.0, help="oracle sample budget per extra workload")
     p.add_argument("--no-stack", action="store_true",
@@ -935,7 +937,7 @@ def run_gpu(a):
 
     # ------------------------------------------------------------- the other workloads
     workloads = None
-    legs = [] if a.legs == "none" or a.experts or a.tokens else LEGS
+    legs = [] if a.legs != "all" or a.experts or a.tokens else LEGS
     if legs and (s.H, s.I, s.E) != (7168, 2048, 896):
         legs = []
     if legs:
@@ -955,6 +957,8 @@ def run_gpu(a):
             del W, Wl, experts
             torch.cuda.empty_cache()
             workloads["stack92/decode_i1536_host_experts"] = run_stack_leg(a, dev, ws)
+    if a.legs == "router":
+        workloads = {f"router/{name}": run_router_leg(a, name, dev, ws, rank) for name in ("decode", "batch8", "prefill")}
     time.sleep(0.2)
     clk = clocks.stop()
     for ent in (workloads or {}).values():  # clocks seen during each workload's timed steps

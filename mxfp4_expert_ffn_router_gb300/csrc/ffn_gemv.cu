@@ -280,20 +280,7 @@ __device__ __forceinline__ void route_weights_tail(const RowsParams &P) {
     wj = 1.0f / static_cast<float>(k);
   } else {
     const int pick = active ? min(max(P.rw_idx[t * k + lane], 0), E - 1) : 0;
-    const float myv = active ? __ldg(row + pick) : 0.f;
-    const float mx = __shfl_sync(0xFFFFFFFFu, myv, 0);  // the first pick holds the largest logit
-    if (mx == -INFINITY) {
-      wj = 1.0f / static_cast<float>(k);
-    } else if (mx == INFINITY) {
-      const int ninf = __popc(__ballot_sync(0xFFFFFFFFu, active && myv == INFINITY));
-      wj = (myv == INFINITY) ? 1.0f / static_cast<float>(ninf) : 0.0f;
-    } else {
-      const double ex = active ? exp(static_cast<double>(myv) - static_cast<double>(mx)) : 0.0;
-      double sum = ex;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
-      wj = static_cast<float>(ex / sum);
-    }
+    wj = warp_route_weight(active ? __ldg(row + pick) : 0.f, k);  // the first pick holds the largest logit
   }
   if (active) P.rw_w[t * k + lane] = wj;
 }
@@ -849,37 +836,6 @@ constexpr int kFrontMaxT = 4, kFrontMaxE = 1024, kFrontMaxA = 128;
 constexpr int kFrontKeys = kFrontMaxE / 32;            // keys per lane
 constexpr int kFrontAux = 1024 - 32 * kFrontMaxT;      // threads of warps 4..31
 
-__device__ __forceinline__ uint32_t front_key(float v) {  // -0 and +0 share a key; 0 = no expert
-  uint32_t u = __float_as_uint(v);
-  if (u == 0x80000000u) u = 0u;
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// The largest of a lane's keys and the lowest slot holding it, by a pairwise
-// tree whose ties keep the left (lower) slot: five levels instead of a chain of
-// 32 dependent compares.
-__device__ __forceinline__ void lane_best(const uint32_t (&key)[kFrontKeys], uint32_t &kb, int &ib) {
-  uint32_t v[kFrontKeys / 2];
-  int ix[kFrontKeys / 2];
-#pragma unroll
-  for (int i = 0; i < kFrontKeys / 2; ++i) {
-    const bool r = key[2 * i + 1] > key[2 * i];
-    v[i] = r ? key[2 * i + 1] : key[2 * i];
-    ix[i] = r ? 2 * i + 1 : 2 * i;
-  }
-#pragma unroll
-  for (int n = kFrontKeys / 4; n >= 1; n >>= 1) {
-#pragma unroll
-    for (int i = 0; i < n; ++i) {  // in place: node i reads 2i and 2i + 1, both >= i
-      const bool r = v[2 * i + 1] > v[2 * i];
-      v[i] = r ? v[2 * i + 1] : v[2 * i];
-      ix[i] = r ? ix[2 * i + 1] : ix[2 * i];
-    }
-  }
-  kb = v[0];
-  ib = ix[0];
-}
-
 }  // namespace
 
 __global__ void __launch_bounds__(1024)
@@ -930,7 +886,7 @@ __global__ void __launch_bounds__(1024)
       float v = 0.f;
       if (e < E) v = __ldg(row + e);
       nan_here |= e < E && v != v;
-      key[i] = e < E ? front_key(v) : 0u;  // 0: no expert (every real key is larger)
+      key[i] = e < E ? order_key(v) : 0u;  // 0: no expert (every real key is larger)
     }
     if (__any_sync(0xFFFFFFFFu, nan_here)) {  // a NaN row: experts 0..k-1 (weights 1/k)
       if (lane < k) {
@@ -939,29 +895,9 @@ __global__ void __launch_bounds__(1024)
       }
       if (lane == 0) set_status(status, K3MOE_DEV_NONFINITE);
     } else {
-      // the k picks in (key desc, index asc) order, one per round of a warp-wide
-      // arg-max: the largest key by one warp reduction, then the smallest index
-      // holding it by another; the winning lane drops that key and finds its
-      // next best.  A lane's best is its largest key at its lowest slot i (index
-      // lane + 32 i); every expert e < E has a key above 0 (k <= E), so a lane
-      // whose keys are all 0 never matches the round's largest key.
-      uint32_t kb;
-      int ib;
-      lane_best(key, kb, ib);
-      int pick = 0;
-      for (int j = 0; j < k; ++j) {
-        const uint32_t bk = __reduce_max_sync(0xFFFFFFFFu, kb);
-        const unsigned cand = kb == bk ? static_cast<unsigned>(lane + 32 * ib) : 0xFFFFFFFFu;
-        const unsigned be = __reduce_min_sync(0xFFFFFFFFu, cand);
-        if (lane == j) pick = static_cast<int>(be);
-        if (static_cast<int>(be & 31u) == lane) {
-          const int rm = static_cast<int>(be >> 5);
-#pragma unroll
-          for (int i = 0; i < kFrontKeys; ++i)
-            if (i == rm) key[i] = 0u;
-          lane_best(key, kb, ib);
-        }
-      }
+      // the k picks in (key desc, index asc) order (warp_top_k: one warp arg-max
+      // per pick); every expert e < E has a key above 0 and k <= E
+      const int pick = warp_top_k<kFrontKeys>(key, k);
       if (lane < k) {
         idx[t * k + lane] = pick;
         s_idx[t * k + lane] = pick;

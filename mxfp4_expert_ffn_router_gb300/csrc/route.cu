@@ -1,4 +1,4 @@
-// route.cu -- router top-k selection and softmax weights (one block per token).
+// route.cu -- router top-k selection and softmax weights.
 //
 // Follows the kimi-k3-in-c CHANGELOG walkthrough, "[0.1.0] Added": each MoE
 // layer routes a token to 16 of 896 experts; the score is the softmax of the
@@ -6,26 +6,21 @@
 // fp32 logits (exact comparisons), ties go to the lower expert index.
 //
 // Per token: each logit becomes an order-preserving unsigned key (-0 and +0 the
-// same key).  A 32-step bitwise search finds tau, the largest key with at least
-// k keys >= tau (the k-th largest key); every key > tau is selected, and keys
-// equal to tau are selected in index order until k are taken.  The k picks are
-// ordered by (key descending, index ascending) and their weights are
-// exp(l - m) / sum exp(l - m) over the picks, in double.
+// same key).  The k picks are ordered by (key descending, index ascending) and
+// their weights are exp(l - m) / sum exp(l - m) over the picks, in double.
+//  * E <= 1024: one warp per token holds the keys (lane l: experts l, l + 32, ...)
+//    and takes the picks by k rounds of a warp arg-max (warp_top_k);
+//  * larger E: one block per token; a 32-step bitwise search finds tau, the
+//    largest key with at least k keys >= tau (the k-th largest key); every key
+//    > tau is selected, and keys equal to tau are selected in index order until
+//    k are taken.
+// Both give the same picks and weights bit for bit.
 #include "k3moe_dev.cuh"
 #include "k3moe_launch.h"
 
 namespace k3moe {
 
 namespace {
-
-// Order-preserving key of an fp32 value (larger value -> larger key; -0 -> +0).
-// Keys of finite and infinite values are >= 0x007FFFFF (the key of -inf), so 0
-// marks a padding slot that is never selected.
-__device__ __forceinline__ uint32_t sort_key(float v) {
-  uint32_t u = __float_as_uint(v);
-  if (u == 0x80000000u) u = 0u;
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
 
 // Sum of one int per thread over the block (all threads get it).  `buf` holds 32
 // ints; consecutive calls must alternate buffers (the second barrier of a call
@@ -70,7 +65,7 @@ __global__ void __launch_bounds__(1024) route_kernel(const float *__restrict__ l
     if (e < E) {
       val[i] = __ldg(row + e);
       if (val[i] != val[i]) nan_here = true;
-      key[i] = sort_key(val[i]);
+      key[i] = order_key(val[i]);
     }
   }
   if (tid == 0) s_n = 0;
@@ -142,29 +137,73 @@ __global__ void __launch_bounds__(1024) route_kernel(const float *__restrict__ l
   }
   __syncthreads();
   if (tid < 32) {  // weights over the k picks; exp and the normalisation in double
-    const bool active = lane < k;
-    const float my_v = active ? s_sorted[lane] : 0.f;
-    const float m = s_sorted[0];
-    float wj;
-    if (m == -INFINITY) {
-      wj = 1.0f / static_cast<float>(k);
-    } else if (m == INFINITY) {
-      const int ninf = __popc(__ballot_sync(0xFFFFFFFFu, active && my_v == INFINITY));
-      wj = (my_v == INFINITY) ? 1.0f / static_cast<float>(ninf) : 0.0f;
-    } else {
-      const double ex = active ? exp(static_cast<double>(my_v) - static_cast<double>(m)) : 0.0;
-      double sum = ex;
+    const float wj = warp_route_weight(lane < k ? s_sorted[lane] : 0.f, k);
+    if (lane < k) wt[lane] = wj;
+  }
+}
+
+// One warp per token, E <= 32 NK: lane l holds the keys of experts l, l + 32, ...
+// (0 past E); a row holding a NaN takes experts 0..k-1 with weights 1/k and is
+// reported, as in route_kernel.
+template <int NK>
+__global__ void __launch_bounds__(256) route_warp_kernel(const float *__restrict__ logits, int T, int E, int k,
+                                                         int32_t *__restrict__ idx, float *__restrict__ w,
+                                                         int32_t *status) {
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const long long t = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;  // the whole warp
+  const float *row = logits + t * E;
+  uint32_t key[NK];
+  bool nan_here = false;
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
-      wj = static_cast<float>(ex / sum);
+  for (int i = 0; i < NK; ++i) {
+    const int e = lane + 32 * i;
+    float v = 0.f;
+    if (e < E) v = __ldg(row + e);
+    nan_here |= e < E && v != v;
+    key[i] = e < E ? order_key(v) : 0u;
+  }
+  int32_t *it = idx + t * k;
+  float *wt = w + t * k;
+  if (__any_sync(0xFFFFFFFFu, nan_here)) {
+    if (lane < k) {
+      it[lane] = lane;
+      wt[lane] = 1.0f / static_cast<float>(k);
     }
-    if (active) wt[lane] = wj;
+    if (lane == 0) set_status(status, K3MOE_DEV_NONFINITE);
+    return;
+  }
+  const int pick = warp_top_k<NK>(key, k);
+  const float wj = warp_route_weight(lane < k ? __ldg(row + pick) : 0.f, k);
+  if (lane < k) {
+    it[lane] = pick;
+    wt[lane] = wj;
   }
 }
 
 int launch_route(const k3moe_shape &s, const float *logits, int32_t *idx, float *w,
                  int32_t *status, cudaStream_t st) {
   if (s.T == 0) return 0;
+  if (s.E <= 1024) {  // a warp per token, 8 tokens per block
+    const dim3 grid(static_cast<unsigned>((s.T + 7) / 8)), block(256);
+    const int nk = (s.E + 31) / 32;
+    cudaError_t err;
+    if (nk <= 1)
+      err = launch_pdl(route_warp_kernel<1>, grid, block, 0, st, logits, s.T, s.E, s.k, idx, w, status);
+    else if (nk <= 2)
+      err = launch_pdl(route_warp_kernel<2>, grid, block, 0, st, logits, s.T, s.E, s.k, idx, w, status);
+    else if (nk <= 4)
+      err = launch_pdl(route_warp_kernel<4>, grid, block, 0, st, logits, s.T, s.E, s.k, idx, w, status);
+    else if (nk <= 8)
+      err = launch_pdl(route_warp_kernel<8>, grid, block, 0, st, logits, s.T, s.E, s.k, idx, w, status);
+    else if (nk <= 16)
+      err = launch_pdl(route_warp_kernel<16>, grid, block, 0, st, logits, s.T, s.E, s.k, idx, w, status);
+    else
+      err = launch_pdl(route_warp_kernel<32>, grid, block, 0, st, logits, s.T, s.E, s.k, idx, w, status);
+    return err == cudaSuccess ? 0 : -1;
+  }
   const int nth = s.E >= 1024 ? 1024 : ((s.E + 31) / 32) * 32;
   const int per = (s.E + nth - 1) / nth;  // <= 4 for E <= 4096
   const dim3 grid(s.T), block(nth);
