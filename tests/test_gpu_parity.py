@@ -277,6 +277,27 @@ def test_maximum_experts_and_k():
     _full_check(s, logits, xbits, experts, r)
 
 
+@pytest.mark.parametrize("E,k", [(100, 8), (200, 16), (512, 32), (1000, 16), (1024, 32), (1025, 16), (2000, 5)])
+def test_route_every_keys_per_lane_instance(E, k):
+    """The route's instances: a warp per token for E <= 1024 (4, 8, 16 and 32 keys
+    per lane here), the block search above it; 37 tokens (several blocks of 8 warps
+    and a ragged tail) with rows of ties, signed zeros, infinities and a NaN row."""
+    T = 37
+    s = gen.Shape(T, 64, 32, E, k)
+    logits = np.random.default_rng(E).standard_normal((T, E)).astype(np.float32)
+    logits[1] = np.round(logits[1])            # many ties at each value
+    logits[2] = 0.0
+    logits[2, ::3] = -0.0                      # all equal, signed zeros
+    logits[3, [5, E - 1]] = np.inf             # two +inf picks share the weight
+    logits[4] = -np.inf                        # all -inf: weights 1/k
+    logits[5, E // 2] = np.nan                 # NaN row: experts 0..k-1, flagged
+    b = alloc_layer(s, with_f32=False)
+    k3.k3moe_route(s, torch.from_numpy(logits).cuda(), b["idx"], b["w"], b["status"])
+    r = host(b)
+    _check_route(s, logits, r)
+    assert r["status"][0] == k3.K3MOE_DEV_NONFINITE
+
+
 def test_large_bucket_multi_tile_bit_exact():
     s = gen.Shape(5000, 32, 32, 300, 7)  # A = 35000: the tiled bucketing path
     rng = np.random.default_rng(4)
