@@ -446,13 +446,12 @@ __global__ void __launch_bounds__(kGvWarps * 32, 2) gemv_rows_kernel(RowsParams 
 }
 
 // ----------------------------------------------------------------------------
-// Exact shapes (K = 1024 * NJ), software-pipelined over half items: a lane's NJ
-// chunks per row are split into halves A (HA chunks) and B (NJ - HA).  While half
-// B of item i is computed, half A of the warp's next item is already loading,
-// and half B of the next item loads while the warp finishes item i; so every
-// warp keeps half an item in flight while it computes, with the registers of one
-// item.  Tokens are taken one at a time; with several tokens on an item the next
-// item's halves load during its last token.
+// Exact shapes (K = 1024 * NJ), software-pipelined chunk by chunk: a lane holds
+// its NJ chunks per row of one item in registers; as soon as chunk j of item i has
+// been computed, chunk j of the warp's next item is loaded into its registers, so
+// while the warp computes it keeps the rest of item i and the start of item i + 1
+// in flight, with the registers of one item.  Tokens are taken one at a time; with
+// several tokens on an item the next item's chunks load during its last token.
 // Gate/up (KIND 0) keeps a pointer per row (rows i and I + i).  The down rows of
 // an item are consecutive (the pipelined down kernel runs only when H is a
 // multiple of R, so every row of an item lies below H): one pointer per item, and
@@ -516,14 +515,16 @@ __device__ __forceinline__ uint32_t ldg_u8_pf(const void *p) {
   return v;
 }
 
+// Chunks J0 .. J0 + NH - 1 of an item's rows into registers (the lane's 16-byte
+// code chunk and scale byte of each row and chunk), in program order.
 template <int KIND, int R, int NJ, int J0, int NH>
-__device__ __forceinline__ void load_half(const ItemRows<KIND, R> &it, uint4 (&cw)[R][NH], uint32_t (&sc)[R][NH]) {
+__device__ __forceinline__ void load_span(const ItemRows<KIND, R> &it, uint4 (&cw)[R][NJ], uint32_t (&sc)[R][NJ]) {
 #pragma unroll
   for (int j = 0; j < NH; ++j)
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      cw[r][j] = ldg_code_pf(row_codes<KIND, R, NJ>(it, r) + 16 * 32 * (J0 + j));
-      sc[r][j] = ldg_u8_pf(row_scales<KIND, R, NJ>(it, r) + 32 * (J0 + j));
+      cw[r][J0 + j] = ldg_code_pf(row_codes<KIND, R, NJ>(it, r) + 16 * 32 * (J0 + j));
+      sc[r][J0 + j] = ldg_u8_pf(row_scales<KIND, R, NJ>(it, r) + 32 * (J0 + j));
     }
 }
 
@@ -531,12 +532,12 @@ __device__ __forceinline__ void load_half(const ItemRows<KIND, R> &it, uint4 (&c
 // Rows are taken in groups of at most four (the activation words are loaded
 // again for each group), so that only a group's partial sums are live; each
 // row's sums are formed in the same order whatever the grouping.
-template <int R, int J0, int NH, int NCH>
-__device__ __forceinline__ void compute_half(const uint4 (&cw)[R][NH], const uint32_t (&sc)[R][NH],
+template <int R, int NJ, int J0, int NH, int NCH>
+__device__ __forceinline__ void compute_span(const uint4 (&cw)[R][NJ], const uint32_t (&sc)[R][NJ],
                                              const uint4 *arow, float (&acc)[R]) {
   constexpr int RG = R < 4 ? R : 4;
 #pragma unroll
-  for (int j = 0; j < NH; ++j) {
+  for (int j = J0; j < J0 + NH; ++j) {
 #pragma unroll
     for (int g = 0; g < R; g += RG) {
       float d0[RG], d1[RG];
@@ -544,7 +545,7 @@ __device__ __forceinline__ void compute_half(const uint4 (&cw)[R][NH], const uin
       for (int r = 0; r < RG; ++r) d0[r] = d1[r] = 0.f;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const uint4 xv = __ldg(arow + q * NCH + 32 * (J0 + j));
+        const uint4 xv = __ldg(arow + q * NCH + 32 * j);
 #pragma unroll
         for (int r = 0; r < RG; ++r) {
           if (g + r >= R) break;  // the last group may be short
@@ -562,6 +563,24 @@ __device__ __forceinline__ void compute_half(const uint4 (&cw)[R][NH], const uin
       for (int r = 0; r < RG; ++r)
         if (g + r < R) acc[g + r] = fmaf(d0[r] + d1[r], e8m0_to_f32(sc[g + r][j]), acc[g + r]);
     }
+  }
+}
+
+// Spans of PS chunks from chunk J on: each is computed from the registers, then,
+// when the warp moves on to the next item after this token, the same chunks of the
+// next item are loaded into those registers.  While a span is computed, the rest
+// of the item and the next item's earlier spans are in flight: with PS = 1 about
+// NJ - 1 of the NJ chunks of a row, and each load has most of an item's compute
+// time to arrive.  The chunks are summed in the same order whatever PS is.
+template <int KIND, int R, int NJ, int NCH, int PS, int J>
+__device__ __forceinline__ void spans_from(const ItemRows<KIND, R> &nxt, bool present, bool reload,
+                                          uint4 (&cw)[R][NJ], uint32_t (&sc)[R][NJ], const uint4 *arow,
+                                          float (&acc)[R]) {
+  if constexpr (J < NJ) {
+    constexpr int NH = NJ - J < PS ? NJ - J : PS;
+    if (present) compute_span<R, NJ, J, NH, NCH>(cw, sc, arow, acc);
+    if (reload) load_span<KIND, R, NJ, J, NH>(nxt, cw, sc);
+    spans_from<KIND, R, NJ, NCH, PS, J + NH>(nxt, present, reload, cw, sc, arow, acc);
   }
 }
 
@@ -597,22 +616,21 @@ __device__ __forceinline__ void prefetch_first_items(const RowsParams &P, int pe
   }
 }
 
+// Chunks per span of the software pipeline (spans_from).
+constexpr int kSpanChunks = 1;
+
 // The warp's items item, item + stride, ... below nitems.
 template <int KIND, int R, int NJ>
 __device__ __forceinline__ void rows_pipe_items(const RowsParams &P, long long item, long long stride, int per_slot,
                                                 long long nitems) {
-  constexpr int HA = (NJ + 1) / 2, HB = NJ - HA;
   constexpr int NCH = 32 * NJ;  // chunks per row
   const int lane = threadIdx.x & 31;
   if (item >= nitems) return;
   ItemRows<KIND, R> cur;
   item_rows_at<KIND, R, NJ>(P, item, per_slot, cur);
-  uint4 ca[R][HA], cb[R][HB > 0 ? HB : 1];
-  uint32_t sa[R][HA], sb[R][HB > 0 ? HB : 1];
-  if (cur.sl.w) {
-    load_half<KIND, R, NJ, 0, HA>(cur, ca, sa);
-    if (HB > 0) load_half<KIND, R, NJ, HA, HB>(cur, cb, sb);
-  }
+  uint4 cw[R][NJ];
+  uint32_t sc[R][NJ];
+  if (cur.sl.w) load_span<KIND, R, NJ, 0, NJ>(cur, cw, sc);
   for (;;) {
     const long long nitem = item + stride;
     const bool has_next = nitem < nitems;
@@ -636,12 +654,7 @@ __device__ __forceinline__ void rows_pipe_items(const RowsParams &P, long long i
       float acc[R];
 #pragma unroll
       for (int r = 0; r < R; ++r) acc[r] = 0.f;
-      if (cur.sl.w) compute_half<R, 0, HA, NCH>(ca, sa, arow, acc);
-      if (last && pf) load_half<KIND, R, NJ, 0, HA>(nxt, ca, sa);  // half A of the next item flies now
-      if (HB > 0) {
-        if (cur.sl.w) compute_half<R, HA, HB, NCH>(cb, sb, arow, acc);
-        if (last && pf) load_half<KIND, R, NJ, HA, HB>(nxt, cb, sb);
-      }
+      spans_from<KIND, R, NJ, NCH, kSpanChunks, 0>(nxt, cur.sl.w != 0, last && pf, cw, sc, arow, acc);
 #pragma unroll
       for (int r = 0; r < R; ++r)
 #pragma unroll
