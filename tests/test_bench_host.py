@@ -128,3 +128,16 @@ def test_layer_kernel_count(bench):
     assert bench.layer_kernel_count(gen.CONFIGS["spec12"], 0) == 1 + 1 + 4 + 1
     assert bench.layer_kernel_count(gen.CONFIGS["prefill"], 0) == 1 + 3 + 6 + 1
     assert bench.layer_kernel_count(gen.CONFIGS["batch8"], 3) == 1 + 1 + 6 + 1
+
+
+def test_legs_option(bench, monkeypatch):
+    """--legs router times the router entry point alone (its own router matrix, so it
+    runs beside a small expert set); the default times every workload."""
+    monkeypatch.setattr("sys.argv", ["bench.py", "--legs", "router", "--experts", "64"])
+    a = bench.parse()
+    assert a.legs == "router" and a.experts == 64
+    monkeypatch.setattr("sys.argv", ["bench.py"])
+    assert bench.parse().legs == "all"
+    monkeypatch.setattr("sys.argv", ["bench.py", "--legs", "some"])
+    with pytest.raises(SystemExit):
+        bench.parse()
